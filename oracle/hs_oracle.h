@@ -1,0 +1,77 @@
+/*
+ * hs_oracle.h -- plain single-threaded CPU oracle for the HiSparse KV-row
+ * swap-in and the indexed KV-row movers.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may include, link or
+ * call this library: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header or constant generator with
+ * the CUDA path; the status-bit values below restate the public interface.
+ *
+ * Every pointer here is a HOST pointer.  Floating point never occurs: the
+ * method moves bytes and does integer bookkeeping ("The kernels only move
+ * bytes; they are dtype agnostic", vLLM csrc/libtorch_stable/hisparse_kernels.cu,
+ * file header).
+ */
+#ifndef HS_ORACLE_H
+#define HS_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Per-row status bits (restated from the public interface). */
+#define HSO_ST_DUP_ID 1
+#define HSO_ST_BAD_POOL_ROW 2
+#define HSO_ST_BAD_LRU_SLOT 4
+#define HSO_ST_BAD_HOT_ROW 8
+#define HSO_ST_TIMEOUT 16
+#define HSO_ST_BAD_STATE 32
+#define HSO_ST_BAD_INDEX 64
+
+typedef struct hso_swap_in_args {
+  int32_t batch;    /* B */
+  int32_t top_k;    /* K */
+  int32_t hot_size; /* H: LRU-managed slots [0,H); slot H holds the newest token */
+  int32_t num_real; /* rows b >= num_real are padding; -1 means all rows are real */
+  const int32_t* topk_ids; int64_t topk_stride;        /* [B, K] */
+  const int64_t* seq_lens;                              /* [B] */
+  const int64_t* req_state;                             /* [B] state row per batch row */
+  int64_t num_states;                                   /* R */
+  int32_t* slot_tokens; int64_t slot_tokens_stride;     /* [R, >=H+1] in/out */
+  const int32_t* slot_rows; int64_t slot_rows_stride;   /* [R, >=H+1] */
+  int16_t* lru; int64_t lru_stride;                     /* [R, >=H] in/out */
+  const int64_t* pool_rows; int64_t pool_rows_stride; int64_t pool_rows_cols; /* [R, cols] */
+  const uint8_t* pool_k; const uint8_t* pool_v; int64_t pool_num_rows;       /* pool_v may be NULL */
+  uint8_t* hot_k; uint8_t* hot_v; int64_t hot_num_rows;                      /* hot_v NULL iff pool_v NULL */
+  int64_t row_bytes;                                    /* S */
+  int32_t* out_rows; int64_t out_stride;                /* [B, K] */
+  int32_t* miss_count;                                  /* [B] or NULL */
+  uint64_t* stats;                                      /* [2] accumulated, or NULL */
+  int32_t* status;                                      /* [B] or NULL */
+} hso_swap_in_args;
+
+/* Returns 0, or -1 when an argument is unusable (the oracle does not try to
+ * mirror every synchronous check of the CUDA library). */
+int hso_swap_in(const hso_swap_in_args* a);
+
+/* dst_k[loc[t]] = k_src[t] (and V), tokens in order; loc out of [0,dst_rows)
+ * is skipped with HSO_ST_BAD_INDEX OR-ed into *status. */
+int hso_store_kv(const uint8_t* k_src, const uint8_t* v_src, int64_t src_k_stride,
+                 int64_t src_v_stride, uint8_t* k_dst, uint8_t* v_dst, int64_t dst_stride,
+                 int64_t dst_rows, const int64_t* loc, int64_t n_tokens, int64_t row_bytes,
+                 int32_t* status);
+
+/* For n in order, for each of the num_layers*(1+has_v) pointer pairs p:
+ * dst_ptrs[p] row dst_idx[n] = src_ptrs[p] row src_idx[n].  Out-of-range
+ * indices skip the pair with HSO_ST_BAD_INDEX. */
+int hso_transfer_kv(const uint64_t* src_ptrs, const uint64_t* dst_ptrs, int32_t num_layers,
+                    int32_t has_v, const int64_t* src_idx, const int64_t* dst_idx, int64_t n,
+                    int64_t src_stride, int64_t dst_stride, int64_t src_rows, int64_t dst_rows,
+                    int64_t row_bytes, int32_t* status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HS_ORACLE_H */
