@@ -1,0 +1,219 @@
+/*
+ * hisparse.h -- C ABI of libhisparse: the HiSparse decode-time KV-row swap-in
+ * and the indexed KV-row movers, as hand-written CUDA kernels for GB300
+ * (sm_103a).
+ *
+ * Conventions shared by every entry point
+ *  - All calls are asynchronous and stream-ordered on `stream` (a CUDA runtime
+ *    stream handle; NULL is the legacy default stream).  The library owns no
+ *    memory, allocates nothing, and keeps no state between calls beyond a
+ *    once-per-process kernel attribute set-up.
+ *  - "device" pointers must be readable/writable by the GPU: device memory
+ *    (or managed memory).  Pool pointers may also be pinned host memory
+ *    (cudaHostAlloc / cudaHostRegister), read over the host link.
+ *  - The synchronous return value covers argument errors and launch errors
+ *    (hs_err).  Problems found in the data while the kernel runs are reported
+ *    through optional per-row or per-call status words (HS_ST_* bits).
+ *  - On any non-HS_OK return, hs_last_error() holds a message for the calling
+ *    thread.  Empty work (batch == 0, top_k == 0, n == 0) returns HS_OK and
+ *    launches nothing.
+ *  - No floating point is involved: rows are opaque bytes.
+ */
+#ifndef HISPARSE_H
+#define HISPARSE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA runtime stream (cudaStream_t has this exact type). */
+typedef struct CUstream_st* hs_stream_t;
+
+typedef enum hs_err {
+  HS_OK = 0,
+  HS_ERR_ARG = 1,         /* a pointer, size, stride or memory type is unusable */
+  HS_ERR_UNSUPPORTED = 2, /* valid, but outside what this build supports */
+  HS_ERR_CUDA = 3         /* a CUDA runtime call or the launch failed */
+} hs_err;
+
+/* Status bits written by the kernels (0 = clean). */
+#define HS_ST_DUP_ID 1        /* a valid id repeated within a row: later copies got -1 */
+#define HS_ST_BAD_POOL_ROW 2  /* a miss's pool row was outside [0, pool_num_rows): -1, not a miss */
+#define HS_ST_BAD_LRU_SLOT 4  /* an LRU entry was outside [0, hot_size) or repeated a slot */
+#define HS_ST_BAD_HOT_ROW 8   /* a miss's hot row was outside [0, hot_num_rows): -1, no copy */
+#define HS_ST_TIMEOUT 16      /* a bounded wait inside a kernel gave up */
+#define HS_ST_BAD_STATE 32    /* req_state[b] >= num_states: row emitted -1 */
+#define HS_ST_BAD_INDEX 64    /* a mover index was out of range: that row was skipped */
+
+/* hs_swap_in_args.flags */
+#define HS_SEQ_LENS_I64 1  /* seq_lens is int64 (else int32) */
+#define HS_REQ_STATE_I64 2 /* req_state is int64 (else int32) */
+
+/*
+ * hs_swap_in -- resolve each batch row's top-k token ids against the row's
+ * device hot buffer, assign LRU slots to misses, copy the missing KV rows from
+ * the pool into the hot buffer, and emit each entry's hot-buffer row.
+ *
+ * Defined by: SGLang jit_kernel/csrc/hisparse.cuh, load_cache_to_device_buffer
+ * and load_cache_to_device_buffer_kernel (one row per batch entry: padding
+ * exit, short-sequence fast path, newest-token slot, LRU walk with hits kept
+ * and evictables compacted, misses in top-k order taking least recently used
+ * slots, LRU writeback, per-miss row copy); vLLM
+ * csrc/libtorch_stable/hisparse_kernels.cu, hisparse_resolve_residency_kernel
+ * (invalid ids resolve to -1, padding rows publish -1, corruption tripwires,
+ * hit/miss statistics).
+ *
+ * Per batch row b (rows are independent):
+ *  - padding: b >= *num_real, or req_state[b] < 0 -> out[b][*] = -1,
+ *    miss_count 0, status 0, state untouched.  req_state[b] >= num_states ->
+ *    the same with status HS_ST_BAD_STATE.
+ *  - r = req_state[b], L = seq_lens[b].  If L <= hot_size (fast path):
+ *    out[b][i] = slot_rows[r][t] for i < min(L, top_k) and 0 <= t < L, else -1
+ *    (t = topk_ids[b][i]); state untouched.
+ *  - otherwise an id t is valid iff 0 <= t < L.  Invalid ids and repeats of an
+ *    earlier valid id (HS_ST_DUP_ID) emit -1.  t == L-1 (the newest token)
+ *    emits slot_rows[r][hot_size]; slot hot_size is never read or written
+ *    otherwise.  Every other valid id is a hit if some LRU slot s holds it
+ *    (slot_tokens[r][s] == t; out = slot_rows[r][s]), else a miss candidate.
+ *    A candidate with pool_rows[r][t] outside [0, pool_num_rows) (or
+ *    t >= pool_rows_cols) emits -1 (HS_ST_BAD_POOL_ROW).  The m-th remaining
+ *    miss in top-k order takes the m-th evictable slot in LRU order, emits
+ *    slot_rows[r][s], records slot_tokens[r][s] = t and copies row_bytes bytes
+ *    of pool_k row pool_rows[r][t] to hot_k row slot_rows[r][s] (and pool_v to
+ *    hot_v).  The LRU row becomes [untouched evictables][misses][hits], each
+ *    group in its previous order (misses in top-k order).
+ *  - tripwires: an LRU entry outside [0, hot_size), or a slot already listed
+ *    earlier in the same LRU row, is never a hit and stays evictable
+ *    (HS_ST_BAD_LRU_SLOT); a miss given such an entry, or a slot whose hot row
+ *    is outside [0, hot_num_rows) (HS_ST_BAD_HOT_ROW), emits -1 and writes no
+ *    token and no bytes but still counts as a miss.
+ *
+ * Layouts (all row-major with the given element strides; device memory unless
+ * noted):
+ *  topk_ids    int32 [batch, >=top_k]           stride topk_stride
+ *  seq_lens    int32/int64 [batch]              (flags & HS_SEQ_LENS_I64)
+ *  req_state   int32/int64 [batch]              (flags & HS_REQ_STATE_I64)
+ *  num_real    int32 [1] or NULL (all rows real)
+ *  slot_tokens int32 [num_states, >=hot_size+1] in/out, -1 = empty slot
+ *  slot_rows   int32 [num_states, >=hot_size+1] hot-buffer row of each slot
+ *  lru         int16 [num_states, >=hot_size]   in/out, least recent first
+ *  pool_rows   int64 [num_states, pool_rows_cols] pool row of each token
+ *  pool_k/_v   bytes [pool_num_rows, row_bytes] device or pinned host; pool_v NULL = K only
+ *  hot_k/_v    bytes [hot_num_rows, row_bytes]  device; hot_v NULL iff pool_v NULL
+ *  out_rows    int32 [batch, >=top_k]           stride out_stride
+ *  miss_count  int32 [batch] or NULL; stats uint64 [2] (+= hits, misses) or NULL;
+ *  status      int32 [batch] or NULL (per-row HS_ST_* bits, overwritten)
+ *
+ * Limits: 1 <= top_k <= hot_size <= 32767 (slots are int16); the row's state
+ * must also fit one SM's shared memory (see hs_swap_in_smem_bytes), else
+ * HS_ERR_UNSUPPORTED.  hot_num_rows <= INT32_MAX.
+ * Preconditions (not checked): distinct req_state values within one call;
+ * slot_rows values distinct across the slots the call can touch; pool and hot
+ * buffers do not overlap; no other work writes these buffers concurrently.
+ * Ownership: the caller owns every buffer; nothing is retained after return.
+ */
+typedef struct hs_swap_in_args {
+  int32_t batch;    /* B */
+  int32_t top_k;    /* K */
+  int32_t hot_size; /* H */
+  int32_t flags;    /* HS_SEQ_LENS_I64 | HS_REQ_STATE_I64 */
+  const int32_t* num_real;
+  const int32_t* topk_ids; int64_t topk_stride;
+  const void* seq_lens;
+  const void* req_state;
+  int64_t num_states;
+  int32_t* slot_tokens; int64_t slot_tokens_stride;
+  const int32_t* slot_rows; int64_t slot_rows_stride;
+  int16_t* lru; int64_t lru_stride;
+  const int64_t* pool_rows; int64_t pool_rows_stride; int64_t pool_rows_cols;
+  const void* pool_k; const void* pool_v; int64_t pool_num_rows;
+  void* hot_k; void* hot_v; int64_t hot_num_rows;
+  int64_t row_bytes;
+  int32_t* out_rows; int64_t out_stride;
+  int32_t* miss_count;
+  unsigned long long* stats;
+  int32_t* status;
+} hs_swap_in_args;
+
+hs_err hs_swap_in(const hs_swap_in_args* args, hs_stream_t stream);
+
+/* Shared memory (bytes) one swap-in row needs for (top_k, hot_size); 0 if the
+ * pair is outside the limits above. */
+int64_t hs_swap_in_smem_bytes(int32_t top_k, int32_t hot_size);
+
+/*
+ * hs_store_kv -- scatter n_tokens rows: k_dst row loc[t] = k_src row t, and
+ * likewise V.  Defined by: tokenspeed tokenspeed_kernel/ops/kvcache/triton.py,
+ * store_kv_cache and _store_kv_cache_kernel (per-token K/V scatter; source
+ * leading axis of any stride, rows contiguous).
+ *
+ *  k_src, v_src  device bytes; row t at k_src + t*src_k_stride (bytes); v_src
+ *                NULL = K only (then v_dst must be NULL)
+ *  k_dst, v_dst  device bytes [dst_rows] rows of dst_stride bytes
+ *  loc           device int64 [n_tokens]
+ *  row_bytes     bytes per row (any >= 1; strides >= row_bytes)
+ *  status        device int32 [1] or NULL: HS_ST_BAD_INDEX is OR-ed in when a
+ *                loc is outside [0, dst_rows) (that token is skipped)
+ * Precondition (not checked): loc values are distinct; src and dst do not overlap.
+ */
+hs_err hs_store_kv(const void* k_src, const void* v_src, int64_t src_k_stride,
+                   int64_t src_v_stride, void* k_dst, void* v_dst, int64_t dst_stride,
+                   int64_t dst_rows, const int64_t* loc, int64_t n_tokens, int64_t row_bytes,
+                   int32_t* status, hs_stream_t stream);
+
+/*
+ * hs_transfer_kv -- indexed row gather/scatter over layers: for every pair n
+ * and every pointer pair p in [0, num_layers * (1 + has_v)),
+ * dst_ptrs[p] row dst_idx[n] = src_ptrs[p] row src_idx[n].  With has_v the
+ * arrays hold num_layers K pointers followed by num_layers V pointers.
+ * num_layers == 1 is the per-layer transfer.  Defined by: tokenspeed
+ * tokenspeed_kernel/ops/kvcache/triton.py, transfer_kv_per_layer(_mla) and
+ * transfer_kv_all_layer(_mla) (per-layer base pointers in uint64 arrays, one
+ * index pair copied across all layers); SGLang jit_kernel/csrc/hisparse.cuh,
+ * transfer_cache_dsv4_mla_kernel (the same all-layer form).
+ *
+ *  src_ptrs, dst_ptrs  device uint64 arrays of base addresses (device or pinned
+ *                      host for sources; device for destinations)
+ *  src_idx, dst_idx    device int64 [n]
+ *  src_stride/dst_stride  row pitch in bytes (>= row_bytes); src_rows/dst_rows
+ *                      bound the indices
+ *  status              device int32 [1] or NULL: HS_ST_BAD_INDEX when a pair is
+ *                      out of range (the pair is skipped for every layer)
+ * Precondition (not checked): dst_idx values are distinct; sources and
+ * destinations do not overlap.
+ */
+hs_err hs_transfer_kv(const uint64_t* src_ptrs, const uint64_t* dst_ptrs, int32_t num_layers,
+                      int32_t has_v, const int64_t* src_idx, const int64_t* dst_idx, int64_t n,
+                      int64_t src_stride, int64_t dst_stride, int64_t src_rows,
+                      int64_t dst_rows, int64_t row_bytes, int32_t* status,
+                      hs_stream_t stream);
+
+/*
+ * hs_probe_read -- measurement utility, not part of the method: stream-read
+ * `bytes` bytes (16-byte aligned pointer, bytes % 16 == 0) from device or
+ * pinned host memory with every SM, folding them into *sink (device uint64
+ * [1]).  Used to measure the host-link read bandwidth that bounds swap-ins
+ * from a pinned-host pool.
+ */
+hs_err hs_probe_read(const void* src, int64_t bytes, unsigned long long* sink,
+                     hs_stream_t stream);
+
+/* Text for an hs_err code. */
+const char* hs_err_string(int32_t err);
+
+/* Name of one HS_ST_* status bit ("" for a value that is not a single known bit). */
+const char* hs_status_string(int32_t bit);
+
+/* Message for the calling thread's last non-HS_OK return ("" if none). */
+const char* hs_last_error(void);
+
+/* ABI version of this header. */
+#define HS_ABI_VERSION 1
+int32_t hs_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HISPARSE_H */

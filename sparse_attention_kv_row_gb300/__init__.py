@@ -1,0 +1,218 @@
+"""HiSparse decode-time KV-row swap-in and indexed KV-row movers for GB300.
+
+Thin PyTorch binding over libhisparse (include/hisparse.h): it checks tensor
+dtypes/shapes and passes raw pointers, strides and the current CUDA stream;
+every step of the computation runs in the library's sm_103a kernels.  PyTorch
+provides device/pinned memory and streams only.  There is no CPU fallback: if
+the library is not built, importing the binding's entry points raises.
+
+Entry points (same names as the C ABI):
+  swap_in(...)       hs_swap_in      -- resolve top-k ids, LRU-assign misses,
+                                        copy missing rows, emit hot-buffer rows
+  store_kv(...)      hs_store_kv     -- k_dst[loc] = k_src, v_dst[loc] = v_src
+  transfer_kv(...)   hs_transfer_kv  -- per-layer / all-layer indexed row copy
+  probe_read(...)    hs_probe_read   -- streaming-read bandwidth probe
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _capi
+from ._capi import (HisparseError, SwapInArgs, ST_BAD_HOT_ROW, ST_BAD_INDEX,  # noqa: F401
+                    ST_BAD_LRU_SLOT, ST_BAD_POOL_ROW, ST_BAD_STATE, ST_DUP_ID, ST_TIMEOUT)
+
+__all__ = ["swap_in", "swap_in_args", "make_swap_in_args", "store_kv", "transfer_kv",
+           "transfer_kv_layers", "probe_read", "swap_in_smem_bytes", "library_path",
+           "HisparseError", "SwapInArgs"]
+
+
+def library_path() -> str:
+    return _capi.LIB_PATH
+
+
+def _lib():
+    return _capi.load()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if isinstance(stream, torch.cuda.Stream) else int(stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def _need(t, dtype, name, ndim=None):
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must be {ndim}-D, got shape {tuple(t.shape)}")
+    if ndim == 2 and t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name} rows must be contiguous")
+    if ndim == 1 and t.numel() > 1 and t.stride(0) != 1:
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _byte_rows(t, name):
+    """(ptr, rows, row_bytes, pitch_bytes) of a tensor whose trailing dims are
+    one contiguous row."""
+    if t.dim() < 1:
+        raise ValueError(f"{name} must have a leading row axis")
+    inner = t[0] if t.shape[0] > 0 else t.new_empty(t.shape[1:])
+    if t.dim() > 1 and not inner.is_contiguous():
+        raise ValueError(f"{name}: each row must be contiguous")
+    row_bytes = (inner.numel() if t.dim() > 1 else 1) * t.element_size()
+    pitch = (t.stride(0) if t.dim() > 1 else 1) * t.element_size()
+    return int(t.data_ptr()), int(t.shape[0]), int(row_bytes), int(pitch)
+
+
+def swap_in_smem_bytes(top_k: int, hot_size: int) -> int:
+    return int(_lib().hs_swap_in_smem_bytes(top_k, hot_size))
+
+
+def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_rows,
+                      pool_k, hot_k, out_rows, hot_size=None, pool_v=None, hot_v=None,
+                      num_real=None, miss_count=None, stats=None, status=None) -> SwapInArgs:
+    """Build a reusable ``hs_swap_in_args`` for these tensors (see include/hisparse.h)."""
+    H = int(hot_size if hot_size is not None else lru.shape[1])
+    _need(topk_ids, torch.int32, "topk_ids", 2)
+    _need(out_rows, torch.int32, "out_rows", 2)
+    _need(slot_tokens, torch.int32, "slot_tokens", 2)
+    _need(slot_rows, torch.int32, "slot_rows", 2)
+    _need(lru, torch.int16, "lru", 2)
+    _need(pool_rows, torch.int64, "pool_rows", 2)
+    if seq_lens.dtype not in (torch.int32, torch.int64) or req_state.dtype not in (
+            torch.int32, torch.int64):
+        raise TypeError("seq_lens and req_state must be int32 or int64")
+    _need(seq_lens, seq_lens.dtype, "seq_lens", 1)
+    _need(req_state, req_state.dtype, "req_state", 1)
+    if num_real is not None:
+        _need(num_real, torch.int32, "num_real", 1)
+    if miss_count is not None:
+        _need(miss_count, torch.int32, "miss_count", 1)
+    if status is not None:
+        _need(status, torch.int32, "status", 1)
+    if stats is not None:
+        if stats.dtype not in (torch.int64, getattr(torch, "uint64", torch.int64)) or \
+                stats.numel() < 2:
+            raise TypeError("stats must be a 2-element 64-bit integer tensor")
+    B, K = topk_ids.shape
+    if out_rows.shape[0] < B or out_rows.shape[1] < K:
+        raise ValueError("out_rows must be at least [batch, top_k]")
+    if seq_lens.numel() < B or req_state.numel() < B:
+        raise ValueError("seq_lens and req_state need one entry per batch row")
+    pk_ptr, p_rows, row_bytes, p_pitch = _byte_rows(pool_k, "pool_k")
+    hk_ptr, h_rows, h_bytes, h_pitch = _byte_rows(hot_k, "hot_k")
+    if h_bytes != row_bytes or p_pitch != row_bytes or h_pitch != row_bytes:
+        raise ValueError("pool and hot buffers need contiguous rows of the same byte width")
+    pv_ptr = hv_ptr = None
+    if pool_v is not None or hot_v is not None:
+        if pool_v is None or hot_v is None:
+            raise ValueError("pool_v and hot_v go together")
+        pv_ptr, pv_rows, pv_bytes, pv_pitch = _byte_rows(pool_v, "pool_v")
+        hv_ptr, hv_rows, hv_bytes, hv_pitch = _byte_rows(hot_v, "hot_v")
+        if {pv_bytes, hv_bytes, pv_pitch, hv_pitch} != {row_bytes}:
+            raise ValueError("V buffers need the same row width as K")
+        p_rows, h_rows = min(p_rows, pv_rows), min(h_rows, hv_rows)
+    flags = (_capi.SEQ_LENS_I64 if seq_lens.dtype == torch.int64 else 0) | (
+        _capi.REQ_STATE_I64 if req_state.dtype == torch.int64 else 0)
+    return SwapInArgs(
+        batch=B, top_k=K, hot_size=H, flags=flags, num_real=_ptr(num_real),
+        topk_ids=_ptr(topk_ids), topk_stride=topk_ids.stride(0),
+        seq_lens=_ptr(seq_lens), req_state=_ptr(req_state),
+        num_states=min(slot_tokens.shape[0], slot_rows.shape[0], lru.shape[0],
+                       pool_rows.shape[0]),
+        slot_tokens=_ptr(slot_tokens), slot_tokens_stride=slot_tokens.stride(0),
+        slot_rows=_ptr(slot_rows), slot_rows_stride=slot_rows.stride(0),
+        lru=_ptr(lru), lru_stride=lru.stride(0),
+        pool_rows=_ptr(pool_rows), pool_rows_stride=pool_rows.stride(0),
+        pool_rows_cols=pool_rows.shape[1],
+        pool_k=pk_ptr, pool_v=pv_ptr, pool_num_rows=p_rows,
+        hot_k=hk_ptr, hot_v=hv_ptr, hot_num_rows=h_rows,
+        row_bytes=row_bytes, out_rows=_ptr(out_rows), out_stride=out_rows.stride(0),
+        miss_count=_ptr(miss_count), stats=_ptr(stats), status=_ptr(status))
+
+
+def swap_in_args(args: SwapInArgs, stream=None) -> None:
+    """Launch hs_swap_in with a prepared argument block."""
+    _capi.check(_lib().hs_swap_in(C.byref(args), C.c_void_p(_stream(stream))), "hs_swap_in")
+
+
+def swap_in(*, stream=None, **tensors) -> None:
+    """One swap-in call; keyword tensors as in ``make_swap_in_args``."""
+    swap_in_args(make_swap_in_args(**tensors), stream)
+
+
+def store_kv(k_src, v_src, k_dst, v_dst, loc, status=None, stream=None) -> None:
+    """k_dst[loc[t]] = k_src[t] and v_dst[loc[t]] = v_src[t] (v_* may be None)."""
+    _need(loc, torch.int64, "loc", 1)
+    ks, n, rb, ksp = _byte_rows(k_src, "k_src")
+    kd, drows, rbd, dp = _byte_rows(k_dst, "k_dst")
+    if rbd != rb:
+        raise ValueError("k_src and k_dst rows differ in width")
+    vs = vd = None
+    vsp = 0
+    if v_src is not None or v_dst is not None:
+        if v_src is None or v_dst is None:
+            raise ValueError("v_src and v_dst go together")
+        vs, vn, vrb, vsp = _byte_rows(v_src, "v_src")
+        vd, vdrows, vdrb, vdp = _byte_rows(v_dst, "v_dst")
+        if vn != n or vrb != rb or vdrb != rb or vdp != dp:
+            raise ValueError("V tensors must match K in rows, width and destination pitch")
+        drows = min(drows, vdrows)
+    if loc.numel() != n:
+        raise ValueError("loc needs one entry per source row")
+    _capi.check(_lib().hs_store_kv(ks, vs, ksp, vsp, kd, vd, dp, drows, _ptr(loc), n, rb,
+                                   _ptr(status), C.c_void_p(_stream(stream))), "hs_store_kv")
+
+
+def transfer_kv(src_ptrs, dst_ptrs, src_idx, dst_idx, *, num_layers, has_v, src_stride,
+                dst_stride, src_rows, dst_rows, row_bytes, status=None, stream=None) -> None:
+    """Raw hs_transfer_kv: device uint64 pointer arrays and int64 index arrays."""
+    _need(src_idx, torch.int64, "src_idx", 1)
+    _need(dst_idx, torch.int64, "dst_idx", 1)
+    if src_idx.numel() != dst_idx.numel():
+        raise ValueError("src_idx and dst_idx differ in length")
+    _capi.check(_lib().hs_transfer_kv(
+        _ptr(src_ptrs), _ptr(dst_ptrs), num_layers, int(bool(has_v)), _ptr(src_idx),
+        _ptr(dst_idx), src_idx.numel(), src_stride, dst_stride, src_rows, dst_rows, row_bytes,
+        _ptr(status), C.c_void_p(_stream(stream))), "hs_transfer_kv")
+
+
+def layer_pointer_array(layers, device) -> torch.Tensor:
+    """Device uint64-as-int64 array of the layers' base addresses."""
+    return torch.tensor([int(t.data_ptr()) for t in layers], dtype=torch.int64, device=device)
+
+
+def transfer_kv_layers(src_layers, dst_layers, src_idx, dst_idx, *, has_v=False, status=None,
+                       stream=None, ptrs=None) -> None:
+    """Convenience form over lists of per-layer tensors [rows, ...] (K layers then V
+    layers when has_v).  ``ptrs`` may pass prebuilt (src_ptrs, dst_ptrs)."""
+    if len(src_layers) != len(dst_layers) or not src_layers:
+        raise ValueError("need matching non-empty layer lists")
+    geo_s = {_byte_rows(t, "src")[2:] for t in src_layers}
+    geo_d = {_byte_rows(t, "dst")[2:] for t in dst_layers}
+    if len(geo_s) != 1 or len(geo_d) != 1:
+        raise ValueError("all layers need the same row width and pitch")
+    (rb, sp), (rbd, dp) = geo_s.pop(), geo_d.pop()
+    if rb != rbd:
+        raise ValueError("source and destination rows differ in width")
+    nl = len(src_layers) // (2 if has_v else 1)
+    if ptrs is None:
+        dev = src_idx.device
+        ptrs = (layer_pointer_array(src_layers, dev), layer_pointer_array(dst_layers, dev))
+    transfer_kv(ptrs[0], ptrs[1], src_idx, dst_idx, num_layers=nl, has_v=has_v, src_stride=sp,
+                dst_stride=dp, src_rows=min(t.shape[0] for t in src_layers),
+                dst_rows=min(t.shape[0] for t in dst_layers), row_bytes=rb, status=status,
+                stream=stream)
+
+
+def probe_read(src, sink, stream=None) -> None:
+    """Stream-read every byte of ``src`` (device or pinned host) into ``sink``."""
+    ptr, n, rb, pitch = _byte_rows(src.view(-1), "src")
+    _capi.check(_lib().hs_probe_read(ptr, n * rb, _ptr(sink), C.c_void_p(_stream(stream))),
+                "hs_probe_read")

@@ -1,0 +1,139 @@
+// hs_device.cuh -- device helpers for the swap-in and mover kernels (sm_103a):
+// cache-hinted loads/stores as inline PTX, LDGSTS staging into shared memory,
+// warp scans, and a 32-bit divider by multiply-high.
+#pragma once
+
+#include <cstdint>
+
+namespace hs {
+
+constexpr int kWarp = 32;
+constexpr unsigned kFullMask = 0xFFFFFFFFu;
+
+// ------------------------------------------------------------------ loads/stores
+// Streaming reads of pool bytes: read-only path, no L1 allocation.  Used on
+// device memory and on pinned host memory alike.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_stream_u8(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u8 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// Hot-buffer writes: cache in L2 only (the attention kernel reads them next).
+__device__ __forceinline__ void st_l2_v4(void* p, uint4 v) {
+  asm volatile("st.global.cg.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_l2_u32(void* p, uint32_t v) {
+  asm volatile("st.global.cg.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_l2_u8(void* p, uint32_t v) {
+  asm volatile("st.global.cg.u8 [%0], %1;" ::"l"(p), "h"((uint16_t)v) : "memory");
+}
+
+// Streaming writes for bulk movers (evict-first).
+__device__ __forceinline__ void st_stream_v4(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_stream_u32(void* p, uint32_t v) {
+  asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_stream_u8(void* p, uint32_t v) {
+  asm volatile("st.global.cs.u8 [%0], %1;" ::"l"(p), "h"((uint16_t)v) : "memory");
+}
+
+// ------------------------------------------------------------------ LDGSTS staging
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async_16(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Copy `nbytes` from global `src` to shared `dst`, where dst and src agree
+// modulo 16 (the shared array is placed at the source's alignment).  The
+// 16-byte-aligned body goes through LDGSTS (no register staging, many copies
+// in flight); the < 16-byte head and tail through plain byte loads.  The
+// caller commits/waits and synchronises.
+__device__ __forceinline__ void stage_bytes(void* dst, const void* src, int64_t nbytes, int tid,
+                                            int nthreads) {
+  const uintptr_t s = reinterpret_cast<uintptr_t>(src);
+  int64_t head = static_cast<int64_t>((16u - (s & 15u)) & 15u);
+  if (head > nbytes) head = nbytes;
+  const int64_t body = ((nbytes - head) / 16) * 16;
+  const int64_t tail = nbytes - head - body;
+  const char* sc = static_cast<const char*>(src);
+  char* dc = static_cast<char*>(dst);
+  if (tid < head) dc[tid] = sc[tid];
+  if (tid >= 32 && tid < 32 + tail) {
+    const int64_t o = head + body + (tid - 32);
+    dc[o] = sc[o];
+  }
+  for (int64_t o = head + static_cast<int64_t>(tid) * 16; o < head + body;
+       o += static_cast<int64_t>(nthreads) * 16)
+    cp_async_16(dc + o, sc + o);
+}
+
+// ------------------------------------------------------------------ scans
+// Exclusive prefix over the 32 lanes; returns the warp total in *total.
+__device__ __forceinline__ int warp_exclusive_scan(int v, int lane, int* total) {
+  int x = v;
+#pragma unroll
+  for (int d = 1; d < kWarp; d <<= 1) {
+    const int y = __shfl_up_sync(kFullMask, x, d);
+    if (lane >= d) x += y;
+  }
+  *total = __shfl_sync(kFullMask, x, kWarp - 1);
+  return x - v;
+}
+
+// In-place exclusive scan of cnt[0..n) (n <= 32 * 1024) by one warp; returns
+// the grand total to every lane of that warp.
+__device__ __forceinline__ int warp_scan_array(int* cnt, int n, int lane) {
+  const int per = (n + kWarp - 1) / kWarp;
+  const int begin = lane * per;
+  const int end = min(n, begin + per);
+  int local = 0;
+  for (int i = begin; i < end; ++i) local += cnt[i];
+  int total;
+  int run = warp_exclusive_scan(local, lane, &total);
+  for (int i = begin; i < end; ++i) {
+    const int c = cnt[i];
+    cnt[i] = run;
+    run += c;
+  }
+  return total;
+}
+
+// ------------------------------------------------------------------ division
+// floor(n / d) for 32-bit n by multiply-high with M = ceil(2^64 / d) (Lemire,
+// Kaser, Kurz, "Faster remainder by direct computation", 2019): exact for every
+// 32-bit n and 1 <= d < 2^32.  M is computed on the host.
+struct FastDiv {
+  uint64_t magic;
+  uint32_t d;
+};
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, FastDiv f) {
+  return static_cast<uint32_t>(__umul64hi(f.magic, static_cast<uint64_t>(n)));
+}
+
+}  // namespace hs

@@ -1,0 +1,32 @@
+// hs_host.h -- host-side helpers shared by the library's translation units:
+// per-thread error message, device properties cache, pointer classification.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/hisparse.h"
+
+namespace hs {
+
+// Records `msg` as the calling thread's last error and returns `code`.
+hs_err fail(hs_err code, const char* fmt, ...);
+void clear_error();
+
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  int max_smem_optin;
+};
+// Properties of the current device (cached per device).
+hs_err current_device(DeviceInfo* out);
+
+enum class MemKind { kDevice, kHost, kManaged, kUnregistered, kUnknown };
+MemKind classify(const void* p);
+
+// Lemire-Kaser-Kurz divider constant for 1 <= d < 2^32 (d == 1 gives magic 0
+// and the device side short-circuits it).
+inline uint64_t fastdiv_magic(uint32_t d) { return d <= 1 ? 0ull : (~0ull) / d + 1ull; }
+
+}  // namespace hs

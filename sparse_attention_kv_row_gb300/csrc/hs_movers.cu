@@ -1,0 +1,285 @@
+// hs_movers.cu -- indexed KV-row movers for sm_103a, plus a streaming-read
+// bandwidth probe.
+//
+//  store_kv   tokenspeed tokenspeed_kernel/ops/kvcache/triton.py, store_kv_cache:
+//             k_dst[loc[t]] = k_src[t], v_dst[loc[t]] = v_src[t].
+//  transfer   tokenspeed ... transfer_kv_per_layer(_mla) / transfer_kv_all_layer(_mla)
+//             and SGLang jit_kernel/csrc/hisparse.cuh, transfer_cache_dsv4_mla_kernel:
+//             for each index pair, the same row of every layer's cache.
+//
+// Work is flattened into (row) units -- (token, K|V) for store_kv and
+// (pair, layer) for transfer, pair-major like the pages -- and spread one
+// warp per unit over a persistent grid sized to the SM count.  A warp moves
+// its row in 16-byte chunks when source, destination and size allow it, else
+// in 4-byte words, else bytes, with up to four chunks per lane in flight.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "hs_device.cuh"
+#include "hs_host.h"
+
+namespace hs {
+namespace {
+
+constexpr int kMoverThreads = 256;
+constexpr int kMoverBlocksPerSm = 8;
+constexpr int kUnroll = 4;
+
+// Copies `bytes` bytes from src to dst with one warp, choosing the widest chunk
+// that all three of (src, dst, bytes) allow.
+__device__ __forceinline__ void warp_copy_row(unsigned char* dst, const unsigned char* src,
+                                              int64_t bytes, int lane) {
+  const uintptr_t al = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) |
+                       static_cast<uintptr_t>(bytes);
+  if ((al & 15) == 0) {
+    const int64_t n = bytes >> 4;
+    for (int64_t c0 = lane; c0 < n; c0 += kWarp * kUnroll) {
+      uint4 v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t c = c0 + u * kWarp;
+        if (c < n) v[u] = ld_stream_v4(src + (c << 4));
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t c = c0 + u * kWarp;
+        if (c < n) st_stream_v4(dst + (c << 4), v[u]);
+      }
+    }
+  } else if ((al & 3) == 0) {
+    const int64_t n = bytes >> 2;
+    for (int64_t c0 = lane; c0 < n; c0 += kWarp * kUnroll) {
+      uint32_t v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t c = c0 + u * kWarp;
+        if (c < n) v[u] = ld_stream_u32(src + (c << 2));
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t c = c0 + u * kWarp;
+        if (c < n) st_stream_u32(dst + (c << 2), v[u]);
+      }
+    }
+  } else {
+    for (int64_t c0 = lane; c0 < bytes; c0 += kWarp * kUnroll) {
+      uint32_t v[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t c = c0 + u * kWarp;
+        if (c < bytes) v[u] = ld_stream_u8(src + c);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t c = c0 + u * kWarp;
+        if (c < bytes) st_stream_u8(dst + c, v[u]);
+      }
+    }
+  }
+}
+
+struct StoreKvParams {
+  const unsigned char* k_src;
+  const unsigned char* v_src;
+  int64_t src_k_stride, src_v_stride;
+  unsigned char* k_dst;
+  unsigned char* v_dst;
+  int64_t dst_stride, dst_rows;
+  const int64_t* loc;
+  int64_t n_tokens, row_bytes;
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(kMoverThreads) store_kv_kernel(const StoreKvParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (kMoverThreads / kWarp);
+  const int kv = p.v_src != nullptr ? 2 : 1;
+  const int64_t units = p.n_tokens * kv;
+  for (int64_t u = static_cast<int64_t>(blockIdx.x) * (kMoverThreads / kWarp) +
+                   (threadIdx.x >> 5);
+       u < units; u += warps) {
+    const int64_t t = kv == 2 ? (u >> 1) : u;
+    const bool is_v = kv == 2 && (u & 1);
+    const int64_t d = __ldg(p.loc + t);
+    if (d < 0 || d >= p.dst_rows) {
+      if (lane == 0 && !is_v && p.status) atomicOr(p.status, HS_ST_BAD_INDEX);
+      continue;
+    }
+    const unsigned char* src = is_v ? p.v_src + t * p.src_v_stride : p.k_src + t * p.src_k_stride;
+    unsigned char* dst = (is_v ? p.v_dst : p.k_dst) + d * p.dst_stride;
+    warp_copy_row(dst, src, p.row_bytes, lane);
+  }
+}
+
+struct TransferParams {
+  const uint64_t* src_ptrs;
+  const uint64_t* dst_ptrs;
+  const int64_t* src_idx;
+  const int64_t* dst_idx;
+  int64_t pair_begin;      // first pair of this launch
+  uint32_t units;          // pairs_in_launch * ptr_pairs  (< 2^32)
+  uint32_t ptr_pairs;      // num_layers * (1 + has_v)
+  FastDiv div_ptr_pairs;
+  int64_t src_stride, dst_stride, src_rows, dst_rows, row_bytes;
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(kMoverThreads) transfer_kernel(const TransferParams p) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t warps = gridDim.x * (kMoverThreads / kWarp);
+  for (uint32_t u = blockIdx.x * (kMoverThreads / kWarp) + (threadIdx.x >> 5); u < p.units;
+       u += warps) {
+    const uint32_t pair = p.ptr_pairs == 1 ? u : fast_div(u, p.div_ptr_pairs);
+    const uint32_t layer = u - pair * p.ptr_pairs;
+    const int64_t n = p.pair_begin + pair;
+    const int64_t s = __ldg(p.src_idx + n);
+    const int64_t d = __ldg(p.dst_idx + n);
+    if (s < 0 || s >= p.src_rows || d < 0 || d >= p.dst_rows) {
+      if (lane == 0 && layer == 0 && p.status) atomicOr(p.status, HS_ST_BAD_INDEX);
+      continue;
+    }
+    const unsigned char* src =
+        reinterpret_cast<const unsigned char*>(__ldg(p.src_ptrs + layer)) + s * p.src_stride;
+    unsigned char* dst =
+        reinterpret_cast<unsigned char*>(__ldg(p.dst_ptrs + layer)) + d * p.dst_stride;
+    warp_copy_row(dst, src, p.row_bytes, lane);
+  }
+}
+
+__global__ void __launch_bounds__(512) probe_read_kernel(const uint4* src, int64_t n16,
+                                                         unsigned long long* sink) {
+  uint32_t acc = 0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 a = ld_stream_v4(src + i);
+    const uint4 b = ld_stream_v4(src + i + stride);
+    const uint4 c = ld_stream_v4(src + i + 2 * stride);
+    const uint4 d = ld_stream_v4(src + i + 3 * stride);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w ^ b.x ^ b.y ^ b.z ^ b.w ^ c.x ^ c.y ^ c.z ^ c.w ^ d.x ^ d.y ^
+           d.z ^ d.w;
+  }
+  for (; i < n16; i += stride) {
+    const uint4 a = ld_stream_v4(src + i);
+    acc ^= a.x ^ a.y ^ a.z ^ a.w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(kFullMask, acc, o);
+  if ((threadIdx.x & 31) == 0 && acc != 0) atomicXor(sink, static_cast<unsigned long long>(acc));
+}
+
+int mover_grid(const DeviceInfo& dev, int64_t units) {
+  const int64_t warps_per_block = kMoverThreads / kWarp;
+  int64_t blocks = (units + warps_per_block - 1) / warps_per_block;
+  const int64_t cap = static_cast<int64_t>(dev.sm_count) * kMoverBlocksPerSm;
+  if (blocks > cap) blocks = cap;
+  return static_cast<int>(blocks < 1 ? 1 : blocks);
+}
+
+}  // namespace
+}  // namespace hs
+
+extern "C" hs_err hs_store_kv(const void* k_src, const void* v_src, int64_t src_k_stride,
+                              int64_t src_v_stride, void* k_dst, void* v_dst, int64_t dst_stride,
+                              int64_t dst_rows, const int64_t* loc, int64_t n_tokens,
+                              int64_t row_bytes, int32_t* status, hs_stream_t stream) {
+  using namespace hs;
+  clear_error();
+  if (n_tokens < 0 || row_bytes < 1 || dst_rows < 0)
+    return fail(HS_ERR_ARG, "hs_store_kv: need n_tokens >= 0, row_bytes >= 1, dst_rows >= 0");
+  if (n_tokens == 0) return HS_OK;
+  if (k_src == nullptr || k_dst == nullptr || loc == nullptr)
+    return fail(HS_ERR_ARG, "hs_store_kv: k_src, k_dst and loc are required");
+  if ((v_src == nullptr) != (v_dst == nullptr))
+    return fail(HS_ERR_ARG, "hs_store_kv: v_src and v_dst must both be set or both be NULL");
+  if (src_k_stride < row_bytes || dst_stride < row_bytes ||
+      (v_src != nullptr && src_v_stride < row_bytes))
+    return fail(HS_ERR_ARG, "hs_store_kv: strides must be >= row_bytes");
+  DeviceInfo dev;
+  hs_err err = current_device(&dev);
+  if (err != HS_OK) return err;
+  StoreKvParams p{static_cast<const unsigned char*>(k_src),
+                  static_cast<const unsigned char*>(v_src),
+                  src_k_stride,
+                  src_v_stride,
+                  static_cast<unsigned char*>(k_dst),
+                  static_cast<unsigned char*>(v_dst),
+                  dst_stride,
+                  dst_rows,
+                  loc,
+                  n_tokens,
+                  row_bytes,
+                  status};
+  const int64_t units = n_tokens * (v_src != nullptr ? 2 : 1);
+  store_kv_kernel<<<mover_grid(dev, units), kMoverThreads, 0,
+                    reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(HS_ERR_CUDA, "hs_store_kv launch: %s", cudaGetErrorString(e));
+  return HS_OK;
+}
+
+extern "C" hs_err hs_transfer_kv(const uint64_t* src_ptrs, const uint64_t* dst_ptrs,
+                                 int32_t num_layers, int32_t has_v, const int64_t* src_idx,
+                                 const int64_t* dst_idx, int64_t n, int64_t src_stride,
+                                 int64_t dst_stride, int64_t src_rows, int64_t dst_rows,
+                                 int64_t row_bytes, int32_t* status, hs_stream_t stream) {
+  using namespace hs;
+  clear_error();
+  if (n < 0 || num_layers < 0 || row_bytes < 1 || src_rows < 0 || dst_rows < 0)
+    return fail(HS_ERR_ARG, "hs_transfer_kv: negative size or row_bytes < 1");
+  if (has_v != 0 && has_v != 1) return fail(HS_ERR_ARG, "hs_transfer_kv: has_v must be 0 or 1");
+  if (n == 0 || num_layers == 0) return HS_OK;
+  if (src_ptrs == nullptr || dst_ptrs == nullptr || src_idx == nullptr || dst_idx == nullptr)
+    return fail(HS_ERR_ARG, "hs_transfer_kv: pointer arrays and index arrays are required");
+  if (src_stride < row_bytes || dst_stride < row_bytes)
+    return fail(HS_ERR_ARG, "hs_transfer_kv: strides must be >= row_bytes");
+  DeviceInfo dev;
+  hs_err err = current_device(&dev);
+  if (err != HS_OK) return err;
+  const uint32_t ptr_pairs = static_cast<uint32_t>(num_layers) * (has_v ? 2u : 1u);
+  // Units are 32-bit: launch at most floor((2^32 - 1) / ptr_pairs) pairs at a time.
+  const int64_t max_pairs = static_cast<int64_t>(0xFFFFFFFFull / ptr_pairs);
+  for (int64_t begin = 0; begin < n; begin += max_pairs) {
+    const int64_t pairs = (n - begin) < max_pairs ? (n - begin) : max_pairs;
+    TransferParams p;
+    p.src_ptrs = src_ptrs;
+    p.dst_ptrs = dst_ptrs;
+    p.src_idx = src_idx;
+    p.dst_idx = dst_idx;
+    p.pair_begin = begin;
+    p.units = static_cast<uint32_t>(pairs * ptr_pairs);
+    p.ptr_pairs = ptr_pairs;
+    p.div_ptr_pairs = FastDiv{fastdiv_magic(ptr_pairs), ptr_pairs};
+    p.src_stride = src_stride;
+    p.dst_stride = dst_stride;
+    p.src_rows = src_rows;
+    p.dst_rows = dst_rows;
+    p.row_bytes = row_bytes;
+    p.status = status;
+    transfer_kernel<<<mover_grid(dev, p.units), kMoverThreads, 0,
+                      reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+      return fail(HS_ERR_CUDA, "hs_transfer_kv launch: %s", cudaGetErrorString(e));
+  }
+  return HS_OK;
+}
+
+extern "C" hs_err hs_probe_read(const void* src, int64_t bytes, unsigned long long* sink,
+                                hs_stream_t stream) {
+  using namespace hs;
+  clear_error();
+  if (src == nullptr || sink == nullptr || bytes < 0 || (bytes & 15) ||
+      (reinterpret_cast<uintptr_t>(src) & 15))
+    return fail(HS_ERR_ARG, "hs_probe_read: need a 16-byte aligned source and bytes %% 16 == 0");
+  if (bytes == 0) return HS_OK;
+  DeviceInfo dev;
+  hs_err err = current_device(&dev);
+  if (err != HS_OK) return err;
+  probe_read_kernel<<<dev.sm_count * 4, 512, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(src), bytes >> 4, sink);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(HS_ERR_CUDA, "hs_probe_read launch: %s", cudaGetErrorString(e));
+  return HS_OK;
+}

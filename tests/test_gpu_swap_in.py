@@ -1,0 +1,146 @@
+"""GPU parity for hs_swap_in: bit-exact against the CPU oracle (indices, LRU
+state, slot tokens, hot-buffer bytes, counters and status bits), through the
+C ABI, over tiny exhaustive-style cases, ragged multi-tile sizes, every copy
+width (16-byte, 4-byte, byte), K+V, pinned-host pools, int32/int64 index
+types, padding rows and host-injected corruption."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import cases
+from gpu_cases import GpuCase, step_both
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+def test_golden_worked_example_on_gpu(dev):
+    import json
+    import os
+
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden",
+                                    "swap_in_worked_example.json")))
+    H, L = g["hot_size"], g["seq_len"]
+    W = H + 1
+    c = cases.Case(H=H, K=3, S=2, topk=np.zeros((1, 3), np.int32),
+                   seq_lens=np.array([L], np.int64), req_state=np.zeros(1, np.int64),
+                   tokens=np.full((1, W), -1, np.int32),
+                   rows=np.array([g["slot_rows"]], np.int32),
+                   lru=np.arange(H, dtype=np.int16)[None], pool_rows=
+                   np.array([[50 + t for t in range(L)]], np.int64),
+                   pool_k=np.array([[x % 256, (x + 1) % 256] for x in range(64)], np.uint8),
+                   pool_v=None, hot_k=np.full((105, 2), 0xEE, np.uint8), hot_v=None)
+    gc = GpuCase(c.copy(), dev)
+    for st in g["steps"]:
+        out, miss, status, _ = gc.step(np.array([st["ids"]], np.int32))
+        assert out[0].tolist() == st["out"]
+        assert int(miss[0]) == st["miss_count"] and int(status[0]) == st["status"]
+        assert gc.lru.cpu().numpy()[0].tolist() == st["lru"]
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_random_tiny_with_corruption(dev, seed):
+    rng = np.random.default_rng(5000 + seed)
+    H = int(rng.integers(1, 40))
+    K = int(rng.integers(1, H + 1))
+    B = int(rng.integers(1, 6))
+    S = int(rng.choice([1, 3, 4, 16, 17, 132, 656]))
+    seq = rng.integers(1, 4 * H + 3, size=B)
+    ref = cases.random_case(rng, B=B, K=K, H=H, S=S, R=B + 2, seq_len=seq,
+                            P=int(rng.integers(4 * H + 3, 8 * H + 8)),
+                            with_v=bool(seed % 3 == 0))
+    ref.num_real = int(rng.choice([-1, B, max(0, B - 1)]))
+    g = GpuCase(ref.copy(), dev, pool_in_host=bool(seed % 4 == 1),
+                seq_dtype=torch.int32 if seed % 2 else torch.int64,
+                req_dtype=torch.int32 if seed % 5 == 0 else torch.int64)
+    g.case = ref
+    prev = None
+    for step in range(6):
+        ids = cases.random_ids(rng, ref, prev=prev)
+        prev = ids
+        if step >= 3:
+            cases.corrupt(np.random.default_rng(seed * 7 + step), ref)
+            g.push_state(ref)
+        step_both(g, ref, ids, f"seed={seed} step={step}")
+
+
+@pytest.mark.parametrize("H,K,S,B,with_v,host", [
+    (1000, 700, 656, 5, False, False),     # several 1024-thread tiles, ragged tail
+    (2500, 2500, 132, 3, False, True),     # K == H, 4-byte path, pinned host pool
+    (4096, 2048, 656, 4, True, False),     # K and V
+    (3001, 1237, 17, 2, False, False),     # byte path, odd sizes
+    (777, 33, 2048, 3, False, True),
+])
+def test_multi_tile_workloads(dev, H, K, S, B, with_v, host):
+    rng = np.random.default_rng(H * 7 + K)
+    L = 8 * H
+    ref = cases.random_case(rng, B=B, K=K, H=H, S=S, R=B + 1, seq_len=L, with_v=with_v,
+                            width_pad=3)
+    g = GpuCase(ref.copy(), dev, pool_in_host=host)
+    g.case = ref
+    import synth
+    ts = synth.TopkStream(H, 0, B, K, L, 0.6)
+    for step in range(5):
+        step_both(g, ref, ts.next(), f"H={H} step={step}")
+    # a step with invalid, duplicate and newest ids mixed in
+    step_both(g, ref, cases.random_ids(rng, ref), "mixed")
+
+
+def test_all_rows_padding_and_empty(dev):
+    rng = np.random.default_rng(3)
+    ref = cases.random_case(rng, B=3, K=8, H=16, S=16, R=4, seq_len=50)
+    ref.num_real = 0
+    g = GpuCase(ref.copy(), dev)
+    g.case = ref
+    out, miss, status, stats = step_both(g, ref, cases.random_ids(rng, ref), "num_real=0")
+    assert np.all(out == -1) and np.all(miss == 0)
+
+
+def test_capture_in_cuda_graph(dev):
+    """A swap-in captured in a CUDA graph and replayed matches eager calls."""
+    import sparse_attention_kv_row_gb300 as hs
+    import synth
+
+    rng = np.random.default_rng(9)
+    H, K, B, L = 256, 64, 4, 4000
+    ref = cases.random_case(rng, B=B, K=K, H=H, S=656, R=B, seq_len=L)
+    g = GpuCase(ref.copy(), dev)
+    ts = synth.TopkStream(1, 0, B, K, L, 0.5)
+    topk = torch.zeros((B, K), dtype=torch.int32, device=dev)
+    out = torch.zeros((B, K), dtype=torch.int32, device=dev)
+    seq = torch.from_numpy(ref.seq_lens).to(dev)
+    req = torch.from_numpy(ref.req_state).to(dev)
+    args = hs.make_swap_in_args(topk_ids=topk, seq_lens=seq, req_state=req,
+                                slot_tokens=g.tokens, slot_rows=g.rows, lru=g.lru,
+                                pool_rows=g.pool_rows, pool_k=g.pool_k, hot_k=g.hot_k,
+                                out_rows=out)
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    # one eager call first (one-time kernel set-up), then restore the state
+    snap = (g.tokens.clone(), g.lru.clone(), g.hot_k.clone())
+    with torch.cuda.stream(s):
+        hs.swap_in_args(args, stream=s)
+    torch.cuda.synchronize()
+    g.tokens.copy_(snap[0]); g.lru.copy_(snap[1]); g.hot_k.copy_(snap[2])
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=s):
+        hs.swap_in_args(args, stream=s)
+    torch.cuda.synchronize()
+    for step in range(4):
+        ids = ts.next()
+        topk.copy_(torch.from_numpy(ids))
+        graph.replay()
+        torch.cuda.synchronize()
+        ref.topk = ids
+        r_out, _, _, _ = cases.run_oracle(ref)
+        np.testing.assert_array_equal(out.cpu().numpy(), r_out)
+        g.assert_matches(ref, f"graph step {step}")
