@@ -1,0 +1,759 @@
+#!/usr/bin/env python
+"""Benchmark of the HiSparse decode-time swap-in on GB300.
+
+Headline workload: the DeepSeek-V3.2-shaped decode step -- 61 layers, each a
+swap-in of batch 32, top_k 2048, hot_size 4096 (+1 newest slot), 656-byte MLA
+rows, a per-layer pool of 32 x 128K rows in HBM, 90 % step-to-step reuse.  One
+step = 61 per-layer hs_swap_in launches, captured as one CUDA graph per step and
+replayed back to back.  value = miss rows copied per second (whole job).
+
+Also measured in the same run and reported under "ops": the store_kv scatter
+(4096 tokens, K and V bf16 [8 x 128]), the tiny swap-in, the indexer-row and
+high-miss swap-ins from pinned host pools, the 61-layer all-layer transfer, and
+the host-link read bandwidth that bounds the host-sourced ones.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "swap-in rows/s and µs per decode step; achieved GB/s vs HBM / host-link roofline"
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+GiB = 1 << 30
+
+
+def log(*a):
+    print("[bench]", *a, file=sys.stderr, flush=True)
+
+
+# --------------------------------------------------------------------------- clocks
+class NvmlSampler:
+    """Samples SM clock and clock-event reasons through NVML (read-only) on a
+    background thread while a region runs."""
+
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x100: "display_clock_setting"}
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        self.ok = False
+        self.samples = []
+        self.period = period_s
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            bus = None
+            try:
+                p = torch.cuda.get_device_properties(device_index)
+                bus = "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+            except Exception:
+                pass
+            rc = 1
+            if bus is not None:
+                rc = self.nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h))
+            if rc != 0:
+                rc = self.nv.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(self.h))
+            if rc != 0:
+                return
+            mx = ctypes.c_uint()
+            self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+            self.max_mhz = mx.value
+            self.ok = True
+        except OSError:
+            pass
+
+    def _one(self):
+        mhz = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(mhz))
+        f = getattr(self.nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        f(self.h, ctypes.byref(rs))
+        return mhz.value, rs.value
+
+    def start(self):
+        self.samples = []
+        self._stop = threading.Event()
+        if not self.ok:
+            return
+        if self.ok:
+            self.samples.append(self._one())
+
+        def run():
+            while not self._stop.is_set():
+                self.samples.append(self._one())
+                time.sleep(self.period)
+
+        self.t = threading.Thread(target=run, daemon=True)
+        self.t.start()
+
+    def stop(self):
+        if not self.ok:
+            return
+        self._stop.set()
+        self.t.join()
+        self.samples.append(self._one())
+
+    def summary(self, smi_csv: str | None):
+        out = {"source": "nvml samples during the timed region", "samples": len(self.samples)}
+        if self.samples:
+            mhz = [m for m, _ in self.samples]
+            reasons = set()
+            for _, r in self.samples:
+                for bit, name in self.REASONS.items():
+                    if r & bit and name != "gpu_idle":
+                        reasons.add(name)
+            out.update(sm_mhz=statistics.median(mhz), sm_min_mhz=min(mhz),
+                       sm_max_mhz=getattr(self, "max_mhz", None), reasons=sorted(reasons))
+        if smi_csv:
+            out["nvidia_smi"] = smi_csv
+        return out
+
+
+def start_smi(index: int, path: str):
+    try:
+        f = open(path, "w")
+        p = subprocess.Popen(
+            ["nvidia-smi", f"--id={index}",
+             "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+             "--format=csv", "-lms", "200"], stdout=f, stderr=subprocess.DEVNULL)
+        return p, f
+    except OSError:
+        return None, None
+
+
+def stop_smi(p, f, path):
+    if p is None:
+        return None
+    p.terminate()
+    try:
+        p.wait(5)
+    except subprocess.TimeoutExpired:
+        p.kill()
+    f.close()
+    lines = [ln.strip() for ln in open(path) if ln.strip() and not ln.startswith("index")]
+    return f"{len(lines)} nvidia-smi samples; last: {lines[-1] if lines else 'none'}"
+
+
+# --------------------------------------------------------------------------- helpers
+def peaks():
+    if os.path.exists(PEAKS_PATH):
+        p = json.load(open(PEAKS_PATH))
+        return float(p["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(name: str, sources):
+    """Per-launch DRAM bytes from a committed ncu summary, valid only while the
+    kernel sources hash the same as when the counters were taken."""
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch=(\d+)\s+source_sha256=([0-9a-f]+)", text)
+    if not m:
+        return None
+    h = hashlib.sha256()
+    for s in sources:
+        h.update(open(os.path.join(ROOT, s), "rb").read())
+    return int(m.group(1)) if h.hexdigest()[:16] == m.group(2)[:16] else None
+
+
+def kernel_source_hash(sources):
+    h = hashlib.sha256()
+    for s in sources:
+        h.update(open(os.path.join(ROOT, s), "rb").read())
+    return h.hexdigest()[:16]
+
+
+SWAP_IN_SOURCES = ["sparse_attention_kv_row_gb300/csrc/hs_swap_in.cu",
+                   "sparse_attention_kv_row_gb300/csrc/hs_device.cuh"]
+
+
+def swapin_alg_bytes(B, K, H, S, launches, misses, with_v=False):
+    """Algorithmic bytes of `launches` swap-in launches of B rows that copied
+    `misses` rows in total: per row 4K ids + 2H lru + 4H slot tokens read,
+    4K slot rows for the outputs, 8 bytes of pool-row lookup per miss, 4K
+    output + 2H lru written, 4 bytes of slot token per miss, and the miss rows
+    read and written (2S per miss, twice with V)."""
+    per_row = 4 * K + 6 * H + 4 * K + 4 * K + 2 * H
+    per_miss = 8 + 4 + 2 * S * (2 if with_v else 1)
+    return launches * B * per_row + misses * per_miss
+
+
+class SwapInWorkload:
+    """Device state, pools and top-k stream of one swap-in configuration."""
+
+    def __init__(self, cfg, dev, layers, rank, pool_host=False, n_pools=None, seed_off=0,
+                 shared_pool=False):
+        import sparse_attention_kv_row_gb300 as hs
+
+        self.hs = hs
+        self.cfg, self.dev, self.layers = cfg, dev, layers
+        B, H, S, L = cfg.batch, cfg.hot_size, cfg.row_bytes, cfg.seq_len
+        self.n_pools = n_pools or layers
+        self.pools = []
+        stage = None
+        P = L if shared_pool else B * L
+        for p in range(self.n_pools):
+            key = synth.stream_key(cfg.seed, rank, p)
+            if pool_host:
+                t = torch.empty((P, S), dtype=torch.uint8, pin_memory=True)
+                chunk = max(1, (1 << 30) // S)
+                stage = stage if stage is not None else torch.empty((chunk, S), dtype=torch.uint8,
+                                                                     device=dev)
+                for r0 in range(0, P, chunk):
+                    r1 = min(P, r0 + chunk)
+                    synth.fill_rows_torch(stage[: r1 - r0], key, first_row=r0)
+                    t[r0:r1].copy_(stage[: r1 - r0])
+                torch.cuda.synchronize()
+            else:
+                t = torch.empty((P, S), dtype=torch.uint8, device=dev)
+                synth.fill_rows_torch(t, key)
+            self.pools.append(t)
+        del stage
+        self.tokens, self.rows, self.lru, self.pool_rows, self.hot = [], [], [], [], []
+        ar = torch.arange(B, device=dev, dtype=torch.int64)[:, None]
+        for l in range(layers):
+            self.tokens.append(torch.full((B, H + 1), -1, dtype=torch.int32, device=dev))
+            self.rows.append(torch.arange(B * (H + 1), dtype=torch.int32, device=dev).view(
+                B, H + 1))
+            self.lru.append(torch.arange(H, dtype=torch.int16, device=dev).repeat(B, 1))
+            if shared_pool:  # every row maps its tokens onto one shared pool, permuted
+                gp = torch.Generator(device=dev)
+                gp.manual_seed(cfg.seed * 31 + l)
+                self.pool_rows.append(torch.stack([torch.randperm(L, generator=gp, device=dev)
+                                                   for _ in range(B)]))
+            else:
+                self.pool_rows.append(ar * L + torch.arange(L, device=dev,
+                                                            dtype=torch.int64)[None])
+            self.hot.append(torch.zeros((B * (H + 1), S), dtype=torch.uint8, device=dev))
+        self.seq = torch.full((B,), L, dtype=torch.int32, device=dev)
+        self.req = torch.arange(B, dtype=torch.int32, device=dev)
+        self.stats = torch.zeros(2, dtype=torch.int64, device=dev)
+        self.miss = [torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(layers)]
+        self.out = [torch.zeros((B, cfg.top_k), dtype=torch.int32, device=dev)
+                    for _ in range(layers)]
+        self.stream = synth.TopkStreamTorch(cfg.seed * 1000 + rank * 7 + seed_off, layers * B,
+                                            cfg.top_k, L, cfg.reuse, dev)
+
+    def next_topk(self):
+        return self.stream.next().view(self.layers, self.cfg.batch, self.cfg.top_k)
+
+    def args(self, l, topk, out=None, miss=None):
+        return self.hs.make_swap_in_args(
+            topk_ids=topk, seq_lens=self.seq, req_state=self.req, slot_tokens=self.tokens[l],
+            slot_rows=self.rows[l], lru=self.lru[l], pool_rows=self.pool_rows[l],
+            pool_k=self.pools[l % self.n_pools], hot_k=self.hot[l],
+            out_rows=self.out[l] if out is None else out,
+            miss_count=self.miss[l] if miss is None else miss, stats=self.stats)
+
+    def eager_step(self, topk, stream):
+        for l in range(self.layers):
+            self.hs.swap_in_args(self.args(l, topk[l]), stream)
+
+    def capture_step(self, topk, stream, out=None, miss=None):
+        g = torch.cuda.CUDAGraph()
+        argv = [self.args(l, topk[l], None if out is None else out[l],
+                          None if miss is None else miss[l]) for l in range(self.layers)]
+        with torch.cuda.graph(g, stream=stream):
+            for a in argv:
+                self.hs.swap_in_args(a, stream)
+        return g
+
+    def free(self):
+        for name in ("pools", "tokens", "rows", "lru", "pool_rows", "hot", "miss", "out"):
+            setattr(self, name, [])
+
+
+def timed_graphs(graphs, stream):
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for g in graphs:
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+# --------------------------------------------------------------------------- headline
+def headline_cfg(args):
+    cfg = synth.DSV32
+    if args.layers and args.layers != cfg.layers:
+        import dataclasses
+
+        cfg = dataclasses.replace(cfg, layers=args.layers,
+                                  name=cfg.name + f" [profiling subset: {args.layers} layers]")
+    return cfg
+
+
+def run_headline(args, dev, rank, world, dist):
+    cfg = headline_cfg(args)
+    B, K, H, S, L, NL = (cfg.batch, cfg.top_k, cfg.hot_size, cfg.row_bytes, cfg.seq_len,
+                         cfg.layers)
+    free, _ = torch.cuda.mem_get_info(dev)
+    pool_bytes = B * L * S
+    steps_total = args.warmup + args.steps
+    per_layer_state = B * (H + 1) * 8 + B * H * 2 + B * L * 8 + B * (H + 1) * S + B * K * 8
+    need_other = NL * per_layer_state + steps_total * NL * B * K * 4 + 2 * NL * B * K * 4
+    budget = free - 12 * GiB - need_other
+    n_pools = int(max(1, min(NL, budget // pool_bytes)))
+    log(f"headline: {n_pools} distinct pools of {pool_bytes / GiB:.2f} GiB, free "
+        f"{free / GiB:.0f} GiB")
+    t0 = time.time()
+    w = SwapInWorkload(cfg, dev, NL, rank, n_pools=n_pools)
+    s = torch.cuda.Stream(dev)
+    # untimed warm-up to the steady state (ceil(H / fresh) + 1 steps)
+    with torch.cuda.stream(s):
+        for _ in range(cfg.warm_steps):
+            w.eager_step(w.next_topk(), s)
+    torch.cuda.synchronize()
+    log(f"headline: set-up and {cfg.warm_steps} warm-up steps in {time.time() - t0:.1f}s")
+    topks = [w.next_topk().clone() for _ in range(steps_total)]
+    graphs = [w.capture_step(t, s) for t in topks]
+    torch.cuda.synchronize()
+    warm, timed = graphs[: args.warmup], graphs[args.warmup:]
+    timed_graphs(warm, s)
+
+    # e2e leg inputs: continue the stream, pinned host copies
+    n_e2e = min(args.steps, 32)
+    e2e_host = [w.next_topk().cpu().pin_memory() for _ in range(n_e2e)]
+    topk_dev = torch.empty((NL, B, K), dtype=torch.int32, device=dev)
+    out_dev = torch.empty((NL, B, K), dtype=torch.int32, device=dev)
+    miss_dev = torch.empty((NL, B), dtype=torch.int32, device=dev)
+    out_host = torch.empty((NL, B, K), dtype=torch.int32, pin_memory=True)
+    miss_host = torch.empty((NL, B), dtype=torch.int32, pin_memory=True)
+    g_e2e = w.capture_step(topk_dev, s, out=out_dev, miss=miss_dev)
+    torch.cuda.synchronize()
+
+    smi_path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
+    os.makedirs(os.path.dirname(smi_path), exist_ok=True)
+    smi, smi_f = start_smi(dev.index, smi_path)
+    sampler = NvmlSampler(dev.index)
+    w.stats.zero_()
+    if dist:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t_dev = timed_graphs(timed, s)
+    sampler.stop()
+    if dist:
+        torch.distributed.barrier()
+    hits, misses = (int(x) for x in w.stats.cpu())
+
+    # e2e: host top-k -> device, graph, outputs -> host, every step
+    w.stats.zero_()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.perf_counter()
+    e0.record(s)
+    with torch.cuda.stream(s):
+        for hb in e2e_host:
+            topk_dev.copy_(hb, non_blocking=True)
+            g_e2e.replay()
+            out_host.copy_(out_dev, non_blocking=True)
+            miss_host.copy_(miss_dev, non_blocking=True)
+    e1.record(s)
+    torch.cuda.synchronize()
+    t_e2e = e0.elapsed_time(e1) / 1e3
+    wall_e2e = time.perf_counter() - wall0
+    e2e_misses = int(w.stats[1].item())
+    smi_summary = stop_smi(smi, smi_f, smi_path)
+
+    launches = NL * args.steps
+    alg = swapin_alg_bytes(B, K, H, S, launches, misses)
+    res = dict(t_dev=t_dev, hits=hits, misses=misses, launches=launches, alg_bytes=alg,
+               n_pools=n_pools, t_e2e=t_e2e, wall_e2e=wall_e2e, e2e_misses=e2e_misses,
+               e2e_steps=n_e2e, h2d=NL * B * K * 4, d2h=NL * B * K * 4 + NL * B * 4,
+               clocks=sampler.summary(smi_summary))
+    del graphs, g_e2e
+    w.free()
+    torch.cuda.empty_cache()
+    return res
+
+
+# --------------------------------------------------------------------------- other ops
+def flush_l2(buf):
+    buf.fill_(1)
+
+
+def time_launches(fn, reps, stream, flush):
+    """Mean device time of fn() over reps launches, L2 flushed before each."""
+    ts = []
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            flush_l2(flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ts.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) / 1e3 for a, b in ts)
+
+
+def run_store_kv(dev, hbm_peak, flush, stream):
+    import sparse_attention_kv_row_gb300 as hs
+
+    c = synth.STORE_KV
+    n, heads, hd, rows = c["n_tokens"], c["heads"], c["head_dim"], c["pool_rows"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(c["seed"])
+    k = torch.randn((n, heads, hd), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((n, heads, hd), generator=g, device=dev).to(torch.bfloat16)
+    kd = torch.zeros((rows, heads, hd), dtype=torch.bfloat16, device=dev)
+    vd = torch.zeros((rows, heads, hd), dtype=torch.bfloat16, device=dev)
+    loc = torch.randperm(rows, generator=g, device=dev)[:n]
+    S = heads * hd * 2
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            hs.store_kv(k, v, kd, vd, loc, stream=stream)
+    t = time_launches(lambda: hs.store_kv(k, v, kd, vd, loc, stream=stream), 30, stream, flush)
+    alg = 2 * 2 * n * S + 8 * n
+    del kd, vd
+    torch.cuda.empty_cache()
+    return dict(workload=c["name"], us_per_call=t * 1e6, alg_bytes=alg, gbs=alg / t / 1e9,
+                roofline=dict(bound="hbm", achieved=alg / t / 1e9, peak=hbm_peak,
+                              frac=alg / t / 1e9 / hbm_peak), launches_timed=30,
+                l2="flushed (256 MiB write) before every launch")
+
+
+def run_host_link_peak(dev, stream, pinned):
+    import sparse_attention_kv_row_gb300 as hs
+
+    sink = torch.zeros(1, dtype=torch.int64, device=dev)
+    n = min(pinned.numel(), 4 * GiB) // 16 * 16
+    view = pinned.view(-1)[:n]
+    with torch.cuda.stream(stream):
+        hs.probe_read(view, sink, stream=stream)
+    torch.cuda.synchronize()
+    t_zc = time_launches(lambda: hs.probe_read(view, sink, stream=stream), 5, stream,
+                         torch.empty(16, device=dev))
+    dst = torch.empty(n, dtype=torch.uint8, device=dev)
+    t_cp = time_launches(lambda: dst.copy_(view, non_blocking=True), 5, stream,
+                         torch.empty(16, device=dev))
+    del dst
+    zc, cp = n / t_zc / 1e9, n / t_cp / 1e9
+    return dict(zero_copy_read_gbs=zc, memcpy_h2d_gbs=cp, peak_gbs=max(zc, cp),
+                bytes=n, note="higher of a zero-copy streaming-read kernel and a pinned "
+                              "cudaMemcpyAsync; measured in this run")
+
+
+def run_swapin_cfg(cfg, dev, stream, steps, hbm_peak, link_peak, flush=None, shared_pool=False):
+    """A single-layer swap-in workload timed as graphs of one launch per step."""
+    B, K, H, S = cfg.batch, cfg.top_k, cfg.hot_size, cfg.row_bytes
+    w = SwapInWorkload(cfg, dev, 1, 0, pool_host=cfg.pool_in_host, shared_pool=shared_pool)
+    with torch.cuda.stream(stream):
+        for _ in range(cfg.warm_steps):
+            w.eager_step(w.next_topk(), stream)
+    torch.cuda.synchronize()
+    topks = [w.next_topk().clone() for _ in range(steps + 2)]
+    graphs = [w.capture_step(t, stream) for t in topks]
+    timed_graphs(graphs[:2], stream)
+    w.stats.zero_()
+    torch.cuda.synchronize()
+    if flush is not None:
+        ts = []
+        for g in graphs[2:]:
+            flush_l2(flush)
+            ts.append(timed_graphs([g], stream))
+        t = sum(ts)
+    else:
+        t = timed_graphs(graphs[2:], stream)
+    hits, misses = (int(x) for x in w.stats.cpu())
+    alg = swapin_alg_bytes(B, K, H, S, steps, misses)
+    link_bytes = misses * S
+    res = dict(workload=cfg.name, us_per_call=t / steps * 1e6, rows_per_s=misses / t,
+               miss_rows_per_call=misses / steps, topk_entries_per_s=steps * B * K / t,
+               alg_bytes_per_call=alg / steps, gbs=alg / t / 1e9, launches_timed=steps)
+    if cfg.pool_in_host:
+        res["roofline"] = dict(bound="host_link", achieved=link_bytes / t / 1e9,
+                               peak=link_peak, frac=link_bytes / t / 1e9 / link_peak,
+                               unit="GB/s", note="bytes over the host link = miss rows")
+    else:
+        res["roofline"] = dict(bound="hbm", achieved=alg / t / 1e9, peak=hbm_peak,
+                               frac=alg / t / 1e9 / hbm_peak, unit="GB/s")
+    del graphs
+    w.free()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_transfer(dev, stream, link_peak, hot_rows_target):
+    import sparse_attention_kv_row_gb300 as hs
+
+    c = synth.TRANSFER
+    NL, S = c["layers"], c["row_bytes"]
+    st = synth.STRESS
+    src_rows = st.seq_len  # one request's worth of rows per layer (pinned budget)
+    n = 78592
+    g = torch.Generator(device=dev)
+    g.manual_seed(c["seed"])
+    stage = torch.empty((src_rows, S), dtype=torch.uint8, device=dev)
+    src = []
+    for l in range(NL):
+        t = torch.empty((src_rows, S), dtype=torch.uint8, pin_memory=True)
+        synth.fill_rows_torch(stage, synth.stream_key(c["seed"], l))
+        t.copy_(stage)
+        src.append(t)
+    del stage
+    dst_rows = hot_rows_target
+    dst = [torch.zeros((dst_rows, S), dtype=torch.uint8, device=dev) for _ in range(NL)]
+    src_idx = torch.randperm(src_rows, generator=g, device=dev)[:n]
+    dst_idx = torch.randperm(dst_rows, generator=g, device=dev)[:n]
+    ptrs = (hs.layer_pointer_array(src, dev), hs.layer_pointer_array(dst, dev))
+    torch.cuda.synchronize()
+    fn = lambda: hs.transfer_kv_layers(src, dst, src_idx, dst_idx, stream=stream, ptrs=ptrs)  # noqa
+    with torch.cuda.stream(stream):
+        fn()
+    torch.cuda.synchronize()
+    t = time_launches(fn, 3, stream, torch.empty(16, device=dev))
+    link_bytes = n * NL * S
+    alg = 2 * n * NL * S + 16 * n
+    # sampled check of the property dst_l[dst_idx[i]] == src_l[src_idx[i]]
+    rng = np.random.default_rng(1)
+    ok = True
+    si, di = src_idx.cpu().numpy(), dst_idx.cpu().numpy()
+    for _ in range(32):
+        l, i = int(rng.integers(NL)), int(rng.integers(n))
+        ok &= bool(torch.equal(dst[l][di[i]].cpu(), src[l][si[i]]))
+    res = dict(workload=c["name"] + f" (src pools {src_rows} rows/layer pinned; dst 61 HBM "
+                                    f"buffers of {dst_rows} rows; indices seeded distinct)",
+               ms_per_call=t * 1e3, rows_per_s=n * NL / t, alg_bytes=alg, gbs=alg / t / 1e9,
+               sampled_check_ok=ok,
+               roofline=dict(bound="host_link", achieved=link_bytes / t / 1e9, peak=link_peak,
+                             frac=link_bytes / t / 1e9 / link_peak, unit="GB/s"))
+    del src, dst
+    torch.cuda.empty_cache()
+    return res
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def cpu_oracle_sample(seconds: float, max_steps: int | None = None, extra_warm: int = 0):
+    """The oracle, as it stands, on one layer of the headline workload (32 rows,
+    real memcpy from a 2.75 GB host pool), single-threaded."""
+    import oracle
+
+    cfg = synth.DSV32
+    B, K, H, S, L = cfg.batch, cfg.top_k, cfg.hot_size, cfg.row_bytes, cfg.seq_len
+    if torch.cuda.is_available():  # generate on the GPU when there is one (untimed)
+        g = torch.empty((B * L, S), dtype=torch.uint8, device="cuda")
+        synth.fill_rows_torch(g, synth.stream_key(cfg.seed, 0, 0))
+        pool = g.cpu().numpy()
+        del g
+        torch.cuda.empty_cache()
+    else:
+        pool = np.empty((B * L, S), dtype=np.uint8)
+        synth.fill_rows_torch(torch.from_numpy(pool), synth.stream_key(cfg.seed, 0, 0),
+                              chunk_words=1 << 24)
+    tokens, rows, lru = synth.cold_state(B, H)
+    pool_rows = (np.arange(B, dtype=np.int64)[:, None] * L + np.arange(L, dtype=np.int64)[None])
+    hot = np.zeros((B * (H + 1), S), np.uint8)
+    seq = np.full(B, L, np.int64)
+    req = np.arange(B, dtype=np.int64)
+    out = np.empty((B, K), np.int32)
+    stats = np.zeros(2, np.uint64)
+    ts = synth.TopkStream(cfg.seed, 0, B, K, L, cfg.reuse)
+
+    def step(ids):
+        oracle.swap_in(topk_ids=ids, seq_lens=seq, req_state=req, slot_tokens=tokens,
+                       slot_rows=rows, lru=lru, pool_rows=pool_rows, pool_k=pool, hot_k=hot,
+                       out_rows=out, hot_size=H, stats=stats)
+
+    for _ in range(cfg.warm_steps + extra_warm):
+        step(ts.next())
+    stats[:] = 0
+    spent, steps = 0.0, 0
+    while spent < seconds and (max_steps is None or steps < max_steps):
+        ids = ts.next()
+        t0 = time.perf_counter()
+        step(ids)
+        spent += time.perf_counter() - t0
+        steps += 1
+    misses = int(stats[1])
+    return dict(value=misses / spent, unit="rows/s", cores=1, kind="oracle",
+                sample=f"{steps} decode steps of 1 of the 61 layers (all 32 rows, warm "
+                       f"state, 2.75 GB host pool, real row memcpy), single thread; "
+                       f"{spent:.1f} s of oracle time",
+                seconds=spent, steps=steps, misses=misses,
+                cpu=_cpu_model(), nproc=os.cpu_count())
+
+
+def _cpu_model():
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part", "hardware")):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# --------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: fewer layers than the workload's 61")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        # warm-up decode steps untimed, then exactly `steps` timed ones
+        r = cpu_oracle_sample(seconds=1e9, max_steps=args.steps, extra_warm=args.warmup)
+        cfg = synth.DSV32
+        line = dict(metric=METRIC, value=r["value"], unit="rows/s", n_gpus=args.gpus,
+                    steps=args.steps, warmup=args.warmup,
+                    ms_per_step=r["seconds"] / r["steps"] * 1e3 * cfg.layers,
+                    higher_is_better=True, scaling="weak", vs_baseline=None, dtype="u8",
+                    data="synthetic", impl="reference",
+                    config=dict(workload=cfg.name, batch=cfg.batch, top_k=cfg.top_k,
+                                hot_size=cfg.hot_size, row_bytes=cfg.row_bytes,
+                                layers=cfg.layers, reuse=cfg.reuse,
+                                sample="each step: 1 of the 61 layers, all 32 rows; "
+                                       "ms_per_step scaled to 61 layers"),
+                    cpu_baseline=dict(value=r["value"], unit="rows/s", cores=1, kind="oracle",
+                                      sample=r["sample"]),
+                    e2e=dict(value=r["value"], unit="rows/s", h2d_bytes_per_step=0,
+                             d2h_bytes_per_step=0))
+        print(json.dumps(line), flush=True)
+        return
+
+    dist = world > 1
+    if dist:
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+
+    if rank == 0 or not dist:
+        __graft_entry__.build()
+    if dist:
+        torch.distributed.barrier()
+        __graft_entry__.build()
+    hbm_peak, peak_src = peaks()
+
+    h = run_headline(args, dev, rank, world, dist)
+    t_dev = h["t_dev"]
+    misses = h["misses"]
+    if dist:
+        tt = torch.tensor([t_dev, h["t_e2e"]], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        mm = torch.tensor([misses, h["e2e_misses"], h["alg_bytes"]], dtype=torch.float64,
+                          device=dev)
+        torch.distributed.all_reduce(mm, op=torch.distributed.ReduceOp.SUM)
+        t_dev, t_e2e = float(tt[0]), float(tt[1])
+        misses_all, e2e_all, alg_all = (float(x) for x in mm)
+    else:
+        t_e2e, misses_all, e2e_all, alg_all = h["t_e2e"], misses, h["e2e_misses"], h["alg_bytes"]
+
+    ops = {}
+    if not args.headline_only and rank == 0:
+        s = torch.cuda.Stream(dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        ops["store_kv"] = run_store_kv(dev, hbm_peak, flush, s)
+        ops["tiny_swap_in"] = run_swapin_cfg(synth.TINY, dev, s, 8, hbm_peak, None, flush=flush,
+                                             shared_pool=True)
+        probe_buf = torch.empty(2 * GiB, dtype=torch.uint8, pin_memory=True)
+        link = run_host_link_peak(dev, s, probe_buf)
+        del probe_buf
+        ops["host_link"] = link
+        ops["indexer_swap_in"] = run_swapin_cfg(synth.INDEXER, dev, s, 20, hbm_peak,
+                                                link["peak_gbs"])
+        ops["stress_swap_in"] = run_swapin_cfg(synth.STRESS, dev, s, 10, hbm_peak,
+                                               link["peak_gbs"])
+        ops["transfer_all_layer"] = run_transfer(dev, s, link["peak_gbs"],
+                                                 synth.STRESS.batch * (synth.STRESS.hot_size + 1))
+
+    if rank != 0:
+        if dist:
+            torch.distributed.destroy_process_group()
+        return
+    cpu = cpu_oracle_sample(args.cpu_seconds)
+    cfg = headline_cfg(args)
+    NL = cfg.layers
+    launches = h["launches"]
+    per_launch_bytes = h["alg_bytes"] / launches
+    avg_launch_s = h["t_dev"] / launches
+    achieved = per_launch_bytes / avg_launch_s / 1e9
+    traffic = profile_traffic("swap_in_dsv32.md", SWAP_IN_SOURCES)
+    value = misses_all / t_dev
+    line = dict(
+        metric=METRIC, value=value, unit="rows/s", n_gpus=world, steps=args.steps,
+        warmup=args.warmup, ms_per_step=t_dev / args.steps * 1e3, higher_is_better=True,
+        scaling="weak", vs_baseline=None, dtype="u8", data="synthetic",
+        config=dict(workload=cfg.name, batch=cfg.batch, top_k=cfg.top_k,
+                    hot_size=cfg.hot_size, row_bytes=cfg.row_bytes, layers=NL,
+                    reuse=cfg.reuse, pools_distinct=h["n_pools"],
+                    step="61 per-layer hs_swap_in launches, one CUDA graph per decode step, "
+                         "graphs replayed back to back",
+                    l2="inputs larger than L2 (each step touches ~630 MB across 61 layers)",
+                    parallelism=f"dp{world} (independent requests per GPU)"),
+        us_per_decode_step=t_dev / args.steps * 1e6,
+        topk_entries_per_s=world * args.steps * NL * cfg.batch * cfg.top_k / t_dev,
+        miss_rows_per_step=misses_all / args.steps / world,
+        hit_rows_per_step=h["hits"] / args.steps,
+        gbs=alg_all / t_dev / 1e9,
+        roofline=dict(bound="hbm", achieved=achieved, peak=hbm_peak, unit="GB/s",
+                      frac=achieved / hbm_peak, traffic=traffic, peak_source=peak_src,
+                      kernel="swap_in_kernel (hs_swap_in)",
+                      per_launch_alg_bytes=per_launch_bytes,
+                      avg_launch_us=avg_launch_s * 1e6),
+        cpu_baseline=dict(value=cpu["value"], unit="rows/s", cores=cpu["cores"], kind="oracle",
+                          sample=cpu["sample"], cpu=cpu["cpu"], nproc=cpu["nproc"]),
+        e2e=dict(value=e2e_all / t_e2e, unit="rows/s", h2d_bytes_per_step=h["h2d"],
+                 d2h_bytes_per_step=h["d2h"], steps=h["e2e_steps"],
+                 us_per_step=t_e2e / h["e2e_steps"] * 1e6,
+                 how="every step: pinned-host top-k -> device, the step's 61 swap-ins "
+                     "(CUDA graph through the C ABI), out rows and miss counts -> pinned host"),
+        gpu_launches=launches,
+        clocks=h["clocks"],
+        ops=ops,
+    )
+    print(json.dumps(line), flush=True)
+    if dist:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

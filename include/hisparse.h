@@ -106,9 +106,11 @@ typedef enum hs_err {
  *  miss_count  int32 [batch] or NULL; stats uint64 [2] (+= hits, misses) or NULL;
  *  status      int32 [batch] or NULL (per-row HS_ST_* bits, overwritten)
  *
- * Limits: 1 <= top_k <= hot_size <= 32767 (slots are int16); the row's state
- * must also fit one SM's shared memory (see hs_swap_in_smem_bytes), else
- * HS_ERR_UNSUPPORTED.  hot_num_rows <= INT32_MAX.
+ * Limits: 1 <= top_k <= hot_size <= 32767 (slots are int16).  Each row runs
+ * on a cluster of up to 8 CTAs; every CTA holds the row's ids, LRU order, slot
+ * tokens, slot rows and a hash of 2*top_k..4*top_k entries, plus its share of
+ * the per-position state, and this must fit one CTA's shared memory
+ * (hs_swap_in_smem_bytes), else HS_ERR_UNSUPPORTED.  hot_num_rows <= INT32_MAX.
  * Preconditions (not checked): distinct req_state values within one call;
  * slot_rows values distinct across the slots the call can touch; pool and hot
  * buffers do not overlap; no other work writes these buffers concurrently.
@@ -139,8 +141,9 @@ typedef struct hs_swap_in_args {
 
 hs_err hs_swap_in(const hs_swap_in_args* args, hs_stream_t stream);
 
-/* Shared memory (bytes) one swap-in row needs for (top_k, hot_size); 0 if the
- * pair is outside the limits above. */
+/* Shared memory (bytes) per CTA that a swap-in row needs for (top_k, hot_size)
+ * when split over the largest cluster (8 CTAs); 0 if the pair is outside the
+ * limits above. */
 int64_t hs_swap_in_smem_bytes(int32_t top_k, int32_t hot_size);
 
 /*

@@ -137,3 +137,70 @@ __device__ __forceinline__ uint32_t fast_div(uint32_t n, FastDiv f) {
 }
 
 }  // namespace hs
+
+namespace hs {
+
+// ------------------------------------------------------------------ clusters
+// Thread-block cluster primitives (sm_90+ PTX): rank within the cluster, the
+// shared-memory window of a peer CTA (DSMEM), and split arrive/wait barriers.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address, in the cluster shared window, of `p` (a local shared pointer) in CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_addr(p)), "r"(rank));
+  return out;
+}
+__device__ __forceinline__ int32_t peer_ld(uint32_t addr) {
+  int32_t v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void peer_st(uint32_t addr, int32_t v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void peer_min(uint32_t addr, int32_t v) {
+  asm volatile("red.shared::cluster.min.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void peer_or(uint32_t addr, int32_t v) {
+  asm volatile("red.shared::cluster.or.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
+}
+
+// ------------------------------------------------------------------ block scan
+// Exclusive prefix of `flag` over the threads of the block in thread order;
+// `wsum` is shared scratch of >= 33 ints.  Returns the prefix and, in *total,
+// the block total.  Every thread of the block must call it.
+__device__ __forceinline__ int block_exclusive_count(bool flag, int* wsum, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  const unsigned m = __ballot_sync(kFullMask, flag);
+  if (lane == 0) wsum[warp] = __popc(m);
+  __syncthreads();
+  if (warp == 0) {
+    const int v = lane < nwarps ? wsum[lane] : 0;
+    int t;
+    const int ex = warp_exclusive_scan(v, lane, &t);
+    if (lane < nwarps) wsum[lane] = ex;
+    if (lane == 0) wsum[32] = t;
+  }
+  __syncthreads();
+  const int r = wsum[warp] + __popc(m & ((1u << lane) - 1u));
+  *total = wsum[32];
+  __syncthreads();  // wsum may be reused right away
+  return r;
+}
+
+}  // namespace hs

@@ -3,27 +3,35 @@
 // Defined by SGLang jit_kernel/csrc/hisparse.cuh (load_cache_to_device_buffer
 // and its kernel) with the invalid-entry rules, padding rows and corruption
 // tripwires of vLLM csrc/libtorch_stable/hisparse_kernels.cu
-// (hisparse_resolve_residency_kernel).  One CTA owns one batch row:
+// (hisparse_resolve_residency_kernel).
 //
-//   A  stage    the row's top-k ids, LRU order, slot tokens and slot rows into
-//               shared memory with LDGSTS (coalesced, all in flight at once)
-//               instead of one dependent gather per LRU position;
-//   B  hash     insert valid ids into an open-addressing table (Knuth
-//               multiplicative hash, linear probing, 2K..4K entries); the
-//               smallest entry index per id wins (atomicMin), which makes the
-//               first occurrence of a repeated id the canonical one;
-//   C  walk     every LRU position probes its slot's token; a hit is claimed
-//               by the lowest position (atomicMin), and the lowest position of
-//               each slot is recorded to catch repeated slots;
-//   D  compact  ballot/popc per warp + one warp-wide scan of chunk counts:
-//               hits forward, evictables in LRU order;
-//   E  misses   candidates in top-k order look up their pool row, then the
-//               same ballot/scan assigns the m-th miss the m-th evictable slot;
-//   F  write    LRU order [stale evictables][misses][hits], output row,
-//               counters;
-//   G  copy     (miss, 16-byte chunk) work items spread over all threads of
-//               the CTA: read-only no-L1 loads from the pool (HBM or pinned
-//               host memory), L2-only stores into the hot buffer.
+// One thread-block cluster of C CTAs owns one batch row (C = 1..8, chosen so
+// that batch * C covers the SMs).  CTA j of the cluster owns LRU positions
+// (and slots) [j*P, (j+1)*P) and top-k entries [j*E, (j+1)*E); per-row
+// results cross CTAs through distributed shared memory:
+//
+//   P0 stage    the row's ids, LRU order, slot tokens and slot rows into
+//               shared memory with LDGSTS (all in flight at once);
+//   P1 hash     every CTA hashes all valid ids (Knuth multiplicative hash,
+//               linear probing, one CAS per id); only when an id repeats does a
+//               second pass make the smallest entry index canonical;
+//   P2 walk     each CTA walks its LRU positions: the lowest position of each
+//               slot and the lowest position holding each wanted token win a
+//               red.min into the owning CTA's shared memory;
+//   P3 hits     a position is a hit when it won its entry; hits emit their hot
+//               row, evictables are compacted in LRU order (ballot + scan);
+//   P4 misses   each CTA classifies its entries; candidates look up their pool
+//               row; misses are compacted in top-k order;
+//   P5 assign   counts are exchanged; the m-th miss of the row reads the m-th
+//               evictable from whichever CTA holds it, records its token and
+//               emits the hot row; every CTA writes its part of the new LRU
+//               order [stale evictables][misses][hits] directly;
+//   P6 copy     each CTA copies its misses' rows, (miss, 16-byte chunk) work
+//               items over all its threads: read-only no-L1 loads from the pool
+//               (HBM or pinned host memory), L2-only stores into the hot buffer.
+//
+// Four cluster barriers separate the phases (two of them split arrive/wait so
+// that initialisation and the copy overlap them).
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -38,11 +46,13 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kCopyUnroll = 4;
+constexpr int kMaxCluster = 8;
+constexpr int32_t kUnclaimed = INT_MAX;
 
-struct SwapInLayout {
-  int hash_bits, hash_size;
-  int o_keys, o_vals, o_ids, o_hitpos, o_out, o_tok, o_rows, o_slotpos, o_found, o_lru,
-      o_hits, o_cnt, o_misc;
+struct Layout {
+  int hash_bits, hash_size, slice_p, slice_e;
+  int o_hash, o_ids, o_lru, o_tok, o_rows, o_mark, o_claim, o_found, o_code, o_evl, o_missi,
+      o_jsrc, o_jdst, o_wsum, o_xch, o_misc;
   int total;
 };
 
@@ -52,36 +62,39 @@ __host__ __device__ inline int take(int* o, int bytes) {
   return r;
 }
 
-// Shared-memory layout of one row.  After phase C the hash keys hold the
-// per-entry pool rows (int64 [K]) and the hash values the per-miss entry index
-// (int32 [K]); after phase C the slot-token array holds the evictable list.
-__host__ __device__ inline SwapInLayout make_layout(int K, int H) {
-  SwapInLayout L;
+// Shared-memory layout of one CTA of a row's cluster.  Every CTA uses the same
+// offsets, so a peer's array is addressed by mapping the local address.
+__host__ __device__ inline Layout make_layout(int K, int H, int C) {
+  Layout L;
   int bits = 1;
   while ((1 << bits) < 2 * K) ++bits;
   L.hash_bits = bits;
   L.hash_size = 1 << bits;
+  L.slice_p = (H + C - 1) / C;
+  L.slice_e = (K + C - 1) / C;
   int o = 0;
-  L.o_keys = take(&o, 4 * L.hash_size);
-  L.o_vals = take(&o, 4 * L.hash_size);
-  L.o_ids = take(&o, 4 * K + 16);
-  L.o_hitpos = take(&o, 4 * K);
-  L.o_out = take(&o, 4 * K);
-  L.o_tok = take(&o, 4 * H + 16);
-  L.o_rows = take(&o, 4 * (H + 1) + 16);
-  L.o_slotpos = take(&o, 4 * H);
-  L.o_found = take(&o, 2 * H);
-  L.o_lru = take(&o, 2 * H + 16);
-  L.o_hits = take(&o, 2 * H);
-  const int chunks = ((H > K ? H : K) + 31) / 32;
-  L.o_cnt = take(&o, 4 * chunks);
-  L.o_misc = take(&o, 16);
+  L.o_hash = take(&o, 8 * L.hash_size);           // int2 {key, entry}
+  L.o_ids = take(&o, 4 * K + 16);                 // staged top-k row
+  L.o_lru = take(&o, 2 * H + 16);                 // staged LRU order
+  L.o_tok = take(&o, 4 * H + 16);                 // staged slot tokens [0, H)
+  L.o_rows = take(&o, 4 * (H + 1) + 16);          // staged slot rows [0, H]
+  L.o_mark = take(&o, 4 * L.slice_p);             // my slots: lowest position
+  L.o_claim = take(&o, 4 * L.slice_e);            // my entries: lowest hit position
+  L.o_found = take(&o, 4 * L.slice_p);            // my positions: wanted entry / -1 / -2
+  L.o_code = take(&o, 4 * L.slice_p);             // my positions: hit rank or ~evict rank
+  L.o_evl = take(&o, 4 * L.slice_p);              // my evictables (slot | bad << 16)
+  L.o_missi = take(&o, 4 * L.slice_e);            // my misses: entry index
+  L.o_jsrc = take(&o, 8 * L.slice_e);             // my misses: pool row
+  L.o_jdst = take(&o, 4 * L.slice_e);             // my misses: hot row or -1
+  L.o_wsum = take(&o, 4 * 40);                    // block-scan scratch
+  L.o_xch = take(&o, 4 * 3 * kMaxCluster);        // per-CTA hits, misses, flags
+  L.o_misc = take(&o, 4 * 8);
   L.total = o;
   return L;
 }
 
 struct SwapInParams {
-  int32_t top_k, hot_size;
+  int32_t top_k, hot_size, cluster;
   const int32_t* num_real;
   const int32_t* topk_ids;
   int64_t topk_stride;
@@ -112,23 +125,20 @@ struct SwapInParams {
   FastDiv div_chunks;
 };
 
-enum { kMiscFlags = 0, kMiscHits = 1, kMiscMisses = 2 };
-constexpr int32_t kWant = INT_MAX;  // hitpos of a wanted, not yet hit entry
-constexpr int32_t kDone = -1;       // hitpos of an entry that is never a hit
+enum { kMiscFlags = 0, kMiscPeerFlags = 1, kMiscRepeat = 2 };
 
 __device__ __forceinline__ uint32_t hash_of(int32_t key, int bits) {
   return (static_cast<uint32_t>(key) * 2654435761u) >> (32 - bits);
 }
 
-// Entry index stored for `key`, or -1 when the key is absent.
-__device__ __forceinline__ int32_t hash_find(const int32_t* keys, const int32_t* vals,
-                                             int32_t key, int bits) {
+// Canonical entry index stored for `key`, or -1 when the key is absent.
+__device__ __forceinline__ int32_t hash_find(const int2* tab, int32_t key, int bits) {
   const uint32_t mask = (1u << bits) - 1u;
   uint32_t h = hash_of(key, bits);
   for (uint32_t n = 0; n <= mask; ++n) {
-    const int32_t k = keys[h];
-    if (k == key) return vals[h];
-    if (k == -1) return -1;
+    const int2 kv = tab[h];
+    if (kv.x == key) return kv.y;
+    if (kv.x == -1) return -1;
     h = (h + 1u) & mask;
   }
   return -1;
@@ -155,16 +165,16 @@ struct Chunk<1> {
   static __device__ __forceinline__ void st(unsigned char* p, T v) { st_l2_u8(p, v); }
 };
 
-// Phase G: copy every applied miss row, work item = (miss m, chunk c).
+// P6: copy this CTA's applied misses, work item = (miss, chunk).
 template <int G>
-__device__ __forceinline__ void copy_misses(const SwapInParams& p, const unsigned char* pool,
-                                            unsigned char* hot, int M, const int32_t* missi,
-                                            const int32_t* out_s, const int64_t* pr_s) {
-  using C = Chunk<G>;
+__device__ __forceinline__ void copy_rows(const SwapInParams& p, const unsigned char* pool,
+                                          unsigned char* hot, int n, const int64_t* jsrc,
+                                          const int32_t* jdst) {
+  using Ch = Chunk<G>;
   const uint32_t cpr = p.chunks_per_row;
-  const uint32_t total = static_cast<uint32_t>(M) * cpr;
+  const uint32_t total = static_cast<uint32_t>(n) * cpr;
   for (uint32_t w0 = threadIdx.x; w0 < total; w0 += kThreads * kCopyUnroll) {
-    typename C::T v[kCopyUnroll];
+    typename Ch::T v[kCopyUnroll];
     unsigned char* dst[kCopyUnroll];
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u) {
@@ -173,18 +183,17 @@ __device__ __forceinline__ void copy_misses(const SwapInParams& p, const unsigne
       if (w < total) {
         const uint32_t m = cpr == 1 ? w : fast_div(w, p.div_chunks);
         const uint32_t c = w - m * cpr;
-        const int32_t i = missi[m];
-        const int32_t d = out_s[i];
+        const int32_t d = jdst[m];
         if (d >= 0) {
           const int64_t off = static_cast<int64_t>(c) * G;
-          v[u] = C::ld(pool + pr_s[i] * p.row_bytes + off);
+          v[u] = Ch::ld(pool + jsrc[m] * p.row_bytes + off);
           dst[u] = hot + static_cast<int64_t>(d) * p.row_bytes + off;
         }
       }
     }
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u)
-      if (dst[u] != nullptr) C::st(dst[u], v[u]);
+      if (dst[u] != nullptr) Ch::st(dst[u], v[u]);
   }
 }
 
@@ -192,15 +201,16 @@ template <typename SeqT, typename ReqT, int G>
 __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  const int warp = tid >> 5;
-  const int b = blockIdx.x;
+  const int C = p.cluster;
+  const int j = static_cast<int>(cluster_rank());
+  const int b = blockIdx.x / C;
   const int K = p.top_k;
   const int H = p.hot_size;
-  const SwapInLayout L = make_layout(K, H);
-  const unsigned lanes_before = (1u << lane) - 1u;
+  const Layout L = make_layout(K, H, C);
+  const int p0 = min(H, j * L.slice_p), p1 = min(H, p0 + L.slice_p);  // my positions / slots
+  const int e0 = min(K, j * L.slice_e), e1 = min(K, e0 + L.slice_e);  // my entries
 
-  // ---- A: stage the top-k row first; it does not depend on the state row.
+  // ---- P0: stage the top-k row first; it does not depend on the state row.
   const int32_t* ids_g = p.topk_ids + static_cast<int64_t>(b) * p.topk_stride;
   int32_t* ids = reinterpret_cast<int32_t*>(smem + L.o_ids +
                                             (reinterpret_cast<uintptr_t>(ids_g) & 15u));
@@ -213,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
 
   if (pad_nr || r < 0 || r >= p.num_states) {  // padding row / bad state row
     cp_async_commit_wait_all();
-    for (int i = tid; i < K; i += kThreads) out_g[i] = -1;
-    if (tid == 0) {
+    for (int i = e0 + tid; i < e1; i += kThreads) out_g[i] = -1;
+    if (j == 0 && tid == 0) {
       if (p.miss_count) p.miss_count[b] = 0;
       if (p.status) p.status[b] = (pad_nr || r < 0) ? 0 : HS_ST_BAD_STATE;
     }
@@ -226,11 +236,11 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     cp_async_commit_wait_all();
     __syncthreads();
     const int64_t count = Lb < K ? Lb : K;
-    for (int i = tid; i < K; i += kThreads) {
+    for (int i = e0 + tid; i < e1; i += kThreads) {
       const int32_t t = ids[i];
       out_g[i] = (i < count && t >= 0 && t < Lb) ? __ldg(rows_g + t) : -1;
     }
-    if (tid == 0) {
+    if (j == 0 && tid == 0) {
       if (p.miss_count) p.miss_count[b] = 0;
       if (p.status) p.status[b] = 0;
     }
@@ -239,35 +249,40 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
 
   int32_t* tokens_g = p.slot_tokens + r * p.slot_tokens_stride;
   int16_t* lru_g = p.lru + r * p.lru_stride;
+  int16_t* lru = reinterpret_cast<int16_t*>(smem + L.o_lru +
+                                            (reinterpret_cast<uintptr_t>(lru_g) & 15u));
   int32_t* tok = reinterpret_cast<int32_t*>(smem + L.o_tok +
                                             (reinterpret_cast<uintptr_t>(tokens_g) & 15u));
   int32_t* rows = reinterpret_cast<int32_t*>(smem + L.o_rows +
                                              (reinterpret_cast<uintptr_t>(rows_g) & 15u));
-  int16_t* lru = reinterpret_cast<int16_t*>(smem + L.o_lru +
-                                            (reinterpret_cast<uintptr_t>(lru_g) & 15u));
+  stage_bytes(lru, lru_g, 2LL * H, tid, kThreads);
   stage_bytes(tok, tokens_g, 4LL * H, tid, kThreads);
   stage_bytes(rows, rows_g, 4LL * (H + 1), tid, kThreads);
-  stage_bytes(lru, lru_g, 2LL * H, tid, kThreads);
 
-  int32_t* keys = reinterpret_cast<int32_t*>(smem + L.o_keys);
-  int32_t* vals = reinterpret_cast<int32_t*>(smem + L.o_vals);
-  int32_t* hitpos = reinterpret_cast<int32_t*>(smem + L.o_hitpos);
-  int32_t* out_s = reinterpret_cast<int32_t*>(smem + L.o_out);
-  int32_t* slotpos = reinterpret_cast<int32_t*>(smem + L.o_slotpos);
-  int16_t* found = reinterpret_cast<int16_t*>(smem + L.o_found);
-  int16_t* hits = reinterpret_cast<int16_t*>(smem + L.o_hits);
-  int32_t* cnt = reinterpret_cast<int32_t*>(smem + L.o_cnt);
+  int2* tab = reinterpret_cast<int2*>(smem + L.o_hash);
+  int32_t* mark = reinterpret_cast<int32_t*>(smem + L.o_mark);
+  int32_t* claim = reinterpret_cast<int32_t*>(smem + L.o_claim);
+  int32_t* found = reinterpret_cast<int32_t*>(smem + L.o_found);
+  int32_t* code = reinterpret_cast<int32_t*>(smem + L.o_code);
+  int32_t* evl = reinterpret_cast<int32_t*>(smem + L.o_evl);
+  int32_t* missi = reinterpret_cast<int32_t*>(smem + L.o_missi);
+  int64_t* jsrc = reinterpret_cast<int64_t*>(smem + L.o_jsrc);
+  int32_t* jdst = reinterpret_cast<int32_t*>(smem + L.o_jdst);
+  int* wsum = reinterpret_cast<int*>(smem + L.o_wsum);
+  int32_t* xch = reinterpret_cast<int32_t*>(smem + L.o_xch);
   int32_t* misc = reinterpret_cast<int32_t*>(smem + L.o_misc);
-  for (int i = tid; i < L.hash_size; i += kThreads) {
-    keys[i] = -1;
-    vals[i] = INT_MAX;
+  {
+    int4* t4 = reinterpret_cast<int4*>(tab);
+    for (int i = tid; i < L.hash_size / 2; i += kThreads) t4[i] = make_int4(-1, -1, -1, -1);
   }
-  for (int s = tid; s < H; s += kThreads) slotpos[s] = INT_MAX;
-  if (tid < 4) misc[tid] = 0;
+  for (int i = tid; i < p1 - p0; i += kThreads) mark[i] = kUnclaimed;
+  for (int i = tid; i < e1 - e0; i += kThreads) claim[i] = kUnclaimed;
+  if (tid < 8) misc[tid] = 0;
   cp_async_commit_wait_all();
   __syncthreads();
+  cluster_arrive();  // B0 (arrive): my mark / claim arrays are initialised
 
-  // ---- B: hash the valid ids; the smallest entry index per id wins.
+  // ---- P1: hash every valid id; CAS on the key, the winner stores its index.
   const int bits = L.hash_bits;
   const uint32_t hmask = static_cast<uint32_t>(L.hash_size) - 1u;
   for (int i = tid; i < K; i += kThreads) {
@@ -275,9 +290,13 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     if (t >= 0 && t < Lb) {
       uint32_t h = hash_of(t, bits);
       for (uint32_t n = 0; n <= hmask; ++n) {
-        const int32_t old = atomicCAS(&keys[h], -1, t);
-        if (old == -1 || old == t) {
-          atomicMin(&vals[h], i);
+        const int32_t old = atomicCAS(&tab[h].x, -1, t);
+        if (old == -1) {
+          tab[h].y = i;
+          break;
+        }
+        if (old == t) {
+          misc[kMiscRepeat] = 1;  // a repeated id: resolved below
           break;
         }
         h = (h + 1u) & hmask;
@@ -285,167 +304,187 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     }
   }
   __syncthreads();
-
-  int32_t my_flags = 0;
-  for (int i = tid; i < K; i += kThreads) {
-    const int32_t t = ids[i];
-    int32_t hp = kDone, o = -1;
-    if (t >= 0 && t < Lb) {
-      if (hash_find(keys, vals, t, bits) != i) {
-        my_flags |= HS_ST_DUP_ID;  // a later copy of an id: -1
-      } else if (t == Lb - 1) {
-        o = rows[H];  // the newest token lives in slot H
-      } else {
-        hp = kWant;
+  if (misc[kMiscRepeat]) {  // rare: make the smallest index of each id canonical
+    for (int i = tid; i < K; i += kThreads) {
+      const int32_t t = ids[i];
+      if (t >= 0 && t < Lb) {
+        uint32_t h = hash_of(t, bits);
+        for (uint32_t n = 0; n <= hmask; ++n) {
+          if (tab[h].x == t) {
+            atomicMin(&tab[h].y, i);
+            break;
+          }
+          h = (h + 1u) & hmask;
+        }
       }
     }
-    hitpos[i] = hp;
-    out_s[i] = o;
+    __syncthreads();
   }
-  __syncthreads();
+  cluster_wait();  // B0 (wait): every peer's arrays are initialised
 
-  // ---- C: walk the LRU order; the lowest position claims each hit and each slot.
-  for (int q = tid; q < H; q += kThreads) {
+  // ---- P2: walk my LRU positions; lowest position wins each slot and each entry.
+  for (int q = p0 + tid; q < p1; q += kThreads) {
     const int s = lru[q];
     int f = -2;  // -2: slot out of range
     if (s >= 0 && s < H) {
-      atomicMin(&slotpos[s], q);
+      peer_min(peer_addr(&mark[s % L.slice_p], s / L.slice_p), q);
       const int32_t tk = tok[s];
-      f = tk >= 0 ? hash_find(keys, vals, tk, bits) : -1;
-      if (f >= 0) atomicMin(&hitpos[f], q);
-    }
-    found[q] = static_cast<int16_t>(f);
-  }
-  __syncthreads();
-
-  // ---- D: compact positions: hits forward, evictables in LRU order.
-  const int pos_chunks = (H + 31) / 32;
-  for (int base = 0; base < H; base += kThreads) {
-    const int q = base + tid;
-    bool hit = false;
-    if (q < H) {
-      const int f = found[q];
-      hit = f >= 0 && hitpos[f] == q;
-    }
-    const unsigned m = __ballot_sync(kFullMask, hit);
-    if (lane == 0 && base + warp * 32 < H) cnt[(base >> 5) + warp] = __popc(m);
-  }
-  __syncthreads();
-  if (warp == 0) {
-    const int nh = warp_scan_array(cnt, pos_chunks, lane);
-    if (lane == 0) misc[kMiscHits] = nh;
-  }
-  __syncthreads();
-  int32_t* evict = reinterpret_cast<int32_t*>(smem + L.o_tok);  // slot tokens are dead now
-  for (int base = 0; base < H; base += kThreads) {
-    const int q = base + tid;
-    bool hit = false;
-    int f = -2;
-    if (q < H) {
-      f = found[q];
-      hit = f >= 0 && hitpos[f] == q;
-    }
-    const unsigned m = __ballot_sync(kFullMask, hit);
-    if (q < H) {
-      const int before = cnt[q >> 5] + __popc(m & lanes_before);
-      const int s = lru[q];
-      if (hit) {
-        hits[before] = static_cast<int16_t>(s);
-        out_s[f] = rows[s];
-      } else {
-        const bool bad = (f == -2) || slotpos[s] != q;
-        if (bad) my_flags |= HS_ST_BAD_LRU_SLOT;
-        evict[q - before] = (bad ? 0x10000 : 0) | (s & 0xFFFF);
+      f = -1;
+      if (tk >= 0 && tk < Lb && tk != Lb - 1) {
+        const int32_t i = hash_find(tab, tk, bits);
+        if (i >= 0) {
+          f = i;
+          peer_min(peer_addr(&claim[i % L.slice_e], i / L.slice_e), q);
+        }
       }
     }
+    found[q - p0] = f;
   }
-  __syncthreads();
+  cluster_sync();  // B1
 
-  // ---- E: miss candidates in top-k order, pool-row check, slot assignment.
-  int64_t* pr_s = reinterpret_cast<int64_t*>(smem + L.o_keys);  // hash is dead now
-  int32_t* missi = reinterpret_cast<int32_t*>(smem + L.o_vals);
+  // ---- P3: hits and evictables of my positions, in LRU order.
+  int32_t my_flags = 0;
+  int my_h = 0;
+  for (int base = p0; base < p1; base += kThreads) {
+    const int q = base + tid;
+    const bool in = q < p1;
+    bool hit = false, bad = false;
+    int s = 0, f = -2;
+    if (in) {
+      s = lru[q];
+      f = found[q - p0];
+      if (f == -2) {
+        bad = true;
+      } else {
+        bad = peer_ld(peer_addr(&mark[s % L.slice_p], s / L.slice_p)) != q;  // repeated slot
+        hit = !bad && f >= 0 &&
+              peer_ld(peer_addr(&claim[f % L.slice_e], f / L.slice_e)) == q;
+      }
+    }
+    int tot;
+    const int rank = block_exclusive_count(hit, wsum, &tot);
+    if (in) {
+      if (hit) {
+        code[q - p0] = my_h + rank;
+        out_g[f] = rows[s];
+      } else {
+        const int er = (q - p0) - (my_h + rank);
+        evl[er] = (bad ? 0x10000 : 0) | (s & 0xFFFF);
+        code[q - p0] = ~er;
+        if (bad) my_flags |= HS_ST_BAD_LRU_SLOT;
+      }
+    }
+    my_h += tot;
+  }
+
+  // ---- P4: my entries in top-k order: invalid, repeated, newest, hit, miss.
   const int64_t* pool_rows_g = p.pool_rows + r * p.pool_rows_stride;
-  const int ent_chunks = (K + 31) / 32;
-  for (int base = 0; base < K; base += kThreads) {
+  int my_m = 0;
+  for (int base = e0; base < e1; base += kThreads) {
     const int i = base + tid;
     bool miss = false;
-    if (i < K) {
-      int64_t pr = -1;
-      if (hitpos[i] == kWant) {
-        const int32_t t = ids[i];
+    int64_t pr = -1;
+    if (i < e1) {
+      const int32_t t = ids[i];
+      if (t < 0 || t >= Lb) {
+        out_g[i] = -1;
+      } else if (hash_find(tab, t, bits) != i) {
+        out_g[i] = -1;
+        my_flags |= HS_ST_DUP_ID;
+      } else if (t == Lb - 1) {
+        out_g[i] = rows[H];  // the newest token lives in slot H
+      } else if (claim[i - e0] == kUnclaimed) {
         pr = t < p.pool_rows_cols ? __ldg(pool_rows_g + t) : -1;
         if (pr >= 0 && pr < p.pool_num_rows) {
           miss = true;
         } else {
-          pr = -1;
+          out_g[i] = -1;
           my_flags |= HS_ST_BAD_POOL_ROW;
         }
       }
-      pr_s[i] = pr;
     }
-    const unsigned m = __ballot_sync(kFullMask, miss);
-    if (lane == 0 && base + warp * 32 < K) cnt[(base >> 5) + warp] = __popc(m);
-  }
-  __syncthreads();
-  if (warp == 0) {
-    const int nm = warp_scan_array(cnt, ent_chunks, lane);
-    if (lane == 0) misc[kMiscMisses] = nm;
-  }
-  __syncthreads();
-  for (int base = 0; base < K; base += kThreads) {
-    const int i = base + tid;
-    const bool miss = i < K && pr_s[i] >= 0;
-    const unsigned m = __ballot_sync(kFullMask, miss);
+    int tot;
+    const int rank = block_exclusive_count(miss, wsum, &tot);
     if (miss) {
-      const int mm = cnt[i >> 5] + __popc(m & lanes_before);
-      missi[mm] = i;
-      const int32_t e = evict[mm];
-      const int s = static_cast<int16_t>(e & 0xFFFF);
-      if (e >> 16) {
-        out_s[i] = -1;
-        my_flags |= HS_ST_BAD_LRU_SLOT;
-      } else {
-        const int32_t hr = rows[s];
-        if (hr < 0 || hr >= p.hot_num_rows) {
-          out_s[i] = -1;
-          my_flags |= HS_ST_BAD_HOT_ROW;
-        } else {
-          out_s[i] = hr;
-          tokens_g[s] = ids[i];
-        }
-      }
+      missi[my_m + rank] = i;
+      jsrc[my_m + rank] = pr;
     }
+    my_m += tot;
   }
   if (my_flags) atomicOr(&misc[kMiscFlags], my_flags);
   __syncthreads();
-
-  // ---- F: LRU writeback, output row, counters.
-  const int nh = misc[kMiscHits];
-  const int M = misc[kMiscMisses];
-  const int E = H - nh;
-  for (int q = tid; q < H; q += kThreads) {
-    int s;
-    if (q < E - M)
-      s = static_cast<int16_t>(evict[M + q] & 0xFFFF);
-    else if (q < E)
-      s = static_cast<int16_t>(evict[q - (E - M)] & 0xFFFF);
-    else
-      s = hits[q - E];
-    lru_g[q] = static_cast<int16_t>(s);
+  if (tid < C) {  // publish my counts and flags to every CTA of the row
+    peer_st(peer_addr(&xch[j], tid), my_h);
+    peer_st(peer_addr(&xch[kMaxCluster + j], tid), my_m);
+    peer_st(peer_addr(&xch[2 * kMaxCluster + j], tid), misc[kMiscFlags]);
   }
-  for (int i = tid; i < K; i += kThreads) out_g[i] = out_s[i];
-  if (tid == 0) {
+  cluster_sync();  // B2
+
+  // ---- P5: totals, slot assignment for my misses, my part of the LRU order.
+  int NH = 0, M = 0, hit_base = 0, miss_base = 0, all_flags = 0;
+  int ev_base[kMaxCluster + 1];
+  ev_base[0] = 0;
+  for (int o = 0; o < C; ++o) {
+    const int h = xch[o], m = xch[kMaxCluster + o];
+    const int len = min(H, (o + 1) * L.slice_p) - min(H, o * L.slice_p);
+    NH += h;
+    M += m;
+    if (o < j) {
+      hit_base += h;
+      miss_base += m;
+    }
+    ev_base[o + 1] = ev_base[o] + (len - h);
+    all_flags |= xch[2 * kMaxCluster + o];
+  }
+  const int E = H - NH;
+  int32_t late_flags = 0;
+  for (int mm = tid; mm < my_m; mm += kThreads) {
+    const int gm = miss_base + mm;  // the row's gm-th miss takes its gm-th evictable
+    int o = 0;
+    while (o + 1 < C && ev_base[o + 1] <= gm) ++o;
+    const int32_t e = peer_ld(peer_addr(&evl[gm - ev_base[o]], o));
+    const int i = missi[mm];
+    int32_t d = -1;
+    if (!(e >> 16)) {
+      const int s = static_cast<int16_t>(e & 0xFFFF);
+      const int32_t hr = rows[s];
+      if (hr >= 0 && hr < p.hot_num_rows) {
+        d = hr;
+        tokens_g[s] = ids[i];
+      } else {
+        late_flags |= HS_ST_BAD_HOT_ROW;
+      }
+    }
+    out_g[i] = d;
+    jdst[mm] = d;
+  }
+  for (int q = p0 + tid; q < p1; q += kThreads) {
+    const int c = code[q - p0];
+    int pos;
+    if (c >= 0) {
+      pos = E + hit_base + c;
+    } else {
+      const int e = ev_base[j] + ~c;
+      pos = e >= M ? e - M : E - M + e;
+    }
+    lru_g[pos] = lru[q];
+  }
+  if (late_flags) peer_or(peer_addr(&misc[kMiscPeerFlags], 0), late_flags);
+  __syncthreads();
+  cluster_arrive();  // B3 (arrive): no more access to any peer's shared memory
+  if (j == 0 && tid == 0) {
     if (p.miss_count) p.miss_count[b] = M;
-    if (p.status) p.status[b] = misc[kMiscFlags];
     if (p.stats) {
-      atomicAdd(p.stats, static_cast<unsigned long long>(nh));
+      atomicAdd(p.stats, static_cast<unsigned long long>(NH));
       atomicAdd(p.stats + 1, static_cast<unsigned long long>(M));
     }
   }
 
-  // ---- G: copy the missing rows.
-  copy_misses<G>(p, p.pool_k, p.hot_k, M, missi, out_s, pr_s);
-  if (p.pool_v != nullptr) copy_misses<G>(p, p.pool_v, p.hot_v, M, missi, out_s, pr_s);
+  // ---- P6: copy my missing rows.
+  copy_rows<G>(p, p.pool_k, p.hot_k, my_m, jsrc, jdst);
+  if (p.pool_v != nullptr) copy_rows<G>(p, p.pool_v, p.hot_v, my_m, jsrc, jdst);
+  cluster_wait();  // B3 (wait): peers are done with my shared memory
+  if (j == 0 && tid == 0 && p.status) p.status[b] = all_flags | misc[kMiscPeerFlags];
 }
 
 using KernelFn = void (*)(const SwapInParams);
@@ -471,22 +510,26 @@ hs_err ensure_smem(KernelFn fn, int device, int bytes) {
   static Entry table[128];
   static int n = 0;
   std::lock_guard<std::mutex> lock(mu);
-  for (int i = 0; i < n; ++i) {
-    if (table[i].fn == fn && table[i].device == device) {
-      if (table[i].bytes >= bytes) return HS_OK;
-      const cudaError_t e =
-          cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-      if (e != cudaSuccess)
-        return fail(HS_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-      table[i].bytes = bytes;
-      return HS_OK;
-    }
-  }
-  const cudaError_t e =
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  int slot = -1;
+  for (int i = 0; i < n; ++i)
+    if (table[i].fn == fn && table[i].device == device) slot = i;
+  if (slot >= 0 && table[slot].bytes >= bytes) return HS_OK;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return fail(HS_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-  if (n < 128) table[n++] = Entry{fn, device, bytes};
+  if (slot >= 0)
+    table[slot].bytes = bytes;
+  else if (n < 128)
+    table[n++] = Entry{fn, device, bytes};
   return HS_OK;
+}
+
+// Cluster size for a batch: the largest power of two <= 8 with batch * C <=
+// SMs (at least 1), raised while the per-CTA state does not fit shared memory.
+int pick_cluster(int batch, int K, int H, const DeviceInfo& dev) {
+  int C = 1;
+  while (C < kMaxCluster && static_cast<int64_t>(batch) * C * 2 <= dev.sm_count) C *= 2;
+  while (C < kMaxCluster && make_layout(K, H, C).total > dev.max_smem_optin) C *= 2;
+  return C;
 }
 
 }  // namespace
@@ -494,7 +537,7 @@ hs_err ensure_smem(KernelFn fn, int device, int bytes) {
 
 extern "C" int64_t hs_swap_in_smem_bytes(int32_t top_k, int32_t hot_size) {
   if (top_k < 1 || hot_size < 1 || hot_size > 32767 || top_k > hot_size) return 0;
-  return hs::make_layout(top_k, hot_size).total;
+  return hs::make_layout(top_k, hot_size, hs::kMaxCluster).total;
 }
 
 extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
@@ -542,12 +585,15 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   DeviceInfo dev;
   hs_err err = current_device(&dev);
   if (err != HS_OK) return err;
-  const SwapInLayout L = make_layout(a->top_k, a->hot_size);
+  const int C = pick_cluster(a->batch, a->top_k, a->hot_size, dev);
+  const Layout L = make_layout(a->top_k, a->hot_size, C);
   if (L.total > dev.max_smem_optin)
     return fail(HS_ERR_UNSUPPORTED,
-                "hs_swap_in: top_k %d / hot_size %d need %d B of shared memory, the device "
-                "allows %d B",
-                a->top_k, a->hot_size, L.total, dev.max_smem_optin);
+                "hs_swap_in: top_k %d / hot_size %d need %d B of shared memory per CTA even "
+                "split over %d CTAs, the device allows %d B",
+                a->top_k, a->hot_size, L.total, C, dev.max_smem_optin);
+  if (static_cast<int64_t>(a->batch) * C > INT32_MAX)
+    return fail(HS_ERR_UNSUPPORTED, "hs_swap_in: batch too large");
 
   const MemKind pk = classify(a->pool_k);
   const MemKind pv = a->pool_v ? classify(a->pool_v) : MemKind::kDevice;
@@ -574,6 +620,7 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   SwapInParams p;
   p.top_k = a->top_k;
   p.hot_size = a->hot_size;
+  p.cluster = C;
   p.num_real = a->num_real;
   p.topk_ids = a->topk_ids;
   p.topk_stride = a->topk_stride;
@@ -608,8 +655,20 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
                         : (G == 4 ? pick_kernel<4>(a->flags) : pick_kernel<1>(a->flags));
   err = ensure_smem(fn, dev.device, L.total);
   if (err != HS_OK) return err;
-  fn<<<a->batch, kThreads, L.total, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-  const cudaError_t e = cudaGetLastError();
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a->batch) * C, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L.total;
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p);
   if (e != cudaSuccess) return fail(HS_ERR_CUDA, "hs_swap_in launch: %s", cudaGetErrorString(e));
   return HS_OK;
 }

@@ -193,3 +193,66 @@ STORE_KV = dict(name="store_kv scatter: 4096 tokens, K and V [8 x 128] bf16 (204
                 seed=202)
 TRANSFER = dict(name="all-layer transfer_kv: 61 layers x 78,592 pairs of 656 B rows, pinned "
                 "host -> HBM", layers=61, row_bytes=656, seed=606)
+
+
+class TopkStreamTorch:
+    """The same recipe as TopkStream, drawn with torch on any device (used for
+    the large benchmark workloads): per row, step s+1 keeps exactly
+    round(reuse*K) ids of step s chosen uniformly without replacement, draws the
+    other ids uniformly without replacement from [0, seq_len) minus step s's
+    set, and shuffles.  Rows are independent; ``rows`` may span many layers."""
+
+    def __init__(self, seed: int, rows: int, top_k: int, seq_len: int, reuse: float, device):
+        import torch
+
+        assert seq_len >= 2 * top_k, "needs seq_len >= 2*top_k"
+        self.rows, self.top_k, self.seq_len, self.reuse = rows, top_k, seq_len, reuse
+        self.device = torch.device(device)
+        self.gen = torch.Generator(device=self.device)
+        self.gen.manual_seed(seed)
+        self.prev = None
+
+    def _distinct(self, n: int, N: int):
+        """[rows, n] distinct uniform values from [0, N), each row independently."""
+        import torch
+
+        R, dev, g = self.rows, self.device, self.gen
+        if n * n > N:  # dense: random keys, take the n smallest
+            out = torch.empty((R, n), dtype=torch.int64, device=dev)
+            for r0 in range(0, R, 64):
+                r1 = min(R, r0 + 64)
+                keys = torch.rand((r1 - r0, N), generator=g, device=dev)
+                out[r0:r1] = keys.topk(n, dim=1, largest=False).indices
+            return out
+        # sparse: draw with replacement and redraw rows holding a repeat; with
+        # n*n <= N a row is repeat-free with probability >= exp(-1/2)
+        out = torch.randint(0, N, (R, n), generator=g, device=dev)
+        while True:
+            srt = out.sort(dim=1).values
+            bad = (srt[:, 1:] == srt[:, :-1]).any(dim=1)
+            nbad = int(bad.sum())
+            if nbad == 0:
+                return out
+            out[bad] = torch.randint(0, N, (nbad, n), generator=g, device=dev)
+
+    def next(self):
+        import torch
+
+        R, K, L, dev, g = self.rows, self.top_k, self.seq_len, self.device, self.gen
+        if self.prev is None:
+            ids = self._distinct(K, L)
+        else:
+            keep_n = int(round(self.reuse * K))
+            order = torch.rand((R, K), generator=g, device=dev).argsort(dim=1)[:, :keep_n]
+            kept = self.prev.gather(1, order)
+            # the v-th element of [0, L) minus the sorted excluded set e is
+            # v + #{j : e[j] - j <= v}
+            e = self.prev.sort(dim=1).values
+            shifted = e - torch.arange(K, device=dev)[None, :]
+            v = self._distinct(K - keep_n, L - K)
+            fresh = v + torch.searchsorted(shifted, v, right=True)
+            ids = torch.cat([kept, fresh], dim=1)
+        perm = torch.rand((R, K), generator=g, device=dev).argsort(dim=1)
+        ids = ids.gather(1, perm)
+        self.prev = ids
+        return ids.to(torch.int32)

@@ -1,0 +1,189 @@
+"""Parity at the benchmark workloads' full sizes, in the launch configuration
+the benchmark times (one hs_swap_in launch per layer and step; one store_kv;
+one all-layer transfer), against the CPU oracle element by element.
+
+- tiny swap-in: B=2, K=16, H=64, 656 B rows, one 1024-row HBM pool shared by
+  both rows, 8 steps at 50 % reuse -- everything, every step;
+- DeepSeek-V3.2-shaped swap-in (one of its 61 identical layers): B=32, K=2048,
+  H=4096, 656 B rows, 32 x 128K-row HBM pool, 90 % reuse, warmed to the steady
+  state -- everything, every step;
+- indexer rows: B=64, K=2048, H=2048, 132 B rows (4-byte path), 64 x 64K-row
+  pinned host pool, 80 % reuse -- everything, every step;
+- high-miss stress: B=128, K=2048, H=2048, 656 B rows, 128 x 128K-row pinned
+  host pool, 70 % reuse -- everything, every step;
+- store_kv: 4096 tokens of K and V [8 x 128] bf16 into two 2^20-row pools;
+- all-layer transfer: 61 layers x 78,592 pairs of 656 B rows, pinned host ->
+  HBM -- three layers compared whole, the rest on sampled pairs.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+def _hs():
+    import sparse_attention_kv_row_gb300 as hs
+
+    return hs
+
+
+def _run_swapin_config(dev, cfg, steps, *, shared_pool=False, check_every=1, warm=True):
+    hs = _hs()
+    B, K, H, S, L = cfg.batch, cfg.top_k, cfg.hot_size, cfg.row_bytes, cfg.seq_len
+    P = L if shared_pool else B * L
+    key = synth.stream_key(cfg.seed, 0, 0)
+    if cfg.pool_in_host:
+        pool_t = torch.empty((P, S), dtype=torch.uint8, pin_memory=True)
+        stage = torch.empty((min(P, (1 << 30) // S), S), dtype=torch.uint8, device=dev)
+        for r0 in range(0, P, stage.shape[0]):
+            r1 = min(P, r0 + stage.shape[0])
+            synth.fill_rows_torch(stage[: r1 - r0], key, first_row=r0)
+            pool_t[r0:r1].copy_(stage[: r1 - r0])
+        torch.cuda.synchronize()
+        del stage
+        pool_np = pool_t.numpy()  # the oracle reads the same pinned host rows
+    else:
+        pool_t = torch.empty((P, S), dtype=torch.uint8, device=dev)
+        synth.fill_rows_torch(pool_t, key)
+        pool_np = pool_t.cpu().numpy()
+    tokens, rows, lru = synth.cold_state(B, H, seed=cfg.seed)
+    if shared_pool:
+        rng = np.random.default_rng(cfg.seed)
+        pool_rows = np.stack([rng.permutation(L) for _ in range(B)]).astype(np.int64)
+    else:
+        pool_rows = (np.arange(B, dtype=np.int64)[:, None] * L + np.arange(L)[None]).astype(
+            np.int64)
+    hot = np.random.default_rng(cfg.seed + 1).integers(0, 256, (B * (H + 1), S), dtype=np.uint8)
+    seq = np.full(B, L, np.int64)
+    req = np.random.default_rng(cfg.seed + 2).permutation(B).astype(np.int64)
+    g = dict(tokens=torch.from_numpy(tokens).to(dev), rows=torch.from_numpy(rows).to(dev),
+             lru=torch.from_numpy(lru).to(dev), pool_rows=torch.from_numpy(pool_rows).to(dev),
+             hot=torch.from_numpy(hot).to(dev), seq=torch.from_numpy(seq).to(dev, torch.int32),
+             req=torch.from_numpy(req).to(dev))
+    ts = synth.TopkStreamTorch(cfg.seed, B, K, L, cfg.reuse, dev)
+    out = torch.empty((B, K), dtype=torch.int32, device=dev)
+    miss = torch.empty(B, dtype=torch.int32, device=dev)
+    status = torch.empty(B, dtype=torch.int32, device=dev)
+    stats = torch.zeros(2, dtype=torch.int64, device=dev)
+    r_out = np.empty((B, K), np.int32)
+    r_miss = np.empty(B, np.int32)
+    r_status = np.empty(B, np.int32)
+    r_stats = np.zeros(2, np.uint64)
+    total_steps = (cfg.warm_steps if warm else 0) + steps
+    for step in range(total_steps):
+        ids = ts.next()
+        hs.swap_in(topk_ids=ids, seq_lens=g["seq"], req_state=g["req"], slot_tokens=g["tokens"],
+                   slot_rows=g["rows"], lru=g["lru"], pool_rows=g["pool_rows"], pool_k=pool_t,
+                   hot_k=g["hot"], out_rows=out, miss_count=miss, status=status, stats=stats)
+        oracle.swap_in(topk_ids=ids.cpu().numpy(), seq_lens=seq, req_state=req,
+                       slot_tokens=tokens, slot_rows=rows, lru=lru, pool_rows=pool_rows,
+                       pool_k=pool_np, hot_k=hot, out_rows=r_out, hot_size=H,
+                       miss_count=r_miss, status=r_status, stats=r_stats)
+        torch.cuda.synchronize()
+        if step % check_every == 0 or step == total_steps - 1:
+            np.testing.assert_array_equal(out.cpu().numpy(), r_out, err_msg=f"out step {step}")
+            np.testing.assert_array_equal(miss.cpu().numpy(), r_miss, err_msg=f"miss {step}")
+            np.testing.assert_array_equal(status.cpu().numpy(), r_status)
+            np.testing.assert_array_equal(g["tokens"].cpu().numpy(), tokens, err_msg=f"tok {step}")
+            np.testing.assert_array_equal(g["lru"].cpu().numpy(), lru, err_msg=f"lru {step}")
+            np.testing.assert_array_equal(g["hot"].cpu().numpy(), hot, err_msg=f"hot {step}")
+    np.testing.assert_array_equal(stats.cpu().numpy().astype(np.uint64), r_stats)
+    assert np.all(r_status == 0)
+    return r_miss
+
+
+def test_tiny_config(dev):
+    _run_swapin_config(dev, synth.TINY, 8, shared_pool=True, warm=False)
+
+
+def test_dsv32_layer_full_size(dev):
+    miss = _run_swapin_config(dev, synth.DSV32, 4, check_every=5)
+    # steady state: about 205 fresh ids per row, a few of them still resident
+    assert 150 < miss.mean() <= 205
+
+
+def test_indexer_rows_full_size(dev):
+    miss = _run_swapin_config(dev, synth.INDEXER, 3, check_every=3)
+    # H == K: the resident set is the previous step's ids, so every fresh id
+    # misses unless it is the newest token or a slot still holds it
+    fresh = 2048 - int(round(0.8 * 2048))
+    assert np.all(miss <= fresh) and miss.mean() > fresh - 2
+
+
+def test_stress_full_size(dev):
+    miss = _run_swapin_config(dev, synth.STRESS, 2, check_every=4)
+    fresh = 2048 - int(round(0.7 * 2048))
+    assert np.all(miss <= fresh) and miss.mean() > fresh - 2
+
+
+def test_store_kv_full_size(dev):
+    hs = _hs()
+    c = synth.STORE_KV
+    n, heads, hd, rows = c["n_tokens"], c["heads"], c["head_dim"], c["pool_rows"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(c["seed"])
+    k = torch.randn((n, heads, hd), generator=gen, device=dev).to(torch.bfloat16)
+    v = torch.randn((n, heads, hd), generator=gen, device=dev).to(torch.bfloat16)
+    kd = torch.randint(0, 256, (rows, heads * hd * 2), generator=gen, device=dev,
+                       dtype=torch.uint8)
+    vd = torch.randint(0, 256, (rows, heads * hd * 2), generator=gen, device=dev,
+                       dtype=torch.uint8)
+    loc = torch.randperm(rows, generator=gen, device=dev)[:n]
+    kd_h, vd_h = kd.cpu().numpy(), vd.cpu().numpy()
+    hs.store_kv(k.view(torch.uint8).view(n, -1), v.view(torch.uint8).view(n, -1), kd, vd, loc)
+    oracle.store_kv(k_src=k.view(torch.uint8).view(n, -1).cpu().numpy(),
+                    v_src=v.view(torch.uint8).view(n, -1).cpu().numpy(), k_dst=kd_h, v_dst=vd_h,
+                    loc=loc.cpu().numpy())
+    torch.cuda.synchronize()
+    assert np.array_equal(kd.cpu().numpy(), kd_h)
+    assert np.array_equal(vd.cpu().numpy(), vd_h)
+
+
+def test_transfer_all_layer_full_size(dev):
+    hs = _hs()
+    c = synth.TRANSFER
+    NL, S = c["layers"], c["row_bytes"]
+    src_rows = synth.STRESS.seq_len
+    dst_rows = synth.STRESS.batch * (synth.STRESS.hot_size + 1)
+    n = 78592
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(c["seed"])
+    stage = torch.empty((src_rows, S), dtype=torch.uint8, device=dev)
+    src = []
+    for l in range(NL):
+        t = torch.empty((src_rows, S), dtype=torch.uint8, pin_memory=True)
+        synth.fill_rows_torch(stage, synth.stream_key(c["seed"], l))
+        t.copy_(stage)
+        src.append(t)
+    dst = [torch.randint(0, 256, (dst_rows, S), generator=gen, device=dev, dtype=torch.uint8)
+           for _ in range(NL)]
+    src_idx = torch.randperm(src_rows, generator=gen, device=dev)[:n]
+    dst_idx = torch.randperm(dst_rows, generator=gen, device=dev)[:n]
+    whole = [0, 30, 60]
+    before = [dst[l].cpu().numpy() for l in whole]
+    hs.transfer_kv_layers(src, dst, src_idx, dst_idx)
+    torch.cuda.synchronize()
+    si, di = src_idx.cpu().numpy(), dst_idx.cpu().numpy()
+    oracle.transfer_kv(src_layers=[src[l].numpy() for l in whole], dst_layers=before,
+                       src_idx=si, dst_idx=di)
+    for l, ref in zip(whole, before):
+        assert np.array_equal(dst[l].cpu().numpy(), ref), f"layer {l}"
+    rng = np.random.default_rng(0)
+    for l in range(NL):
+        pick = rng.choice(n, size=64, replace=False)
+        got = dst[l][torch.from_numpy(di[pick]).to(dev)].cpu().numpy()
+        assert np.array_equal(got, src[l].numpy()[si[pick]]), f"layer {l}"

@@ -51,3 +51,33 @@ def test_cold_state_layout():
     assert lru[2].tolist() == list(range(5))
     _, prow, _ = synth.cold_state(3, 5, seed=1)
     assert sorted(prow.reshape(-1).tolist()) == list(range(18))
+
+
+def test_topk_stream_torch_recipe():
+    ts = synth.TopkStreamTorch(3, 5, 64, 700, 0.75, "cpu")
+    prev = ts.next().numpy()
+    for _ in range(6):
+        cur = ts.next().numpy()
+        for b in range(5):
+            s = set(cur[b].tolist())
+            assert len(s) == 64 and min(s) >= 0 and max(s) < 700
+            assert len(s & set(prev[b].tolist())) == 48
+        prev = cur
+    a = synth.TopkStreamTorch(3, 5, 64, 700, 0.75, "cpu")
+    b = synth.TopkStreamTorch(3, 5, 64, 700, 0.75, "cpu")
+    for _ in range(3):
+        np.testing.assert_array_equal(a.next().numpy(), b.next().numpy())
+
+
+def test_topk_stream_torch_fresh_is_uniform_over_complement():
+    # the complement mapping covers every non-excluded id and never an excluded one
+    ts = synth.TopkStreamTorch(4, 200, 8, 20, 0.5, "cpu")
+    first = ts.next()
+    second = ts.next().numpy()
+    prev = first.numpy()
+    seen = set()
+    for r in range(200):
+        fresh = set(second[r].tolist()) - set(prev[r].tolist())
+        assert len(fresh) == 4
+        seen |= fresh
+    assert seen == set(range(20))
