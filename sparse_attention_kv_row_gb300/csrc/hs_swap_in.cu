@@ -5,33 +5,38 @@
 // tripwires of vLLM csrc/libtorch_stable/hisparse_kernels.cu
 // (hisparse_resolve_residency_kernel).
 //
-// One thread-block cluster of C CTAs owns one batch row (C = 1..8, chosen so
-// that batch * C covers the SMs).  CTA j of the cluster owns LRU positions
-// (and slots) [j*P, (j+1)*P) and top-k entries [j*E, (j+1)*E); per-row
-// results cross CTAs through distributed shared memory:
+// Each batch row runs on a cluster of C CTAs (C = 1..8, chosen so that
+// batch * C covers the SMs).  Every CTA of the cluster computes the row's
+// whole bookkeeping in its own shared memory -- it is cheap, local and
+// identical in every CTA -- and then applies only its share of the writes:
+// CTA j owns top-k entries [j*E, (j+1)*E) (their outputs, their misses'
+// token records and row copies) and LRU positions [j*P, (j+1)*P) (their place
+// in the new LRU order).  Exchanging per-position results through
+// distributed shared memory instead was measured slower than recomputing
+// them.  The only cross-CTA step is one split cluster barrier: no CTA writes
+// the row's LRU order or slot tokens before every CTA has staged them.
 //
 //   P0 stage    the row's ids, LRU order, slot tokens and slot rows into
 //               shared memory with LDGSTS (all in flight at once);
-//   P1 hash     every CTA hashes all valid ids (Knuth multiplicative hash,
-//               linear probing, one CAS per id); only when an id repeats does a
-//               second pass make the smallest entry index canonical;
-//   P2 walk     each CTA walks its LRU positions: the lowest position of each
-//               slot and the lowest position holding each wanted token win a
-//               red.min into the owning CTA's shared memory;
-//   P3 hits     a position is a hit when it won its entry; hits emit their hot
-//               row, evictables are compacted in LRU order (ballot + scan);
-//   P4 misses   each CTA classifies its entries; candidates look up their pool
-//               row; misses are compacted in top-k order;
-//   P5 assign   counts are exchanged; the m-th miss of the row reads the m-th
-//               evictable from whichever CTA holds it, records its token and
-//               emits the hot row; every CTA writes its part of the new LRU
-//               order [stale evictables][misses][hits] directly;
-//   P6 copy     each CTA copies its misses' rows, (miss, 16-byte chunk) work
-//               items over all its threads: read-only no-L1 loads from the pool
-//               (HBM or pinned host memory), L2-only stores into the hot buffer.
-//
-// Four cluster barriers separate the phases (two of them split arrive/wait so
-// that initialisation and the copy overlap them).
+//   P1 hash     all valid ids into an open-addressing table (Knuth
+//               multiplicative hash, linear probing, one CAS per id); only when
+//               an id repeats does a second pass make its smallest entry
+//               index canonical.  The LRU row is checked to be a permutation
+//               (plain stores, then a lowest-position pass only if a slot
+//               repeats);
+//   P2 walk     every position probes its slot's token; the lowest position
+//               holding a wanted token claims the entry (atomicMin);
+//   P3 hits     position-ordered ballot/popc + one warp scan of chunk counts:
+//               hit ranks, and the evictables in LRU order;
+//   P4 misses   entries in top-k order: candidates look up their pool row; the
+//               same scan gives each miss its rank m, and the m-th miss takes
+//               the m-th evictable; the CTA owning the entry emits its output,
+//               records the slot's new token and queues the row copy;
+//   P5 LRU      each CTA writes its positions' places in the new order
+//               [stale evictables][misses][hits];
+//   P6 copy     (miss, 16-byte chunk) work items over all threads: read-only
+//               no-L1 loads from the pool (HBM or pinned host memory), L2-only
+//               stores into the hot buffer.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -49,10 +54,13 @@ constexpr int kCopyUnroll = 4;
 constexpr int kMaxCluster = 8;
 constexpr int32_t kUnclaimed = INT_MAX;
 
+// Per-entry classification, stored as one byte per top-k entry.
+enum : int8_t { kInvalid = 0, kRepeat = 1, kNewest = 2, kHit = 3, kBadPool = 4, kMiss = 5 };
+
 struct Layout {
   int hash_bits, hash_size, slice_p, slice_e;
-  int o_hash, o_ids, o_lru, o_tok, o_rows, o_mark, o_claim, o_found, o_code, o_evl, o_missi,
-      o_jsrc, o_jdst, o_wsum, o_xch, o_misc;
+  int o_hash, o_ids, o_lru, o_tok, o_rows, o_mark, o_claim, o_found, o_evl, o_cntp, o_cnte,
+      o_code, o_misc, o_jsrc, o_jdst;
   int total;
 };
 
@@ -62,33 +70,33 @@ __host__ __device__ inline int take(int* o, int bytes) {
   return r;
 }
 
-// Shared-memory layout of one CTA of a row's cluster.  Every CTA uses the same
-// offsets, so a peer's array is addressed by mapping the local address.
+// Shared-memory layout of one CTA.  Slices are whole 32-element chunks so a
+// warp's ballot covers one chunk of the row.
 __host__ __device__ inline Layout make_layout(int K, int H, int C) {
   Layout L;
   int bits = 1;
   while ((1 << bits) < 2 * K) ++bits;
   L.hash_bits = bits;
   L.hash_size = 1 << bits;
-  L.slice_p = (H + C - 1) / C;
-  L.slice_e = (K + C - 1) / C;
+  L.slice_p = ((H + C - 1) / C + 31) & ~31;
+  L.slice_e = ((K + C - 1) / C + 31) & ~31;
+  const int chunks_p = (H + 31) / 32, chunks_e = (K + 31) / 32;
   int o = 0;
-  L.o_hash = take(&o, 8 * L.hash_size);           // int2 {key, entry}
-  L.o_ids = take(&o, 4 * K + 16);                 // staged top-k row
-  L.o_lru = take(&o, 2 * H + 16);                 // staged LRU order
-  L.o_tok = take(&o, 4 * H + 16);                 // staged slot tokens [0, H)
-  L.o_rows = take(&o, 4 * (H + 1) + 16);          // staged slot rows [0, H]
-  L.o_mark = take(&o, 4 * L.slice_p);             // my slots: lowest position
-  L.o_claim = take(&o, 4 * L.slice_e);            // my entries: lowest hit position
-  L.o_found = take(&o, 4 * L.slice_p);            // my positions: wanted entry / -1 / -2
-  L.o_code = take(&o, 4 * L.slice_p);             // my positions: hit rank or ~evict rank
-  L.o_evl = take(&o, 4 * L.slice_p);              // my evictables (slot | bad << 16)
-  L.o_missi = take(&o, 4 * L.slice_e);            // my misses: entry index
-  L.o_jsrc = take(&o, 8 * L.slice_e);             // my misses: pool row
-  L.o_jdst = take(&o, 4 * L.slice_e);             // my misses: hot row or -1
-  L.o_wsum = take(&o, 4 * 40);                    // block-scan scratch
-  L.o_xch = take(&o, 4 * 3 * kMaxCluster);        // per-CTA hits, misses, flags
+  L.o_hash = take(&o, 8 * L.hash_size);   // int2 {key, canonical entry}
+  L.o_ids = take(&o, 4 * K + 16);         // staged top-k row
+  L.o_lru = take(&o, 2 * H + 16);         // staged LRU order
+  L.o_tok = take(&o, 4 * H + 16);         // staged slot tokens [0, H)
+  L.o_rows = take(&o, 4 * (H + 1) + 16);  // staged slot rows [0, H]
+  L.o_mark = take(&o, 4 * H);             // slot -> its LRU position (lowest if repeated)
+  L.o_claim = take(&o, 4 * K);            // entry -> lowest position holding its token
+  L.o_found = take(&o, 4 * H);            // position -> wanted entry, -1 none, -2 corrupt
+  L.o_evl = take(&o, 4 * H);              // evictables in LRU order: slot | corrupt << 16
+  L.o_cntp = take(&o, 4 * chunks_p);      // per-chunk hit counts -> exclusive prefixes
+  L.o_cnte = take(&o, 4 * chunks_e);      // per-chunk miss counts -> exclusive prefixes
+  L.o_code = take(&o, K);                 // per-entry classification
   L.o_misc = take(&o, 4 * 8);
+  L.o_jsrc = take(&o, 8 * L.slice_e);     // my misses: pool row
+  L.o_jdst = take(&o, 4 * L.slice_e);     // my misses: hot row or -1
   L.total = o;
   return L;
 }
@@ -125,7 +133,7 @@ struct SwapInParams {
   FastDiv div_chunks;
 };
 
-enum { kMiscFlags = 0, kMiscPeerFlags = 1, kMiscRepeat = 2 };
+enum { kMiscFlags = 0, kMiscRepeat = 1, kMiscSlotRepeat = 2, kMiscHits = 3, kMiscMisses = 4 };
 
 __device__ __forceinline__ uint32_t hash_of(int32_t key, int bits) {
   return (static_cast<uint32_t>(key) * 2654435761u) >> (32 - bits);
@@ -165,7 +173,7 @@ struct Chunk<1> {
   static __device__ __forceinline__ void st(unsigned char* p, T v) { st_l2_u8(p, v); }
 };
 
-// P6: copy this CTA's applied misses, work item = (miss, chunk).
+// P6: copy this CTA's misses, work item = (miss, chunk).
 template <int G>
 __device__ __forceinline__ void copy_rows(const SwapInParams& p, const unsigned char* pool,
                                           unsigned char* hot, int n, const int64_t* jsrc,
@@ -197,17 +205,26 @@ __device__ __forceinline__ void copy_rows(const SwapInParams& p, const unsigned 
   }
 }
 
+// Hit test of LRU position q (after P2).
+__device__ __forceinline__ bool is_hit(const int32_t* found, const int32_t* claim, int q) {
+  const int f = found[q];
+  return f >= 0 && claim[f] == q;
+}
+
 template <typename SeqT, typename ReqT, int G>
 __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const unsigned lanes_before = (1u << lane) - 1u;
   const int C = p.cluster;
   const int j = static_cast<int>(cluster_rank());
   const int b = blockIdx.x / C;
   const int K = p.top_k;
   const int H = p.hot_size;
   const Layout L = make_layout(K, H, C);
-  const int p0 = min(H, j * L.slice_p), p1 = min(H, p0 + L.slice_p);  // my positions / slots
+  const int p0 = min(H, j * L.slice_p), p1 = min(H, p0 + L.slice_p);  // my LRU positions
   const int e0 = min(K, j * L.slice_e), e1 = min(K, e0 + L.slice_e);  // my entries
 
   // ---- P0: stage the top-k row first; it does not depend on the state row.
@@ -263,28 +280,29 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   int32_t* mark = reinterpret_cast<int32_t*>(smem + L.o_mark);
   int32_t* claim = reinterpret_cast<int32_t*>(smem + L.o_claim);
   int32_t* found = reinterpret_cast<int32_t*>(smem + L.o_found);
-  int32_t* code = reinterpret_cast<int32_t*>(smem + L.o_code);
   int32_t* evl = reinterpret_cast<int32_t*>(smem + L.o_evl);
-  int32_t* missi = reinterpret_cast<int32_t*>(smem + L.o_missi);
+  int32_t* cntp = reinterpret_cast<int32_t*>(smem + L.o_cntp);
+  int32_t* cnte = reinterpret_cast<int32_t*>(smem + L.o_cnte);
+  int8_t* code = reinterpret_cast<int8_t*>(smem + L.o_code);
+  int32_t* misc = reinterpret_cast<int32_t*>(smem + L.o_misc);
   int64_t* jsrc = reinterpret_cast<int64_t*>(smem + L.o_jsrc);
   int32_t* jdst = reinterpret_cast<int32_t*>(smem + L.o_jdst);
-  int* wsum = reinterpret_cast<int*>(smem + L.o_wsum);
-  int32_t* xch = reinterpret_cast<int32_t*>(smem + L.o_xch);
-  int32_t* misc = reinterpret_cast<int32_t*>(smem + L.o_misc);
   {
     int4* t4 = reinterpret_cast<int4*>(tab);
     for (int i = tid; i < L.hash_size / 2; i += kThreads) t4[i] = make_int4(-1, -1, -1, -1);
   }
-  for (int i = tid; i < p1 - p0; i += kThreads) mark[i] = kUnclaimed;
-  for (int i = tid; i < e1 - e0; i += kThreads) claim[i] = kUnclaimed;
+  for (int i = tid; i < K; i += kThreads) claim[i] = kUnclaimed;
   if (tid < 8) misc[tid] = 0;
   cp_async_commit_wait_all();
   __syncthreads();
-  cluster_arrive();  // B0 (arrive): my mark / claim arrays are initialised
+  // Every CTA of the row has staged the state once all have arrived here; the
+  // matching wait comes right before the first write to that state.
+  cluster_arrive();
 
-  // ---- P1: hash every valid id; CAS on the key, the winner stores its index.
+  // ---- P1: hash the valid ids; mark each slot with its LRU position.
   const int bits = L.hash_bits;
   const uint32_t hmask = static_cast<uint32_t>(L.hash_size) - 1u;
+  int32_t my_flags = 0;
   for (int i = tid; i < K; i += kThreads) {
     const int32_t t = ids[i];
     if (t >= 0 && t < Lb) {
@@ -303,8 +321,15 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       }
     }
   }
+  for (int q = tid; q < H; q += kThreads) {
+    const int s = lru[q];
+    if (s >= 0 && s < H)
+      mark[s] = q;
+    else
+      my_flags |= HS_ST_BAD_LRU_SLOT;
+  }
   __syncthreads();
-  if (misc[kMiscRepeat]) {  // rare: make the smallest index of each id canonical
+  if (misc[kMiscRepeat]) {  // rare: the smallest index of a repeated id is canonical
     for (int i = tid; i < K; i += kThreads) {
       const int32_t t = ids[i];
       if (t >= 0 && t < Lb) {
@@ -318,173 +343,182 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
         }
       }
     }
+  }
+  for (int q = tid; q < H; q += kThreads) {
+    const int s = lru[q];
+    if (s >= 0 && s < H && mark[s] != q) misc[kMiscSlotRepeat] = 1;
+  }
+  __syncthreads();
+  if (misc[kMiscSlotRepeat]) {  // rare: a slot listed twice keeps its lowest position
+    for (int q = tid; q < H; q += kThreads) {
+      const int s = lru[q];
+      if (s >= 0 && s < H) mark[s] = kUnclaimed;
+    }
+    __syncthreads();
+    for (int q = tid; q < H; q += kThreads) {
+      const int s = lru[q];
+      if (s >= 0 && s < H) atomicMin(&mark[s], q);
+    }
     __syncthreads();
   }
-  cluster_wait();  // B0 (wait): every peer's arrays are initialised
 
-  // ---- P2: walk my LRU positions; lowest position wins each slot and each entry.
-  for (int q = p0 + tid; q < p1; q += kThreads) {
+  // ---- P2: walk the LRU order; the lowest position holding a wanted token claims it.
+  for (int q = tid; q < H; q += kThreads) {
     const int s = lru[q];
-    int f = -2;  // -2: slot out of range
-    if (s >= 0 && s < H) {
-      peer_min(peer_addr(&mark[s % L.slice_p], s / L.slice_p), q);
-      const int32_t tk = tok[s];
+    int f = -2;  // corrupt entry: out of range, or a repeat of an earlier slot
+    if (s >= 0 && s < H && mark[s] == q) {
       f = -1;
+      const int32_t tk = tok[s];
       if (tk >= 0 && tk < Lb && tk != Lb - 1) {
         const int32_t i = hash_find(tab, tk, bits);
         if (i >= 0) {
           f = i;
-          peer_min(peer_addr(&claim[i % L.slice_e], i / L.slice_e), q);
+          atomicMin(&claim[i], q);
         }
       }
     }
-    found[q - p0] = f;
+    found[q] = f;
   }
-  cluster_sync();  // B1
+  __syncthreads();
 
-  // ---- P3: hits and evictables of my positions, in LRU order.
-  int32_t my_flags = 0;
-  int my_h = 0;
-  for (int base = p0; base < p1; base += kThreads) {
+  // ---- P3: hit ranks in LRU order; evictables compacted in LRU order.
+  const int chunks_p = (H + 31) / 32;
+  for (int base = 0; base < H; base += kThreads) {
     const int q = base + tid;
-    const bool in = q < p1;
-    bool hit = false, bad = false;
-    int s = 0, f = -2;
-    if (in) {
-      s = lru[q];
-      f = found[q - p0];
-      if (f == -2) {
-        bad = true;
-      } else {
-        bad = peer_ld(peer_addr(&mark[s % L.slice_p], s / L.slice_p)) != q;  // repeated slot
-        hit = !bad && f >= 0 &&
-              peer_ld(peer_addr(&claim[f % L.slice_e], f / L.slice_e)) == q;
-      }
+    const unsigned m = __ballot_sync(kFullMask, q < H && is_hit(found, claim, q));
+    if (lane == 0 && base + warp * 32 < H) cntp[(base >> 5) + warp] = __popc(m);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nh = warp_scan_array(cntp, chunks_p, lane);
+    if (lane == 0) misc[kMiscHits] = nh;
+  }
+  __syncthreads();
+  for (int base = 0; base < H; base += kThreads) {
+    const int q = base + tid;
+    const bool hit = q < H && is_hit(found, claim, q);
+    const unsigned m = __ballot_sync(kFullMask, hit);
+    if (q < H && !hit) {
+      const int before = cntp[q >> 5] + __popc(m & lanes_before);
+      const bool corrupt = found[q] == -2;
+      if (corrupt) my_flags |= HS_ST_BAD_LRU_SLOT;
+      evl[q - before] = (corrupt ? 0x10000 : 0) | (lru[q] & 0xFFFF);
     }
-    int tot;
-    const int rank = block_exclusive_count(hit, wsum, &tot);
-    if (in) {
-      if (hit) {
-        code[q - p0] = my_h + rank;
-        out_g[f] = rows[s];
-      } else {
-        const int er = (q - p0) - (my_h + rank);
-        evl[er] = (bad ? 0x10000 : 0) | (s & 0xFFFF);
-        code[q - p0] = ~er;
-        if (bad) my_flags |= HS_ST_BAD_LRU_SLOT;
-      }
-    }
-    my_h += tot;
   }
 
-  // ---- P4: my entries in top-k order: invalid, repeated, newest, hit, miss.
+  // ---- P4: entries in top-k order.
   const int64_t* pool_rows_g = p.pool_rows + r * p.pool_rows_stride;
-  int my_m = 0;
-  for (int base = e0; base < e1; base += kThreads) {
+  const int chunks_e = (K + 31) / 32;
+  for (int base = 0; base < K; base += kThreads) {
     const int i = base + tid;
     bool miss = false;
-    int64_t pr = -1;
-    if (i < e1) {
+    if (i < K) {
       const int32_t t = ids[i];
+      int8_t c;
       if (t < 0 || t >= Lb) {
-        out_g[i] = -1;
+        c = kInvalid;
       } else if (hash_find(tab, t, bits) != i) {
-        out_g[i] = -1;
+        c = kRepeat;
         my_flags |= HS_ST_DUP_ID;
       } else if (t == Lb - 1) {
-        out_g[i] = rows[H];  // the newest token lives in slot H
-      } else if (claim[i - e0] == kUnclaimed) {
-        pr = t < p.pool_rows_cols ? __ldg(pool_rows_g + t) : -1;
+        c = kNewest;
+      } else if (claim[i] != kUnclaimed) {
+        c = kHit;
+      } else {
+        const int64_t pr = t < p.pool_rows_cols ? __ldg(pool_rows_g + t) : -1;
         if (pr >= 0 && pr < p.pool_num_rows) {
+          c = kMiss;
           miss = true;
+          if (i >= e0 && i < e1) jsrc[i - e0] = pr;  // compacted below
         } else {
-          out_g[i] = -1;
+          c = kBadPool;
           my_flags |= HS_ST_BAD_POOL_ROW;
         }
       }
+      code[i] = c;
     }
-    int tot;
-    const int rank = block_exclusive_count(miss, wsum, &tot);
-    if (miss) {
-      missi[my_m + rank] = i;
-      jsrc[my_m + rank] = pr;
+    const unsigned m = __ballot_sync(kFullMask, miss);
+    if (lane == 0 && base + warp * 32 < K) cnte[(base >> 5) + warp] = __popc(m);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nm = warp_scan_array(cnte, chunks_e, lane);
+    if (lane == 0) misc[kMiscMisses] = nm;
+  }
+  __syncthreads();
+  const int NH = misc[kMiscHits];
+  const int M = misc[kMiscMisses];
+  const int E = H - NH;
+  const int my_first_miss = e0 < K ? cnte[e0 >> 5] : M;
+  // The first state write of the row follows: wait until every CTA has staged.
+  cluster_wait();
+  int64_t my_pr = 0;
+  for (int base = 0; base < K; base += kThreads) {
+    const int i = base + tid;
+    const bool mine = i >= e0 && i < e1;
+    const int8_t c = i < K ? code[i] : kInvalid;
+    const unsigned m = __ballot_sync(kFullMask, c == kMiss);
+    if (mine) my_pr = c == kMiss ? jsrc[i - e0] : 0;
+    __syncthreads();  // jsrc is rewritten in compacted order below
+    if (c == kMiss) {
+      const int mm = cnte[i >> 5] + __popc(m & lanes_before);  // the row's mm-th miss
+      const int32_t e = evl[mm];                               // takes the mm-th evictable
+      int32_t d = -1;
+      if (!(e >> 16)) {
+        const int s = static_cast<int16_t>(e & 0xFFFF);
+        const int32_t hr = rows[s];
+        if (hr >= 0 && hr < p.hot_num_rows) {
+          d = hr;
+          if (mine) tokens_g[s] = ids[i];
+        } else {
+          my_flags |= HS_ST_BAD_HOT_ROW;
+        }
+      }
+      if (mine) {
+        out_g[i] = d;
+        jsrc[mm - my_first_miss] = my_pr;
+        jdst[mm - my_first_miss] = d;
+      }
+    } else if (mine) {
+      int32_t o = -1;
+      if (c == kNewest) o = rows[H];  // the newest token lives in slot H
+      if (c == kHit) o = rows[lru[claim[i]]];
+      out_g[i] = o;
     }
-    my_m += tot;
+  }
+
+  // ---- P5: my positions' places in the new LRU order.
+  for (int base = p0; base < p1; base += kThreads) {
+    const int q = base + tid;
+    const bool hit = q < p1 && is_hit(found, claim, q);
+    const unsigned m = __ballot_sync(kFullMask, hit);
+    if (q < p1) {
+      const int hr = cntp[q >> 5] + __popc(m & lanes_before);  // hits before q
+      int pos;
+      if (hit) {
+        pos = E + hr;
+      } else {
+        const int e = q - hr;
+        pos = e >= M ? e - M : E - M + e;
+      }
+      lru_g[pos] = lru[q];
+    }
   }
   if (my_flags) atomicOr(&misc[kMiscFlags], my_flags);
   __syncthreads();
-  if (tid < C) {  // publish my counts and flags to every CTA of the row
-    peer_st(peer_addr(&xch[j], tid), my_h);
-    peer_st(peer_addr(&xch[kMaxCluster + j], tid), my_m);
-    peer_st(peer_addr(&xch[2 * kMaxCluster + j], tid), misc[kMiscFlags]);
-  }
-  cluster_sync();  // B2
-
-  // ---- P5: totals, slot assignment for my misses, my part of the LRU order.
-  int NH = 0, M = 0, hit_base = 0, miss_base = 0, all_flags = 0;
-  int ev_base[kMaxCluster + 1];
-  ev_base[0] = 0;
-  for (int o = 0; o < C; ++o) {
-    const int h = xch[o], m = xch[kMaxCluster + o];
-    const int len = min(H, (o + 1) * L.slice_p) - min(H, o * L.slice_p);
-    NH += h;
-    M += m;
-    if (o < j) {
-      hit_base += h;
-      miss_base += m;
-    }
-    ev_base[o + 1] = ev_base[o] + (len - h);
-    all_flags |= xch[2 * kMaxCluster + o];
-  }
-  const int E = H - NH;
-  int32_t late_flags = 0;
-  for (int mm = tid; mm < my_m; mm += kThreads) {
-    const int gm = miss_base + mm;  // the row's gm-th miss takes its gm-th evictable
-    int o = 0;
-    while (o + 1 < C && ev_base[o + 1] <= gm) ++o;
-    const int32_t e = peer_ld(peer_addr(&evl[gm - ev_base[o]], o));
-    const int i = missi[mm];
-    int32_t d = -1;
-    if (!(e >> 16)) {
-      const int s = static_cast<int16_t>(e & 0xFFFF);
-      const int32_t hr = rows[s];
-      if (hr >= 0 && hr < p.hot_num_rows) {
-        d = hr;
-        tokens_g[s] = ids[i];
-      } else {
-        late_flags |= HS_ST_BAD_HOT_ROW;
-      }
-    }
-    out_g[i] = d;
-    jdst[mm] = d;
-  }
-  for (int q = p0 + tid; q < p1; q += kThreads) {
-    const int c = code[q - p0];
-    int pos;
-    if (c >= 0) {
-      pos = E + hit_base + c;
-    } else {
-      const int e = ev_base[j] + ~c;
-      pos = e >= M ? e - M : E - M + e;
-    }
-    lru_g[pos] = lru[q];
-  }
-  if (late_flags) peer_or(peer_addr(&misc[kMiscPeerFlags], 0), late_flags);
-  __syncthreads();
-  cluster_arrive();  // B3 (arrive): no more access to any peer's shared memory
   if (j == 0 && tid == 0) {
     if (p.miss_count) p.miss_count[b] = M;
+    if (p.status) p.status[b] = misc[kMiscFlags];
     if (p.stats) {
       atomicAdd(p.stats, static_cast<unsigned long long>(NH));
       atomicAdd(p.stats + 1, static_cast<unsigned long long>(M));
     }
   }
 
-  // ---- P6: copy my missing rows.
+  // ---- P6: copy my misses' rows.
+  const int my_m = (e1 < K ? cnte[e1 >> 5] : M) - my_first_miss;
   copy_rows<G>(p, p.pool_k, p.hot_k, my_m, jsrc, jdst);
   if (p.pool_v != nullptr) copy_rows<G>(p, p.pool_v, p.hot_v, my_m, jsrc, jdst);
-  cluster_wait();  // B3 (wait): peers are done with my shared memory
-  if (j == 0 && tid == 0 && p.status) p.status[b] = all_flags | misc[kMiscPeerFlags];
 }
 
 using KernelFn = void (*)(const SwapInParams);
