@@ -65,6 +65,16 @@ __device__ __forceinline__ void cp_async_16(void* dst_smem, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src)
                : "memory");
 }
+__device__ __forceinline__ void cp_async_8(void* dst_smem, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst_smem)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
 __device__ __forceinline__ void cp_async_commit_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
@@ -72,25 +82,37 @@ __device__ __forceinline__ void cp_async_commit_wait_all() {
 // Copy `nbytes` from global `src` to shared `dst`, where dst and src agree
 // modulo 16 (the shared array is placed at the source's alignment).  The
 // 16-byte-aligned body goes through LDGSTS (no register staging, many copies
-// in flight); the < 16-byte head and tail through plain byte loads.  The
-// caller commits/waits and synchronises.
-__device__ __forceinline__ void stage_bytes(void* dst, const void* src, int64_t nbytes, int tid,
-                                            int nthreads) {
+// in flight).  Each of the < 16 head bytes and < 16 tail bytes is loaded by one
+// thread into a register and stored by stage_finish() only after the caller's
+// LDGSTS wait, so no thread stalls on it in between.
+struct StagePending {
+  int32_t off;  // byte offset in dst, or -1
+  uint32_t val;
+};
+__device__ __forceinline__ StagePending stage_bytes(void* dst, const void* src, int64_t nbytes,
+                                                    int tid, int nthreads) {
   const uintptr_t s = reinterpret_cast<uintptr_t>(src);
   int64_t head = static_cast<int64_t>((16u - (s & 15u)) & 15u);
   if (head > nbytes) head = nbytes;
   const int64_t body = ((nbytes - head) / 16) * 16;
   const int64_t tail = nbytes - head - body;
-  const char* sc = static_cast<const char*>(src);
+  const unsigned char* sc = static_cast<const unsigned char*>(src);
   char* dc = static_cast<char*>(dst);
-  if (tid < head) dc[tid] = sc[tid];
-  if (tid >= 32 && tid < 32 + tail) {
-    const int64_t o = head + body + (tid - 32);
-    dc[o] = sc[o];
+  StagePending pend{-1, 0};
+  if (tid < head) {
+    pend.off = tid;
+    pend.val = sc[tid];
+  } else if (tid >= 32 && tid < 32 + tail) {
+    pend.off = static_cast<int32_t>(head + body + (tid - 32));
+    pend.val = sc[pend.off];
   }
   for (int64_t o = head + static_cast<int64_t>(tid) * 16; o < head + body;
        o += static_cast<int64_t>(nthreads) * 16)
     cp_async_16(dc + o, sc + o);
+  return pend;
+}
+__device__ __forceinline__ void stage_finish(void* dst, StagePending pend) {
+  if (pend.off >= 0) static_cast<unsigned char*>(dst)[pend.off] = static_cast<unsigned char>(pend.val);
 }
 
 // ------------------------------------------------------------------ scans

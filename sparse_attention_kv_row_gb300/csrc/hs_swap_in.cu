@@ -57,10 +57,12 @@ constexpr int32_t kUnclaimed = INT_MAX;
 // Per-entry classification, stored as one byte per top-k entry.
 enum : int8_t { kInvalid = 0, kRepeat = 1, kNewest = 2, kHit = 3, kBadPool = 4, kMiss = 5 };
 
+constexpr int kBloomBits = 17;  // request filter: 2^17 bits = 16 KB
+
 struct Layout {
   int hash_bits, hash_size, slice_p, slice_e;
-  int o_hash, o_ids, o_lru, o_tok, o_rows, o_mark, o_claim, o_found, o_evl, o_cntp, o_cnte,
-      o_code, o_misc, o_jsrc, o_jdst;
+  int o_hash, o_bloom, o_prs, o_ids, o_lru, o_tok, o_rows, o_mark, o_sbits, o_claim, o_found,
+      o_evl, o_cntp, o_cnte, o_code, o_misc, o_jsrc, o_jdst;
   int total;
 };
 
@@ -70,12 +72,17 @@ __host__ __device__ inline int take(int* o, int bytes) {
   return r;
 }
 
+// Hash-table size exponent: the smallest power of two >= mult * K.
+__host__ __device__ inline int hash_bits_for(int K, int mult) {
+  int bits = 1;
+  while ((1 << bits) < mult * K) ++bits;
+  return bits;
+}
+
 // Shared-memory layout of one CTA.  Slices are whole 32-element chunks so a
 // warp's ballot covers one chunk of the row.
-__host__ __device__ inline Layout make_layout(int K, int H, int C) {
+__host__ __device__ inline Layout make_layout(int K, int H, int C, int bits) {
   Layout L;
-  int bits = 1;
-  while ((1 << bits) < 2 * K) ++bits;
   L.hash_bits = bits;
   L.hash_size = 1 << bits;
   L.slice_p = ((H + C - 1) / C + 31) & ~31;
@@ -83,11 +90,14 @@ __host__ __device__ inline Layout make_layout(int K, int H, int C) {
   const int chunks_p = (H + 31) / 32, chunks_e = (K + 31) / 32;
   int o = 0;
   L.o_hash = take(&o, 8 * L.hash_size);   // int2 {key, canonical entry}
+  L.o_bloom = take(&o, 4 << (kBloomBits - 5));  // one bit per hashed requested id
+  L.o_prs = take(&o, 8 * K);              // pool row of each miss candidate (LDGSTS)
   L.o_ids = take(&o, 4 * K + 16);         // staged top-k row
   L.o_lru = take(&o, 2 * H + 16);         // staged LRU order
   L.o_tok = take(&o, 4 * H + 16);         // staged slot tokens [0, H)
   L.o_rows = take(&o, 4 * (H + 1) + 16);  // staged slot rows [0, H]
-  L.o_mark = take(&o, 4 * H);             // slot -> its LRU position (lowest if repeated)
+  L.o_mark = take(&o, 4 * H);             // slot -> lowest LRU position (repeated slots only)
+  L.o_sbits = take(&o, 4 * ((H + 31) / 32));  // slots seen in the LRU row
   L.o_claim = take(&o, 4 * K);            // entry -> lowest position holding its token
   L.o_found = take(&o, 4 * H);            // position -> wanted entry, -1 none, -2 corrupt
   L.o_evl = take(&o, 4 * H);              // evictables in LRU order: slot | corrupt << 16
@@ -102,7 +112,7 @@ __host__ __device__ inline Layout make_layout(int K, int H, int C) {
 }
 
 struct SwapInParams {
-  int32_t top_k, hot_size, cluster;
+  int32_t top_k, hot_size, cluster, hash_bits;
   const int32_t* num_real;
   const int32_t* topk_ids;
   int64_t topk_stride;
@@ -137,6 +147,11 @@ enum { kMiscFlags = 0, kMiscRepeat = 1, kMiscSlotRepeat = 2, kMiscHits = 3, kMis
 
 __device__ __forceinline__ uint32_t hash_of(int32_t key, int bits) {
   return (static_cast<uint32_t>(key) * 2654435761u) >> (32 - bits);
+}
+
+// Bit of `key` in the request filter (a second multiplicative hash).
+__device__ __forceinline__ uint32_t bloom_bit(int32_t key) {
+  return (static_cast<uint32_t>(key) * 0x85EBCA6Bu) >> (32 - kBloomBits);
 }
 
 // Canonical entry index stored for `key`, or -1 when the key is absent.
@@ -223,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const int b = blockIdx.x / C;
   const int K = p.top_k;
   const int H = p.hot_size;
-  const Layout L = make_layout(K, H, C);
+  const Layout L = make_layout(K, H, C, p.hash_bits);
   const int p0 = min(H, j * L.slice_p), p1 = min(H, p0 + L.slice_p);  // my LRU positions
   const int e0 = min(K, j * L.slice_e), e1 = min(K, e0 + L.slice_e);  // my entries
 
@@ -231,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const int32_t* ids_g = p.topk_ids + static_cast<int64_t>(b) * p.topk_stride;
   int32_t* ids = reinterpret_cast<int32_t*>(smem + L.o_ids +
                                             (reinterpret_cast<uintptr_t>(ids_g) & 15u));
-  stage_bytes(ids, ids_g, 4LL * K, tid, kThreads);
+  const StagePending pend_ids = stage_bytes(ids, ids_g, 4LL * K, tid, kThreads);
 
   int32_t* out_g = p.out_rows + static_cast<int64_t>(b) * p.out_stride;
   const bool pad_nr = p.num_real != nullptr && b >= __ldg(p.num_real);
@@ -251,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const int32_t* rows_g = p.slot_rows + r * p.slot_rows_stride;
   if (Lb <= H) {  // fast path: the whole sequence sits in the hot buffer in order
     cp_async_commit_wait_all();
+    stage_finish(ids, pend_ids);
     __syncthreads();
     const int64_t count = Lb < K ? Lb : K;
     for (int i = e0 + tid; i < e1; i += kThreads) {
@@ -272,12 +288,15 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
                                             (reinterpret_cast<uintptr_t>(tokens_g) & 15u));
   int32_t* rows = reinterpret_cast<int32_t*>(smem + L.o_rows +
                                              (reinterpret_cast<uintptr_t>(rows_g) & 15u));
-  stage_bytes(lru, lru_g, 2LL * H, tid, kThreads);
-  stage_bytes(tok, tokens_g, 4LL * H, tid, kThreads);
-  stage_bytes(rows, rows_g, 4LL * (H + 1), tid, kThreads);
+  const StagePending pend_lru = stage_bytes(lru, lru_g, 2LL * H, tid, kThreads);
+  const StagePending pend_tok = stage_bytes(tok, tokens_g, 4LL * H, tid, kThreads);
+  const StagePending pend_rows = stage_bytes(rows, rows_g, 4LL * (H + 1), tid, kThreads);
 
   int2* tab = reinterpret_cast<int2*>(smem + L.o_hash);
+  uint32_t* bloom = reinterpret_cast<uint32_t*>(smem + L.o_bloom);
+  int64_t* prs = reinterpret_cast<int64_t*>(smem + L.o_prs);
   int32_t* mark = reinterpret_cast<int32_t*>(smem + L.o_mark);
+  uint32_t* sbits = reinterpret_cast<uint32_t*>(smem + L.o_sbits);
   int32_t* claim = reinterpret_cast<int32_t*>(smem + L.o_claim);
   int32_t* found = reinterpret_cast<int32_t*>(smem + L.o_found);
   int32_t* evl = reinterpret_cast<int32_t*>(smem + L.o_evl);
@@ -292,8 +311,14 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     for (int i = tid; i < L.hash_size / 2; i += kThreads) t4[i] = make_int4(-1, -1, -1, -1);
   }
   for (int i = tid; i < K; i += kThreads) claim[i] = kUnclaimed;
+  for (int i = tid; i < (1 << (kBloomBits - 5)); i += kThreads) bloom[i] = 0;
+  for (int i = tid; i < (H + 31) / 32; i += kThreads) sbits[i] = 0;
   if (tid < 8) misc[tid] = 0;
   cp_async_commit_wait_all();
+  stage_finish(ids, pend_ids);
+  stage_finish(lru, pend_lru);
+  stage_finish(tok, pend_tok);
+  stage_finish(rows, pend_rows);
   __syncthreads();
   // Every CTA of the row has staged the state once all have arrived here; the
   // matching wait comes right before the first write to that state.
@@ -306,6 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   for (int i = tid; i < K; i += kThreads) {
     const int32_t t = ids[i];
     if (t >= 0 && t < Lb) {
+      const uint32_t bb = bloom_bit(t);
+      atomicOr(&bloom[bb >> 5], 1u << (bb & 31));
       uint32_t h = hash_of(t, bits);
       for (uint32_t n = 0; n <= hmask; ++n) {
         const int32_t old = atomicCAS(&tab[h].x, -1, t);
@@ -323,10 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   }
   for (int q = tid; q < H; q += kThreads) {
     const int s = lru[q];
-    if (s >= 0 && s < H)
-      mark[s] = q;
-    else
+    if (s >= 0 && s < H) {
+      const uint32_t bit = 1u << (s & 31);
+      if (atomicOr(&sbits[s >> 5], bit) & bit) misc[kMiscSlotRepeat] = 1;
+    } else {
       my_flags |= HS_ST_BAD_LRU_SLOT;
+    }
   }
   __syncthreads();
   if (misc[kMiscRepeat]) {  // rare: the smallest index of a repeated id is canonical
@@ -344,12 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       }
     }
   }
-  for (int q = tid; q < H; q += kThreads) {
-    const int s = lru[q];
-    if (s >= 0 && s < H && mark[s] != q) misc[kMiscSlotRepeat] = 1;
-  }
   __syncthreads();
-  if (misc[kMiscSlotRepeat]) {  // rare: a slot listed twice keeps its lowest position
+  const bool slot_repeat = misc[kMiscSlotRepeat] != 0;
+  if (slot_repeat) {  // rare: a slot listed twice keeps its lowest position
     for (int q = tid; q < H; q += kThreads) {
       const int s = lru[q];
       if (s >= 0 && s < H) mark[s] = kUnclaimed;
@@ -366,10 +392,11 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   for (int q = tid; q < H; q += kThreads) {
     const int s = lru[q];
     int f = -2;  // corrupt entry: out of range, or a repeat of an earlier slot
-    if (s >= 0 && s < H && mark[s] == q) {
+    if (s >= 0 && s < H && (!slot_repeat || mark[s] == q)) {
       f = -1;
       const int32_t tk = tok[s];
-      if (tk >= 0 && tk < Lb && tk != Lb - 1) {
+      const uint32_t bb = bloom_bit(tk);
+      if (tk >= 0 && tk < Lb && tk != Lb - 1 && ((bloom[bb >> 5] >> (bb & 31)) & 1u)) {
         const int32_t i = hash_find(tab, tk, bits);
         if (i >= 0) {
           f = i;
@@ -380,6 +407,20 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     found[q] = f;
   }
   __syncthreads();
+  // Pool rows of the miss candidates (wanted, not newest, not claimed), loaded
+  // with LDGSTS now so the load overlaps P3.
+  const bool id_repeat = misc[kMiscRepeat] != 0;
+  const int64_t* pool_rows_g = p.pool_rows + r * p.pool_rows_stride;
+  for (int i = tid; i < K; i += kThreads) {
+    const int32_t t = ids[i];
+    const bool cand = t >= 0 && t < Lb && t != Lb - 1 && claim[i] == kUnclaimed &&
+                      t < p.pool_rows_cols && (!id_repeat || hash_find(tab, t, bits) == i);
+    if (cand)
+      cp_async_8(&prs[i], pool_rows_g + t);
+    else
+      prs[i] = -1;
+  }
+  cp_async_commit();
 
   // ---- P3: hit ranks in LRU order; evictables compacted in LRU order.
   const int chunks_p = (H + 31) / 32;
@@ -407,7 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   }
 
   // ---- P4: entries in top-k order.
-  const int64_t* pool_rows_g = p.pool_rows + r * p.pool_rows_stride;
+  cp_async_wait_all();
+  __syncthreads();
   const int chunks_e = (K + 31) / 32;
   for (int base = 0; base < K; base += kThreads) {
     const int i = base + tid;
@@ -417,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       int8_t c;
       if (t < 0 || t >= Lb) {
         c = kInvalid;
-      } else if (hash_find(tab, t, bits) != i) {
+      } else if (id_repeat && hash_find(tab, t, bits) != i) {
         c = kRepeat;
         my_flags |= HS_ST_DUP_ID;
       } else if (t == Lb - 1) {
@@ -425,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       } else if (claim[i] != kUnclaimed) {
         c = kHit;
       } else {
-        const int64_t pr = t < p.pool_rows_cols ? __ldg(pool_rows_g + t) : -1;
+        const int64_t pr = prs[i];
         if (pr >= 0 && pr < p.pool_num_rows) {
           c = kMiss;
           miss = true;
@@ -559,10 +601,10 @@ hs_err ensure_smem(KernelFn fn, int device, int bytes) {
 
 // Cluster size for a batch: the largest power of two <= 8 with batch * C <=
 // SMs (at least 1), raised while the per-CTA state does not fit shared memory.
-int pick_cluster(int batch, int K, int H, const DeviceInfo& dev) {
+int pick_cluster(int batch, int K, int H, int bits, const DeviceInfo& dev) {
   int C = 1;
   while (C < kMaxCluster && static_cast<int64_t>(batch) * C * 2 <= dev.sm_count) C *= 2;
-  while (C < kMaxCluster && make_layout(K, H, C).total > dev.max_smem_optin) C *= 2;
+  while (C < kMaxCluster && make_layout(K, H, C, bits).total > dev.max_smem_optin) C *= 2;
   return C;
 }
 
@@ -571,7 +613,7 @@ int pick_cluster(int batch, int K, int H, const DeviceInfo& dev) {
 
 extern "C" int64_t hs_swap_in_smem_bytes(int32_t top_k, int32_t hot_size) {
   if (top_k < 1 || hot_size < 1 || hot_size > 32767 || top_k > hot_size) return 0;
-  return hs::make_layout(top_k, hot_size, hs::kMaxCluster).total;
+  return hs::make_layout(top_k, hot_size, hs::kMaxCluster, hs::hash_bits_for(top_k, 2)).total;
 }
 
 extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
@@ -619,8 +661,15 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   DeviceInfo dev;
   hs_err err = current_device(&dev);
   if (err != HS_OK) return err;
-  const int C = pick_cluster(a->batch, a->top_k, a->hot_size, dev);
-  const Layout L = make_layout(a->top_k, a->hot_size, C);
+  // A hash table of >= 4K entries (load <= 1/4) keeps probe chains short; fall
+  // back to >= 2K entries where shared memory is tight.
+  int bits = hash_bits_for(a->top_k, 4);
+  int C = pick_cluster(a->batch, a->top_k, a->hot_size, bits, dev);
+  if (make_layout(a->top_k, a->hot_size, C, bits).total > dev.max_smem_optin) {
+    bits = hash_bits_for(a->top_k, 2);
+    C = pick_cluster(a->batch, a->top_k, a->hot_size, bits, dev);
+  }
+  const Layout L = make_layout(a->top_k, a->hot_size, C, bits);
   if (L.total > dev.max_smem_optin)
     return fail(HS_ERR_UNSUPPORTED,
                 "hs_swap_in: top_k %d / hot_size %d need %d B of shared memory per CTA even "
@@ -655,6 +704,7 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   p.top_k = a->top_k;
   p.hot_size = a->hot_size;
   p.cluster = C;
+  p.hash_bits = bits;
   p.num_real = a->num_real;
   p.topk_ids = a->topk_ids;
   p.topk_stride = a->topk_stride;
