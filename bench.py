@@ -260,7 +260,7 @@ class SwapInWorkload:
         self.miss = [torch.zeros(B, dtype=torch.int32, device=dev) for _ in range(layers)]
         self.out = [torch.zeros((B, cfg.top_k), dtype=torch.int32, device=dev)
                     for _ in range(layers)]
-        self.stream = synth.TopkStreamTorch(cfg.seed * 1000 + rank * 7 + seed_off, layers * B,
+        self.stream = synth.TopkStreamTorch(rank_seed(cfg.seed, rank) + seed_off, layers * B,
                                             cfg.top_k, L, cfg.reuse, dev)
 
     def next_topk(self):
@@ -617,6 +617,25 @@ def _cpu_model():
     return "unknown"
 
 
+# --------------------------------------------------------------------------- ranks
+def combine_ranks(t_dev, t_e2e, misses, e2e_misses, alg_bytes, dist, device):
+    """Whole-job figures over all ranks: the slowest rank's times (max) and the
+    units every rank processed (sum).  Ranks share nothing on the data path;
+    this is the only collective."""
+    if not dist:
+        return t_dev, t_e2e, misses, e2e_misses, alg_bytes
+    tt = torch.tensor([t_dev, t_e2e], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+    mm = torch.tensor([misses, e2e_misses, alg_bytes], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(mm, op=torch.distributed.ReduceOp.SUM)
+    return float(tt[0]), float(tt[1]), float(mm[0]), float(mm[1]), float(mm[2])
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank serves its own requests: a distinct top-k stream per rank."""
+    return base * 1000 + rank * 7
+
+
 # --------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -676,16 +695,8 @@ def main():
     h = run_headline(args, dev, rank, world, dist)
     t_dev = h["t_dev"]
     misses = h["misses"]
-    if dist:
-        tt = torch.tensor([t_dev, h["t_e2e"]], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        mm = torch.tensor([misses, h["e2e_misses"], h["alg_bytes"]], dtype=torch.float64,
-                          device=dev)
-        torch.distributed.all_reduce(mm, op=torch.distributed.ReduceOp.SUM)
-        t_dev, t_e2e = float(tt[0]), float(tt[1])
-        misses_all, e2e_all, alg_all = (float(x) for x in mm)
-    else:
-        t_e2e, misses_all, e2e_all, alg_all = h["t_e2e"], misses, h["e2e_misses"], h["alg_bytes"]
+    t_dev, t_e2e, misses_all, e2e_all, alg_all = combine_ranks(
+        h["t_dev"], h["t_e2e"], misses, h["e2e_misses"], h["alg_bytes"], dist, dev)
 
     ops = {}
     if not args.headline_only and rank == 0:

@@ -144,3 +144,37 @@ def test_capture_in_cuda_graph(dev):
         r_out, _, _, _ = cases.run_oracle(ref)
         np.testing.assert_array_equal(out.cpu().numpy(), r_out)
         g.assert_matches(ref, f"graph step {step}")
+
+
+def test_row_subsets_match_whole_batch(dev):
+    """Rows are independent: two disjoint halves of the batch, swapped in by two
+    calls (as two GPUs of a data-parallel job would), give exactly the results
+    of one whole-batch call."""
+    import sparse_attention_kv_row_gb300 as hs
+    import synth
+
+    rng = np.random.default_rng(77)
+    B, K, H, L = 6, 96, 256, 3000
+    base = cases.random_case(rng, B=B, K=K, H=H, S=656, R=B, seq_len=L)
+    whole = GpuCase(base.copy(), dev)
+    split = GpuCase(base.copy(), dev)
+    ts = synth.TopkStream(3, 0, B, K, L, 0.7)
+    for step in range(4):
+        ids = ts.next()
+        whole_out = whole.step(ids)[0]
+        split_out = []
+        for rows_ in (slice(0, 3), slice(3, 6)):
+            sub = torch.from_numpy(np.ascontiguousarray(ids[rows_])).to(dev)
+            out = torch.empty((3, K), dtype=torch.int32, device=dev)
+            hs.swap_in(topk_ids=sub,
+                       seq_lens=torch.from_numpy(base.seq_lens[rows_]).to(dev),
+                       req_state=torch.from_numpy(base.req_state[rows_]).to(dev),
+                       slot_tokens=split.tokens, slot_rows=split.rows, lru=split.lru,
+                       pool_rows=split.pool_rows, pool_k=split.pool_k, hot_k=split.hot_k,
+                       out_rows=out)
+            split_out.append(out)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(whole_out, torch.cat(split_out).cpu().numpy())
+        for a, b in ((whole.tokens, split.tokens), (whole.lru, split.lru),
+                     (whole.hot_k, split.hot_k)):
+            assert torch.equal(a, b), f"step {step}"
