@@ -50,6 +50,7 @@ namespace hs {
 namespace {
 
 constexpr int kThreads = 1024;
+constexpr int kMaxItems = 8;  // LRU positions per thread: hot_size <= 8192
 constexpr int kCopyUnroll = 4;
 constexpr int kMaxCluster = 8;
 constexpr int32_t kUnclaimed = INT_MAX;
@@ -61,8 +62,7 @@ constexpr int kBloomBits = 17;  // request filter: 2^17 bits = 16 KB
 
 struct Layout {
   int hash_bits, hash_size, slice_p, slice_e;
-  int o_hash, o_bloom, o_prs, o_ids, o_lru, o_tok, o_rows, o_mark, o_sbits, o_claim, o_found,
-      o_evl, o_cntp, o_cnte, o_code, o_misc, o_jsrc, o_jdst;
+  int o_hash, o_bloom, o_prs, o_ids, o_lru, o_tok, o_rows, o_mark, o_sbits, o_claim, o_evl, o_cntp, o_cnte, o_code, o_misc, o_jsrc, o_jdst;
   int total;
 };
 
@@ -99,7 +99,6 @@ __host__ __device__ inline Layout make_layout(int K, int H, int C, int bits) {
   L.o_mark = take(&o, 4 * H);             // slot -> lowest LRU position (repeated slots only)
   L.o_sbits = take(&o, 4 * ((H + 31) / 32));  // slots seen in the LRU row
   L.o_claim = take(&o, 4 * K);            // entry -> lowest position holding its token
-  L.o_found = take(&o, 4 * H);            // position -> wanted entry, -1 none, -2 corrupt
   L.o_evl = take(&o, 4 * H);              // evictables in LRU order: slot | corrupt << 16
   L.o_cntp = take(&o, 4 * chunks_p);      // per-chunk hit counts -> exclusive prefixes
   L.o_cnte = take(&o, 4 * chunks_e);      // per-chunk miss counts -> exclusive prefixes
@@ -112,7 +111,7 @@ __host__ __device__ inline Layout make_layout(int K, int H, int C, int bits) {
 }
 
 struct SwapInParams {
-  int32_t top_k, hot_size, cluster, hash_bits;
+  int32_t top_k, hot_size, cluster, hash_bits, flags;
   const int32_t* num_real;
   const int32_t* topk_ids;
   int64_t topk_stride;
@@ -220,13 +219,22 @@ __device__ __forceinline__ void copy_rows(const SwapInParams& p, const unsigned 
   }
 }
 
-// Hit test of LRU position q (after P2).
-__device__ __forceinline__ bool is_hit(const int32_t* found, const int32_t* claim, int q) {
-  const int f = found[q];
-  return f >= 0 && claim[f] == q;
+// Continues a linear probe for `key` after its first slot `h` held another key.
+__device__ __forceinline__ int32_t probe_rest(const int2* tab, int32_t key, uint32_t h,
+                                              uint32_t mask) {
+  for (uint32_t n = 1; n <= mask; ++n) {
+    h = (h + 1u) & mask;
+    const int2 kv = tab[h];
+    if (kv.x == key) return kv.y;
+    if (kv.x == -1) return -1;
+  }
+  return -1;
 }
 
-template <typename SeqT, typename ReqT, int G>
+// IT = LRU positions per thread (position k * 1024 + tid for k < IT); their
+// slot, claimed entry and hit flag stay in registers from P1 to P5, and each
+// phase handles them as batched, independent loads.
+template <int IT, int G>
 __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x;
@@ -250,8 +258,12 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
 
   int32_t* out_g = p.out_rows + static_cast<int64_t>(b) * p.out_stride;
   const bool pad_nr = p.num_real != nullptr && b >= __ldg(p.num_real);
-  const int64_t r = static_cast<int64_t>(__ldg(static_cast<const ReqT*>(p.req_state) + b));
-  const int64_t Lb = static_cast<int64_t>(__ldg(static_cast<const SeqT*>(p.seq_lens) + b));
+  const int64_t r = (p.flags & HS_REQ_STATE_I64)
+                        ? __ldg(static_cast<const int64_t*>(p.req_state) + b)
+                        : static_cast<int64_t>(__ldg(static_cast<const int32_t*>(p.req_state) + b));
+  const int64_t Lb = (p.flags & HS_SEQ_LENS_I64)
+                         ? __ldg(static_cast<const int64_t*>(p.seq_lens) + b)
+                         : static_cast<int64_t>(__ldg(static_cast<const int32_t*>(p.seq_lens) + b));
 
   if (pad_nr || r < 0 || r >= p.num_states) {  // padding row / bad state row
     cp_async_commit_wait_all();
@@ -298,7 +310,6 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   int32_t* mark = reinterpret_cast<int32_t*>(smem + L.o_mark);
   uint32_t* sbits = reinterpret_cast<uint32_t*>(smem + L.o_sbits);
   int32_t* claim = reinterpret_cast<int32_t*>(smem + L.o_claim);
-  int32_t* found = reinterpret_cast<int32_t*>(smem + L.o_found);
   int32_t* evl = reinterpret_cast<int32_t*>(smem + L.o_evl);
   int32_t* cntp = reinterpret_cast<int32_t*>(smem + L.o_cntp);
   int32_t* cnte = reinterpret_cast<int32_t*>(smem + L.o_cnte);
@@ -348,11 +359,18 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       }
     }
   }
-  for (int q = tid; q < H; q += kThreads) {
-    const int s = lru[q];
-    if (s >= 0 && s < H) {
-      const uint32_t bit = 1u << (s & 31);
-      if (atomicOr(&sbits[s >> 5], bit) & bit) misc[kMiscSlotRepeat] = 1;
+  int sl[IT];  // the slot at each of my LRU positions
+#pragma unroll
+  for (int k = 0; k < IT; ++k) {
+    const int q = k * kThreads + tid;
+    sl[k] = q < H ? lru[q] : 0;
+  }
+#pragma unroll
+  for (int k = 0; k < IT; ++k) {
+    if (k * kThreads + tid >= H) continue;
+    if (sl[k] >= 0 && sl[k] < H) {
+      const uint32_t bit = 1u << (sl[k] & 31);
+      if (atomicOr(&sbits[sl[k] >> 5], bit) & bit) misc[kMiscSlotRepeat] = 1;
     } else {
       my_flags |= HS_ST_BAD_LRU_SLOT;
     }
@@ -376,35 +394,59 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   __syncthreads();
   const bool slot_repeat = misc[kMiscSlotRepeat] != 0;
   if (slot_repeat) {  // rare: a slot listed twice keeps its lowest position
-    for (int q = tid; q < H; q += kThreads) {
-      const int s = lru[q];
-      if (s >= 0 && s < H) mark[s] = kUnclaimed;
-    }
+#pragma unroll
+    for (int k = 0; k < IT; ++k)
+      if (k * kThreads + tid < H && sl[k] >= 0 && sl[k] < H) mark[sl[k]] = kUnclaimed;
     __syncthreads();
-    for (int q = tid; q < H; q += kThreads) {
-      const int s = lru[q];
-      if (s >= 0 && s < H) atomicMin(&mark[s], q);
-    }
+#pragma unroll
+    for (int k = 0; k < IT; ++k)
+      if (k * kThreads + tid < H && sl[k] >= 0 && sl[k] < H) atomicMin(&mark[sl[k]], k * kThreads + tid);
     __syncthreads();
   }
 
   // ---- P2: walk the LRU order; the lowest position holding a wanted token claims it.
-  for (int q = tid; q < H; q += kThreads) {
-    const int s = lru[q];
-    int f = -2;  // corrupt entry: out of range, or a repeat of an earlier slot
-    if (s >= 0 && s < H && (!slot_repeat || mark[s] == q)) {
-      f = -1;
-      const int32_t tk = tok[s];
-      const uint32_t bb = bloom_bit(tk);
-      if (tk >= 0 && tk < Lb && tk != Lb - 1 && ((bloom[bb >> 5] >> (bb & 31)) & 1u)) {
-        const int32_t i = hash_find(tab, tk, bits);
-        if (i >= 0) {
-          f = i;
-          atomicMin(&claim[i], q);
-        }
-      }
+  int f[IT];  // per position: the wanted entry it holds, -1 none, -2 corrupt entry
+  {
+    bool ok[IT];
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      const int q = k * kThreads + tid;
+      ok[k] = q < H && sl[k] >= 0 && sl[k] < H;
     }
-    found[q] = f;
+    if (slot_repeat) {
+#pragma unroll
+      for (int k = 0; k < IT; ++k)
+        if (ok[k]) ok[k] = mark[sl[k]] == k * kThreads + tid;
+    }
+    int32_t tk[IT];
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      f[k] = ok[k] ? -1 : -2;
+      tk[k] = ok[k] ? tok[sl[k]] : -1;
+    }
+    uint32_t bw[IT];
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      ok[k] = ok[k] && tk[k] >= 0 && tk[k] < Lb && tk[k] != Lb - 1;
+      bw[k] = ok[k] ? bloom[bloom_bit(tk[k]) >> 5] : 0u;
+    }
+    int2 kv[IT];
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      ok[k] = ok[k] && ((bw[k] >> (bloom_bit(tk[k]) & 31)) & 1u);
+      kv[k] = ok[k] ? tab[hash_of(tk[k], bits)] : make_int2(-1, -1);
+    }
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      if (!ok[k]) continue;
+      if (kv[k].x == tk[k])
+        f[k] = kv[k].y;
+      else if (kv[k].x != -1)
+        f[k] = probe_rest(tab, tk[k], hash_of(tk[k], bits), hmask);
+    }
+#pragma unroll
+    for (int k = 0; k < IT; ++k)
+      if (f[k] >= 0) atomicMin(&claim[f[k]], k * kThreads + tid);
   }
   __syncthreads();
   // Pool rows of the miss candidates (wanted, not newest, not claimed), loaded
@@ -424,10 +466,18 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
 
   // ---- P3: hit ranks in LRU order; evictables compacted in LRU order.
   const int chunks_p = (H + 31) / 32;
-  for (int base = 0; base < H; base += kThreads) {
-    const int q = base + tid;
-    const unsigned m = __ballot_sync(kFullMask, q < H && is_hit(found, claim, q));
-    if (lane == 0 && base + warp * 32 < H) cntp[(base >> 5) + warp] = __popc(m);
+  bool hit[IT];
+  unsigned hm[IT];
+  {
+    int cl[IT];
+#pragma unroll
+    for (int k = 0; k < IT; ++k) cl[k] = f[k] >= 0 ? claim[f[k]] : -1;
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      hit[k] = f[k] >= 0 && cl[k] == k * kThreads + tid;
+      hm[k] = __ballot_sync(kFullMask, hit[k]);
+      if (lane == 0 && k * kThreads + warp * 32 < H) cntp[k * 32 + warp] = __popc(hm[k]);
+    }
   }
   __syncthreads();
   if (warp == 0) {
@@ -435,15 +485,17 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     if (lane == 0) misc[kMiscHits] = nh;
   }
   __syncthreads();
-  for (int base = 0; base < H; base += kThreads) {
-    const int q = base + tid;
-    const bool hit = q < H && is_hit(found, claim, q);
-    const unsigned m = __ballot_sync(kFullMask, hit);
-    if (q < H && !hit) {
-      const int before = cntp[q >> 5] + __popc(m & lanes_before);
-      const bool corrupt = found[q] == -2;
+  int hb[IT];  // hits before each of my positions
+#pragma unroll
+  for (int k = 0; k < IT; ++k) {
+    const int q = k * kThreads + tid;
+    hb[k] = 0;
+    if (q >= H) continue;
+    hb[k] = cntp[k * 32 + warp] + __popc(hm[k] & lanes_before);
+    if (!hit[k]) {
+      const bool corrupt = f[k] == -2;
       if (corrupt) my_flags |= HS_ST_BAD_LRU_SLOT;
-      evl[q - before] = (corrupt ? 0x10000 : 0) | (lru[q] & 0xFFFF);
+      evl[q - hb[k]] = (corrupt ? 0x10000 : 0) | (sl[k] & 0xFFFF);
     }
   }
 
@@ -530,21 +582,18 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   }
 
   // ---- P5: my positions' places in the new LRU order.
-  for (int base = p0; base < p1; base += kThreads) {
-    const int q = base + tid;
-    const bool hit = q < p1 && is_hit(found, claim, q);
-    const unsigned m = __ballot_sync(kFullMask, hit);
-    if (q < p1) {
-      const int hr = cntp[q >> 5] + __popc(m & lanes_before);  // hits before q
-      int pos;
-      if (hit) {
-        pos = E + hr;
-      } else {
-        const int e = q - hr;
-        pos = e >= M ? e - M : E - M + e;
-      }
-      lru_g[pos] = lru[q];
+#pragma unroll
+  for (int k = 0; k < IT; ++k) {
+    const int q = k * kThreads + tid;
+    if (q < p0 || q >= p1) continue;
+    int pos;
+    if (hit[k]) {
+      pos = E + hb[k];
+    } else {
+      const int e = q - hb[k];
+      pos = e >= M ? e - M : E - M + e;
     }
+    lru_g[pos] = static_cast<int16_t>(sl[k]);
   }
   if (my_flags) atomicOr(&misc[kMiscFlags], my_flags);
   __syncthreads();
@@ -566,12 +615,13 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
 using KernelFn = void (*)(const SwapInParams);
 
 template <int G>
-KernelFn pick_kernel(int flags) {
-  const bool s64 = flags & HS_SEQ_LENS_I64, r64 = flags & HS_REQ_STATE_I64;
-  if (s64 && r64) return swap_in_kernel<int64_t, int64_t, G>;
-  if (s64) return swap_in_kernel<int64_t, int32_t, G>;
-  if (r64) return swap_in_kernel<int32_t, int64_t, G>;
-  return swap_in_kernel<int32_t, int32_t, G>;
+KernelFn pick_items(int items) {
+  switch (items) {
+    case 1: return swap_in_kernel<1, G>;
+    case 2: return swap_in_kernel<2, G>;
+    case 4: return swap_in_kernel<4, G>;
+    default: return swap_in_kernel<8, G>;
+  }
 }
 
 // Raises the dynamic shared-memory limit of a kernel once per device to the
@@ -612,7 +662,8 @@ int pick_cluster(int batch, int K, int H, int bits, const DeviceInfo& dev) {
 }  // namespace hs
 
 extern "C" int64_t hs_swap_in_smem_bytes(int32_t top_k, int32_t hot_size) {
-  if (top_k < 1 || hot_size < 1 || hot_size > 32767 || top_k > hot_size) return 0;
+  if (top_k < 1 || hot_size < 1 || hot_size > hs::kMaxItems * hs::kThreads || top_k > hot_size)
+    return 0;
   return hs::make_layout(top_k, hot_size, hs::kMaxCluster, hs::hash_bits_for(top_k, 2)).total;
 }
 
@@ -625,6 +676,9 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
                 a->top_k);
   if (a->hot_size < 1 || a->hot_size > 32767)
     return fail(HS_ERR_UNSUPPORTED, "hs_swap_in: hot_size %d outside [1, 32767]", a->hot_size);
+  if (a->hot_size > kMaxItems * kThreads)
+    return fail(HS_ERR_UNSUPPORTED, "hs_swap_in: this build handles hot_size <= %d",
+                kMaxItems * kThreads);
   if (a->top_k > a->hot_size)
     return fail(HS_ERR_UNSUPPORTED, "hs_swap_in: top_k %d > hot_size %d", a->top_k,
                 a->hot_size);
@@ -705,6 +759,7 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   p.hot_size = a->hot_size;
   p.cluster = C;
   p.hash_bits = bits;
+  p.flags = a->flags;
   p.num_real = a->num_real;
   p.topk_ids = a->topk_ids;
   p.topk_stride = a->topk_stride;
@@ -735,8 +790,10 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   p.chunks_per_row = static_cast<uint32_t>(cpr);
   p.div_chunks = FastDiv{fastdiv_magic(static_cast<uint32_t>(cpr)), static_cast<uint32_t>(cpr)};
 
-  KernelFn fn = G == 16 ? pick_kernel<16>(a->flags)
-                        : (G == 4 ? pick_kernel<4>(a->flags) : pick_kernel<1>(a->flags));
+  int items = 1;
+  while (items * kThreads < a->hot_size) items *= 2;
+  KernelFn fn = G == 16 ? pick_items<16>(items)
+                        : (G == 4 ? pick_items<4>(items) : pick_items<1>(items));
   err = ensure_smem(fn, dev.device, L.total);
   if (err != HS_OK) return err;
 
