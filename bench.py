@@ -215,6 +215,7 @@ class SwapInWorkload:
         import sparse_attention_kv_row_gb300 as hs
 
         self.hs = hs
+        self.overlap = True
         self.cfg, self.dev, self.layers = cfg, dev, layers
         B, H, S, L = cfg.batch, cfg.hot_size, cfg.row_bytes, cfg.seq_len
         self.n_pools = n_pools or layers
@@ -267,12 +268,15 @@ class SwapInWorkload:
         return self.stream.next().view(self.layers, self.cfg.batch, self.cfg.top_k)
 
     def args(self, l, topk, out=None, miss=None):
+        # Layer l's launch may overlap layer l-1's: its state rows are written
+        # only by its own launch of the previous decode step.
         return self.hs.make_swap_in_args(
             topk_ids=topk, seq_lens=self.seq, req_state=self.req, slot_tokens=self.tokens[l],
             slot_rows=self.rows[l], lru=self.lru[l], pool_rows=self.pool_rows[l],
             pool_k=self.pools[l % self.n_pools], hot_k=self.hot[l],
             out_rows=self.out[l] if out is None else out,
-            miss_count=self.miss[l] if miss is None else miss, stats=self.stats)
+            miss_count=self.miss[l] if miss is None else miss, stats=self.stats,
+            overlap_prev=self.overlap and l > 0)
 
     def eager_step(self, topk, stream):
         for l in range(self.layers):
@@ -388,13 +392,26 @@ def run_headline(args, dev, rank, world, dist):
     e2e_misses = int(w.stats[1].item())
     smi_summary = stop_smi(smi, smi_f, smi_path)
 
+    # the same decode step with every launch waiting for the one before it
+    w.overlap = False
+    n_seq = min(args.steps, 50)
+    seq_topks = [w.next_topk().clone() for _ in range(n_seq + 3)]  # alive while replayed
+    seq_graphs = [w.capture_step(t, s) for t in seq_topks]
+    timed_graphs(seq_graphs[:3], s)
+    w.stats.zero_()
+    torch.cuda.synchronize()
+    t_seq = timed_graphs(seq_graphs[3:], s)
+    seq_misses = int(w.stats[1].item())
+    w.overlap = True
+
     launches = NL * args.steps
     alg = swapin_alg_bytes(B, K, H, S, launches, misses)
     res = dict(t_dev=t_dev, hits=hits, misses=misses, launches=launches, alg_bytes=alg,
                n_pools=n_pools, t_e2e=t_e2e, wall_e2e=wall_e2e, e2e_misses=e2e_misses,
                e2e_steps=n_e2e, h2d=NL * B * K * 4, d2h=NL * B * K * 4 + NL * B * 4,
+               t_seq=t_seq, seq_steps=n_seq, seq_misses=seq_misses,
                clocks=sampler.summary(smi_summary))
-    del graphs, g_e2e
+    del graphs, g_e2e, seq_graphs, seq_topks
     w.free()
     torch.cuda.empty_cache()
     return res
@@ -737,7 +754,9 @@ def main():
                     hot_size=cfg.hot_size, row_bytes=cfg.row_bytes, layers=NL,
                     reuse=cfg.reuse, pools_distinct=h["n_pools"],
                     step="61 per-layer hs_swap_in launches, one CUDA graph per decode step, "
-                         "graphs replayed back to back",
+                         "graphs replayed back to back; layers 1..60 launched with "
+                         "HS_OVERLAP_PREV (each may start while the previous layer's "
+                         "swap-in finishes; it reads the top-k row only after that)",
                     l2="inputs larger than L2 (each step touches ~630 MB across 61 layers)",
                     parallelism=f"dp{world} (independent requests per GPU)"),
         us_per_decode_step=t_dev / args.steps * 1e6,
@@ -757,6 +776,11 @@ def main():
                  us_per_step=t_e2e / h["e2e_steps"] * 1e6,
                  how="every step: pinned-host top-k -> device, the step's 61 swap-ins "
                      "(CUDA graph through the C ABI), out rows and miss counts -> pinned host"),
+        sequential=dict(us_per_decode_step=h["t_seq"] / h["seq_steps"] * 1e6,
+                        value=h["seq_misses"] / h["t_seq"], unit="rows/s",
+                        steps=h["seq_steps"],
+                        how="the same decode step with every launch waiting for the one "
+                            "before it (no HS_OVERLAP_PREV)"),
         gpu_launches=launches,
         clocks=h["clocks"],
         ops=ops,

@@ -50,6 +50,13 @@ typedef enum hs_err {
 /* hs_swap_in_args.flags */
 #define HS_SEQ_LENS_I64 1  /* seq_lens is int64 (else int32) */
 #define HS_REQ_STATE_I64 2 /* req_state is int64 (else int32) */
+/* The call may start while the kernel before it in the stream is still
+ * running (programmatic dependent launch): until that kernel has completed it
+ * reads only seq_lens, req_state, num_real, slot_tokens, slot_rows and lru,
+ * and writes nothing.  Set it only when no kernel still in flight in the
+ * stream writes those six buffers; topk_ids and every other buffer may be
+ * written by the preceding kernel. */
+#define HS_OVERLAP_PREV 4
 
 /*
  * hs_swap_in -- resolve each batch row's top-k token ids against the row's
@@ -120,7 +127,7 @@ typedef struct hs_swap_in_args {
   int32_t batch;    /* B */
   int32_t top_k;    /* K */
   int32_t hot_size; /* H */
-  int32_t flags;    /* HS_SEQ_LENS_I64 | HS_REQ_STATE_I64 */
+  int32_t flags;    /* HS_SEQ_LENS_I64 | HS_REQ_STATE_I64 | HS_OVERLAP_PREV */
   const int32_t* num_real;
   const int32_t* topk_ids; int64_t topk_stride;
   const void* seq_lens;

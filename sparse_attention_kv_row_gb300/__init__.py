@@ -76,8 +76,14 @@ def swap_in_smem_bytes(top_k: int, hot_size: int) -> int:
 
 def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_rows,
                       pool_k, hot_k, out_rows, hot_size=None, pool_v=None, hot_v=None,
-                      num_real=None, miss_count=None, stats=None, status=None) -> SwapInArgs:
-    """Build a reusable ``hs_swap_in_args`` for these tensors (see include/hisparse.h)."""
+                      num_real=None, miss_count=None, stats=None, status=None,
+                      overlap_prev=False) -> SwapInArgs:
+    """Build a reusable ``hs_swap_in_args`` for these tensors (see include/hisparse.h).
+
+    ``overlap_prev`` sets HS_OVERLAP_PREV: the launch may start while the
+    kernel before it in the stream still runs, reading only the request
+    metadata and state rows (seq_lens, req_state, num_real, slot_tokens,
+    slot_rows, lru) until that kernel completes."""
     H = int(hot_size if hot_size is not None else lru.shape[1])
     _need(topk_ids, torch.int32, "topk_ids", 2)
     _need(out_rows, torch.int32, "out_rows", 2)
@@ -119,8 +125,9 @@ def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, 
             raise ValueError("V buffers need the same row width as K")
         p_rows, h_rows = min(p_rows, pv_rows), min(h_rows, hv_rows)
     flags = (_capi.SEQ_LENS_I64 if seq_lens.dtype == torch.int64 else 0) | (
-        _capi.REQ_STATE_I64 if req_state.dtype == torch.int64 else 0)
-    return SwapInArgs(
+        _capi.REQ_STATE_I64 if req_state.dtype == torch.int64 else 0) | (
+        _capi.OVERLAP_PREV if overlap_prev else 0)
+    args = SwapInArgs(
         batch=B, top_k=K, hot_size=H, flags=flags, num_real=_ptr(num_real),
         topk_ids=_ptr(topk_ids), topk_stride=topk_ids.stride(0),
         seq_lens=_ptr(seq_lens), req_state=_ptr(req_state),
@@ -135,6 +142,10 @@ def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, 
         hot_k=hk_ptr, hot_v=hv_ptr, hot_num_rows=h_rows,
         row_bytes=row_bytes, out_rows=_ptr(out_rows), out_stride=out_rows.stride(0),
         miss_count=_ptr(miss_count), stats=_ptr(stats), status=_ptr(status))
+    # the struct holds raw pointers: keep the tensors alive as long as it lives
+    args.tensors = (topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_rows,
+                    pool_k, pool_v, hot_k, hot_v, out_rows, num_real, miss_count, stats, status)
+    return args
 
 
 def swap_in_args(args: SwapInArgs, stream=None) -> None:

@@ -22,6 +22,7 @@ ST_BAD_STATE = 32
 ST_BAD_INDEX = 64
 SEQ_LENS_I64 = 1
 REQ_STATE_I64 = 2
+OVERLAP_PREV = 4
 ABI_VERSION = 1
 
 # Every symbol include/hisparse.h declares.

@@ -85,6 +85,17 @@ __device__ __forceinline__ void cp_async_commit_wait_all() {
 // in flight).  Each of the < 16 head bytes and < 16 tail bytes is loaded by one
 // thread into a register and stored by stage_finish() only after the caller's
 // LDGSTS wait, so no thread stalls on it in between.
+// ------------------------------------------------------------------ grid dependency
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialization may start before the preceding kernel in its stream has
+// finished; `grid_dep_wait` blocks until that kernel has completed and its
+// writes are visible (a no-op for a grid launched the ordinary way), and
+// `grid_dep_launch_dependents` lets the next such grid start early.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 struct StagePending {
   int32_t off;  // byte offset in dst, or -1
   uint32_t val;

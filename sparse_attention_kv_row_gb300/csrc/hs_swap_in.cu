@@ -16,14 +16,15 @@
 // them.  The only cross-CTA step is one split cluster barrier: no CTA writes
 // the row's LRU order or slot tokens before every CTA has staged them.
 //
-//   P0 stage    the row's ids, LRU order, slot tokens and slot rows into
-//               shared memory with LDGSTS (all in flight at once);
-//   P1 hash     all valid ids into an open-addressing table (Knuth
-//               multiplicative hash, linear probing, one CAS per id); only when
-//               an id repeats does a second pass make its smallest entry
-//               index canonical.  The LRU row is checked to be a permutation
-//               (plain stores, then a lowest-position pass only if a slot
-//               repeats);
+//   P0 stage    the row's LRU order, slot tokens and slot rows into shared
+//               memory with LDGSTS (head and tail bytes asynchronously);
+//   P1 state    check the LRU row is a permutation of the slots (one atomicOr
+//               bitmap pass; a lowest-position pass only if a slot repeats)
+//               and gather each position's slot token into registers;
+//      request  then the top-k row: all valid ids into an open-addressing
+//               table (Knuth multiplicative hash, linear probing, one CAS per
+//               id) and a 16 KB bitmap filter; only when an id repeats does a
+//               second pass make its smallest entry index canonical;
 //   P2 walk     every position probes its slot's token; the lowest position
 //               holding a wanted token claims the entry (atomicMin);
 //   P3 hits     position-ordered ballot/popc + one warp scan of chunk counts:
@@ -37,6 +38,11 @@
 //   P6 copy     (miss, 16-byte chunk) work items over all threads: read-only
 //               no-L1 loads from the pool (HBM or pinned host memory), L2-only
 //               stores into the hot buffer.
+//
+// With HS_OVERLAP_PREV the launch may begin while the preceding kernel in the
+// stream is still running: P0 and the state half of P1 read only request
+// metadata and state rows, and the grid-dependency wait sits right before the
+// top-k row is read; nothing is written to global memory before it.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -250,11 +256,17 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const int p0 = min(H, j * L.slice_p), p1 = min(H, p0 + L.slice_p);  // my LRU positions
   const int e0 = min(K, j * L.slice_e), e1 = min(K, e0 + L.slice_e);  // my entries
 
-  // ---- P0: stage the top-k row first; it does not depend on the state row.
+  // ---- P0: request metadata and the state row.  With HS_OVERLAP_PREV this
+  // grid may start while the preceding kernel in the stream still runs: until
+  // grid_dep_wait() it reads only the request's metadata and state row and
+  // writes nothing to global memory; the top-k row is read after the wait.
+  grid_dep_launch_dependents();
+  const bool overlap = (p.flags & HS_OVERLAP_PREV) != 0;
   const int32_t* ids_g = p.topk_ids + static_cast<int64_t>(b) * p.topk_stride;
   int32_t* ids = reinterpret_cast<int32_t*>(smem + L.o_ids +
                                             (reinterpret_cast<uintptr_t>(ids_g) & 15u));
-  const StagePending pend_ids = stage_bytes(ids, ids_g, 4LL * K, tid, kThreads);
+  StagePending pend_ids{-1, 0u};
+  if (!overlap) pend_ids = stage_bytes(ids, ids_g, 4LL * K, tid, kThreads);
 
   int32_t* out_g = p.out_rows + static_cast<int64_t>(b) * p.out_stride;
   const bool pad_nr = p.num_real != nullptr && b >= __ldg(p.num_real);
@@ -266,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
                          : static_cast<int64_t>(__ldg(static_cast<const int32_t*>(p.seq_lens) + b));
 
   if (pad_nr || r < 0 || r >= p.num_states) {  // padding row / bad state row
+    grid_dep_wait();
     cp_async_commit_wait_all();
     for (int i = e0 + tid; i < e1; i += kThreads) out_g[i] = -1;
     if (j == 0 && tid == 0) {
@@ -277,6 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
 
   const int32_t* rows_g = p.slot_rows + r * p.slot_rows_stride;
   if (Lb <= H) {  // fast path: the whole sequence sits in the hot buffer in order
+    grid_dep_wait();
+    if (overlap) pend_ids = stage_bytes(ids, ids_g, 4LL * K, tid, kThreads);
     cp_async_commit_wait_all();
     stage_finish(ids, pend_ids);
     __syncthreads();
@@ -326,7 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   for (int i = tid; i < (H + 31) / 32; i += kThreads) sbits[i] = 0;
   if (tid < 8) misc[tid] = 0;
   cp_async_commit_wait_all();
-  stage_finish(ids, pend_ids);
   stage_finish(lru, pend_lru);
   stage_finish(tok, pend_tok);
   stage_finish(rows, pend_rows);
@@ -335,10 +349,72 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   // matching wait comes right before the first write to that state.
   cluster_arrive();
 
-  // ---- P1: hash the valid ids; mark each slot with its LRU position.
+  // ---- P1 (state half): check the LRU row is a permutation of the slots.
+  int32_t my_flags = 0;
+  int sl[IT];  // the slot at each of my LRU positions
+#pragma unroll
+  for (int k = 0; k < IT; ++k) {
+    const int q = k * kThreads + tid;
+    sl[k] = q < H ? lru[q] : 0;
+  }
+#pragma unroll
+  for (int k = 0; k < IT; ++k) {
+    if (k * kThreads + tid >= H) continue;
+    if (sl[k] >= 0 && sl[k] < H) {
+      const uint32_t bit = 1u << (sl[k] & 31);
+      if (atomicOr(&sbits[sl[k] >> 5], bit) & bit) misc[kMiscSlotRepeat] = 1;
+    } else {
+      my_flags |= HS_ST_BAD_LRU_SLOT;
+    }
+  }
+  __syncthreads();
+  const bool slot_repeat = misc[kMiscSlotRepeat] != 0;
+  if (slot_repeat) {  // rare: a slot listed twice keeps its lowest position
+#pragma unroll
+    for (int k = 0; k < IT; ++k)
+      if (k * kThreads + tid < H && sl[k] >= 0 && sl[k] < H) mark[sl[k]] = kUnclaimed;
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < IT; ++k)
+      if (k * kThreads + tid < H && sl[k] >= 0 && sl[k] < H) atomicMin(&mark[sl[k]], k * kThreads + tid);
+    __syncthreads();
+  }
+  // The token each of my positions holds, if it could be wanted.
+  int f[IT];  // per position: the wanted entry it holds, -1 none, -2 corrupt entry
+  int32_t tk[IT];
+  bool ok[IT];
+  {
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      const int q = k * kThreads + tid;
+      ok[k] = q < H && sl[k] >= 0 && sl[k] < H;
+    }
+    if (slot_repeat) {
+#pragma unroll
+      for (int k = 0; k < IT; ++k)
+        if (ok[k]) ok[k] = mark[sl[k]] == k * kThreads + tid;
+    }
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      f[k] = ok[k] ? -1 : -2;
+      tk[k] = ok[k] ? tok[sl[k]] : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < IT; ++k) ok[k] = ok[k] && tk[k] >= 0 && tk[k] < Lb && tk[k] != Lb - 1;
+  }
+
+  // ---- P1 (request half): the top-k row, written by the preceding kernel.
+  grid_dep_wait();
+  if (overlap) {
+    pend_ids = stage_bytes(ids, ids_g, 4LL * K, tid, kThreads);
+    cp_async_commit_wait_all();
+  }
+  stage_finish(ids, pend_ids);
+  __syncthreads();
+  // Hash the valid ids; only when an id repeats does a second pass make its
+  // smallest entry index canonical.
   const int bits = L.hash_bits;
   const uint32_t hmask = static_cast<uint32_t>(L.hash_size) - 1u;
-  int32_t my_flags = 0;
   for (int i = tid; i < K; i += kThreads) {
     const int32_t t = ids[i];
     if (t >= 0 && t < Lb) {
@@ -359,24 +435,8 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       }
     }
   }
-  int sl[IT];  // the slot at each of my LRU positions
-#pragma unroll
-  for (int k = 0; k < IT; ++k) {
-    const int q = k * kThreads + tid;
-    sl[k] = q < H ? lru[q] : 0;
-  }
-#pragma unroll
-  for (int k = 0; k < IT; ++k) {
-    if (k * kThreads + tid >= H) continue;
-    if (sl[k] >= 0 && sl[k] < H) {
-      const uint32_t bit = 1u << (sl[k] & 31);
-      if (atomicOr(&sbits[sl[k] >> 5], bit) & bit) misc[kMiscSlotRepeat] = 1;
-    } else {
-      my_flags |= HS_ST_BAD_LRU_SLOT;
-    }
-  }
   __syncthreads();
-  if (misc[kMiscRepeat]) {  // rare: the smallest index of a repeated id is canonical
+  if (misc[kMiscRepeat]) {  // rare
     for (int i = tid; i < K; i += kThreads) {
       const int32_t t = ids[i];
       if (t >= 0 && t < Lb) {
@@ -390,46 +450,14 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
         }
       }
     }
-  }
-  __syncthreads();
-  const bool slot_repeat = misc[kMiscSlotRepeat] != 0;
-  if (slot_repeat) {  // rare: a slot listed twice keeps its lowest position
-#pragma unroll
-    for (int k = 0; k < IT; ++k)
-      if (k * kThreads + tid < H && sl[k] >= 0 && sl[k] < H) mark[sl[k]] = kUnclaimed;
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < IT; ++k)
-      if (k * kThreads + tid < H && sl[k] >= 0 && sl[k] < H) atomicMin(&mark[sl[k]], k * kThreads + tid);
     __syncthreads();
   }
 
   // ---- P2: walk the LRU order; the lowest position holding a wanted token claims it.
-  int f[IT];  // per position: the wanted entry it holds, -1 none, -2 corrupt entry
   {
-    bool ok[IT];
-#pragma unroll
-    for (int k = 0; k < IT; ++k) {
-      const int q = k * kThreads + tid;
-      ok[k] = q < H && sl[k] >= 0 && sl[k] < H;
-    }
-    if (slot_repeat) {
-#pragma unroll
-      for (int k = 0; k < IT; ++k)
-        if (ok[k]) ok[k] = mark[sl[k]] == k * kThreads + tid;
-    }
-    int32_t tk[IT];
-#pragma unroll
-    for (int k = 0; k < IT; ++k) {
-      f[k] = ok[k] ? -1 : -2;
-      tk[k] = ok[k] ? tok[sl[k]] : -1;
-    }
     uint32_t bw[IT];
 #pragma unroll
-    for (int k = 0; k < IT; ++k) {
-      ok[k] = ok[k] && tk[k] >= 0 && tk[k] < Lb && tk[k] != Lb - 1;
-      bw[k] = ok[k] ? bloom[bloom_bit(tk[k]) >> 5] : 0u;
-    }
+    for (int k = 0; k < IT; ++k) bw[k] = ok[k] ? bloom[bloom_bit(tk[k]) >> 5] : 0u;
     int2 kv[IT];
 #pragma unroll
     for (int k = 0; k < IT; ++k) {
@@ -683,7 +711,7 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
     return fail(HS_ERR_UNSUPPORTED, "hs_swap_in: top_k %d > hot_size %d", a->top_k,
                 a->hot_size);
   if (a->row_bytes < 1) return fail(HS_ERR_ARG, "hs_swap_in: row_bytes must be >= 1");
-  if (a->flags & ~(HS_SEQ_LENS_I64 | HS_REQ_STATE_I64))
+  if (a->flags & ~(HS_SEQ_LENS_I64 | HS_REQ_STATE_I64 | HS_OVERLAP_PREV))
     return fail(HS_ERR_ARG, "hs_swap_in: unknown flags 0x%x", a->flags);
   if (a->batch == 0 || a->top_k == 0) return HS_OK;
 
@@ -802,13 +830,15 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = L.total;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = (a->flags & HS_OVERLAP_PREV) ? 2 : 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p);
   if (e != cudaSuccess) return fail(HS_ERR_CUDA, "hs_swap_in launch: %s", cudaGetErrorString(e));
   return HS_OK;

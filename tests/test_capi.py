@@ -67,6 +67,7 @@ def _args(**kw):
     (dict(batch=-1), 1),
     (dict(row_bytes=0), 1),
     (dict(flags=8), 1),
+    (dict(flags=16), 1),
     (dict(), 1),                    # required pointers are NULL
 ])
 def test_swap_in_rejects(lib, kw, code):

@@ -178,3 +178,81 @@ def test_row_subsets_match_whole_batch(dev):
         for a, b in ((whole.tokens, split.tokens), (whole.lru, split.lru),
                      (whole.hot_k, split.hot_k)):
             assert torch.equal(a, b), f"step {step}"
+
+
+@pytest.mark.parametrize("mode", ["chain", "interleaved", "graph"])
+def test_overlap_prev(dev, mode):
+    """HS_OVERLAP_PREV: launches that may start before the preceding kernel
+    finishes still match the oracle.  'chain': one kernel writes every layer's
+    top-k rows, then the layers' swap-ins run back to back (each may overlap
+    the one before); 'interleaved': a kernel writes layer l's top-k rows right
+    before layer l's swap-in; 'graph': the chain captured in a CUDA graph.
+    Rows include a padding row and a short sequence (the fast path)."""
+    import sparse_attention_kv_row_gb300 as hs
+    import synth
+
+    rng = np.random.default_rng(123)
+    NL, B, K, H, L = 4, 5, 300, 1000, 9000
+    refs, gpus = [], []
+    for l in range(NL):
+        ref = cases.random_case(rng, B=B, K=K, H=H, S=132, R=B + 2, seq_len=L)
+        ref.seq_lens[1] = H - 3  # fast path
+        ref.num_real = B - 1     # last row is padding
+        refs.append(ref)
+        gpus.append(GpuCase(ref.copy(), dev))
+    stream_ = [synth.TopkStream(40 + l, 0, B, K, L, 0.8) for l in range(NL)]
+    # top-k rows sit at the end of a large buffer so the writing kernel reaches them late
+    big = 1 << 24
+    src = torch.zeros(big + NL * B * K, dtype=torch.int32, device=dev)
+    dst = torch.zeros_like(src)
+    topk = dst[big:].view(NL, B, K)
+    outs = torch.zeros((NL, B, K), dtype=torch.int32, device=dev)
+    miss = torch.zeros((NL, B), dtype=torch.int32, device=dev)
+    num_real = torch.tensor([B - 1], dtype=torch.int32, device=dev)
+    args = [hs.make_swap_in_args(
+        topk_ids=topk[l], seq_lens=torch.from_numpy(refs[l].seq_lens).to(dev),
+        req_state=torch.from_numpy(refs[l].req_state).to(dev), slot_tokens=gpus[l].tokens,
+        slot_rows=gpus[l].rows, lru=gpus[l].lru, pool_rows=gpus[l].pool_rows,
+        pool_k=gpus[l].pool_k, hot_k=gpus[l].hot_k, out_rows=outs[l], miss_count=miss[l],
+        num_real=num_real, overlap_prev=True) for l in range(NL)]
+    s = torch.cuda.Stream()
+
+    def step_chain():
+        torch.add(src, 0, out=dst)
+        for a in args:
+            hs.swap_in_args(a, stream=s)
+
+    graph = None
+    if mode == "graph":
+        snap = [(g.tokens.clone(), g.lru.clone(), g.hot_k.clone()) for g in gpus]
+        with torch.cuda.stream(s):
+            step_chain()  # one eager pass first (one-time kernel set-up), then restore
+        torch.cuda.synchronize()
+        for g, (t, lr, hk) in zip(gpus, snap):
+            g.tokens.copy_(t); g.lru.copy_(lr); g.hot_k.copy_(hk)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            step_chain()
+        torch.cuda.synchronize()
+    for step in range(4):
+        ids = np.stack([st.next() for st in stream_])
+        src[big:].copy_(torch.from_numpy(ids.reshape(-1)))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            if mode == "chain":
+                step_chain()
+            elif mode == "interleaved":
+                for l in range(NL):
+                    torch.add(src[big + l * B * K: big + (l + 1) * B * K], l * 0,
+                              out=dst[big + l * B * K: big + (l + 1) * B * K])
+                    hs.swap_in_args(args[l], stream=s)
+            else:
+                graph.replay()
+        torch.cuda.synchronize()
+        for l in range(NL):
+            refs[l].topk = ids[l]
+            r_out, r_miss, _, _ = cases.run_oracle(refs[l])
+            np.testing.assert_array_equal(outs[l].cpu().numpy(), r_out, f"{mode} {step} {l}")
+            np.testing.assert_array_equal(miss[l].cpu().numpy(), r_miss)
+            gpus[l].assert_matches(refs[l], f"{mode} step {step} layer {l}")
