@@ -47,6 +47,8 @@ class _SwapInArgs(C.Structure):
         ("row_bytes", C.c_int64),
         ("out_rows", C.c_void_p), ("out_stride", C.c_int64),
         ("miss_count", C.c_void_p), ("stats", C.c_void_p), ("status", C.c_void_p),
+        ("miss_src", C.c_void_p), ("miss_dst", C.c_void_p), ("plan_stride", C.c_int64),
+        ("miss_mask", C.c_void_p), ("mask_stride", C.c_int64),
     ]
 
 
@@ -69,6 +71,11 @@ def load(mutant: int = 0) -> C.CDLL:
                                         C.c_int64, C.c_int64, C.c_int64, C.c_int64,
                                         C.c_void_p]
         lib.hso_transfer_kv.restype = C.c_int
+        lib.hso_gather_misses.argtypes = [C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p,
+                                          C.c_void_p, C.c_int64, C.c_int64, C.c_void_p,
+                                          C.c_void_p, C.c_int64, C.c_void_p, C.c_int32,
+                                          C.c_int32, C.c_void_p]
+        lib.hso_gather_misses.restype = C.c_int
         _LIBS[mutant] = lib
     return _LIBS[mutant]
 
@@ -93,7 +100,8 @@ def _check(a, dtype, name, ndim=None):
 
 def swap_in(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_rows,
             pool_k, hot_k, out_rows, hot_size, pool_v=None, hot_v=None, num_real=-1,
-            miss_count=None, stats=None, status=None, mutant: int = 0) -> None:
+            miss_count=None, stats=None, status=None, miss_src=None, miss_dst=None,
+            miss_mask=None, mutant: int = 0) -> None:
     """One swap-in call over B batch rows; mutates slot_tokens, lru, hot_k/hot_v,
     out_rows and the optional outputs in place (all numpy, host memory).
 
@@ -101,6 +109,9 @@ def swap_in(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_
     slot_tokens / slot_rows int32 [R, >=H+1]; lru int16 [R, >=H];
     pool_rows int64 [R, cols]; pool_k/pool_v uint8 [P, S];
     hot_k/hot_v uint8 [rows, S]; out_rows int32 [B, K].
+    Optional plan outputs: miss_src int64 [B, >=K] and miss_dst int32 [B, >=K]
+    (the row's misses in order; entries past the miss count untouched),
+    miss_mask int32 [B, >=K].
     """
     _check(topk_ids, np.int32, "topk_ids", 2)
     _check(seq_lens, np.int64, "seq_lens", 1)
@@ -115,6 +126,13 @@ def swap_in(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_
     _check(miss_count, np.int32, "miss_count", 1)
     _check(stats, np.uint64, "stats", 1)
     _check(status, np.int32, "status", 1)
+    _check(miss_src, np.int64, "miss_src", 2)
+    _check(miss_dst, np.int32, "miss_dst", 2)
+    _check(miss_mask, np.int32, "miss_mask", 2)
+    if (miss_src is None) != (miss_dst is None):
+        raise ValueError("miss_src and miss_dst go together")
+    if miss_src is not None and _row_stride(miss_src) != _row_stride(miss_dst):
+        raise ValueError("miss_src and miss_dst need the same row stride")
     for a in (seq_lens, req_state, pool_k, pool_v, hot_k, hot_v, miss_count, stats, status):
         if a is not None:
             assert a.flags.c_contiguous
@@ -132,10 +150,34 @@ def swap_in(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_
         hot_k=_ptr(hot_k), hot_v=_ptr(hot_v), hot_num_rows=hot_k.shape[0],
         row_bytes=pool_k.shape[1],
         out_rows=_ptr(out_rows), out_stride=_row_stride(out_rows),
-        miss_count=_ptr(miss_count), stats=_ptr(stats), status=_ptr(status))
+        miss_count=_ptr(miss_count), stats=_ptr(stats), status=_ptr(status),
+        miss_src=_ptr(miss_src), miss_dst=_ptr(miss_dst),
+        plan_stride=_row_stride(miss_src) if miss_src is not None else 0,
+        miss_mask=_ptr(miss_mask),
+        mask_stride=_row_stride(miss_mask) if miss_mask is not None else 0)
     rc = load(mutant).hso_swap_in(C.byref(a))
     if rc != 0:
         raise ValueError("oracle swap_in rejected its arguments")
+
+
+def gather_misses(*, pool_k, hot_k, miss_src, miss_dst, miss_count, pool_v=None, hot_v=None,
+                  status=None, mutant: int = 0) -> None:
+    """Replay a swap-in's miss plan onto another layer: hot row miss_dst[b][m] =
+    pool row miss_src[b][m] for m < miss_count[b] (K, and V when given)."""
+    for n, a in (("pool_k", pool_k), ("pool_v", pool_v), ("hot_k", hot_k), ("hot_v", hot_v)):
+        _check(a, np.uint8, n, 2)
+    _check(miss_src, np.int64, "miss_src", 2)
+    _check(miss_dst, np.int32, "miss_dst", 2)
+    _check(miss_count, np.int32, "miss_count", 1)
+    if _row_stride(miss_src) != _row_stride(miss_dst):
+        raise ValueError("miss_src and miss_dst need the same row stride")
+    B, K = miss_src.shape
+    rc = load(mutant).hso_gather_misses(
+        _ptr(pool_k), _ptr(pool_v), pool_k.shape[0], _ptr(hot_k), _ptr(hot_v), hot_k.shape[0],
+        pool_k.shape[1], _ptr(miss_src), _ptr(miss_dst), _row_stride(miss_src),
+        _ptr(miss_count), B, K, _ptr(status))
+    if rc != 0:
+        raise ValueError("oracle gather_misses rejected its arguments")
 
 
 def store_kv(*, k_src, v_src, k_dst, v_dst, loc, status=None) -> None:

@@ -17,6 +17,10 @@
  *    padding rows publish -1, corruption tripwires (LRU slot out of range,
  *    eviction slot out of range), hit/miss statistics, the same writeback
  *    stated a second way.
+ *  - vLLM csrc/libtorch_stable/hisparse_kernels.cu, hisparse_gather_plan_kernel
+ *    and hisparse_gather_compact_kernel: a resolving layer's miss plan (which
+ *    entries missed, which pool row went to which hot row) replayed onto a
+ *    layer that shares its indices, with no LRU resolution.
  *  - tokenspeed tokenspeed_kernel/ops/kvcache/triton.py, store_kv_cache and
  *    transfer_kv_per_layer / transfer_kv_all_layer(_mla): indexed row scatter
  *    and gather over per-layer pointer arrays.
@@ -65,6 +69,8 @@ void swap_in_row(const hso_swap_in_args* a, int32_t b) {
   const int32_t H = a->hot_size;
   int32_t* out = a->out_rows + (int64_t)b * a->out_stride;
   const int32_t* ids = a->topk_ids + (int64_t)b * a->topk_stride;
+  if (a->miss_mask)
+    for (int32_t i = 0; i < K; ++i) a->miss_mask[(int64_t)b * a->mask_stride + i] = 0;
 
   // Step 1: CUDA-graph padding rows.
   if (a->num_real >= 0 && b >= a->num_real) { pad_row(a, b); return; }
@@ -182,6 +188,11 @@ void swap_in_row(const hso_swap_in_args* a, int32_t b) {
   int32_t applied = 0;
   for (int32_t m = 0; m < M; ++m) {
     const Miss& ms = misses[m];
+    if (a->miss_mask) a->miss_mask[(int64_t)b * a->mask_stride + ms.i] = 1;
+    if (a->miss_src) {
+      a->miss_src[(int64_t)b * a->plan_stride + m] = ms.pool_row;
+      a->miss_dst[(int64_t)b * a->plan_stride + m] = -1;  // set below once a row is given
+    }
     const int32_t s = order[m];
     if (order_bad[m]) { st |= HSO_ST_BAD_LRU_SLOT; continue; }
     const int32_t hr = rows[s];
@@ -189,6 +200,11 @@ void swap_in_row(const hso_swap_in_args* a, int32_t b) {
     // Corrupt entries (out of range, or a repeat of an earlier slot) were
     // marked in the walk, so every slot written here is distinct.
     out[ms.i] = hr;
+#if HSO_MUTANT == 12
+    if (a->miss_src) a->miss_dst[(int64_t)b * a->plan_stride + m] = s;
+#else
+    if (a->miss_src) a->miss_dst[(int64_t)b * a->plan_stride + m] = hr;
+#endif
     tokens[s] = ms.id;
 #if HSO_MUTANT == 6
     const int64_t src_row = ms.id;
@@ -244,6 +260,38 @@ extern "C" int hso_swap_in(const hso_swap_in_args* a) {
     return -1;
   if (a->batch <= 0 || a->top_k == 0) return 0;
   for (int32_t b = 0; b < a->batch; ++b) swap_in_row(a, b);
+  return 0;
+}
+
+extern "C" int hso_gather_misses(const uint8_t* pool_k, const uint8_t* pool_v,
+                                 int64_t pool_num_rows, uint8_t* hot_k, uint8_t* hot_v,
+                                 int64_t hot_num_rows, int64_t row_bytes, const int64_t* miss_src,
+                                 const int32_t* miss_dst, int64_t plan_stride,
+                                 const int32_t* miss_count, int32_t batch, int32_t top_k,
+                                 int32_t* status) {
+  if (row_bytes < 1 || batch < 0 || top_k < 0) return -1;
+  for (int32_t b = 0; b < batch; ++b) {
+    int32_t n = miss_count[b];
+    if (n < 0) n = 0;
+#if HSO_MUTANT == 11
+    if (n > top_k + 1) n = top_k + 1;
+    for (int32_t m = 0; m <= n && m < top_k; ++m) {
+#else
+    if (n > top_k) n = top_k;
+    for (int32_t m = 0; m < n; ++m) {
+#endif
+      const int64_t s = miss_src[(int64_t)b * plan_stride + m];
+      const int32_t d = miss_dst[(int64_t)b * plan_stride + m];
+      if (d < 0) continue;  // this miss was given no hot row
+      if (s < 0 || s >= pool_num_rows || (int64_t)d >= hot_num_rows) {
+        if (status) *status |= HSO_ST_BAD_INDEX;
+        continue;
+      }
+      std::memcpy(hot_k + (int64_t)d * row_bytes, pool_k + s * row_bytes, (size_t)row_bytes);
+      if (pool_v)
+        std::memcpy(hot_v + (int64_t)d * row_bytes, pool_v + s * row_bytes, (size_t)row_bytes);
+    }
+  }
   return 0;
 }
 

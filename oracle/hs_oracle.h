@@ -50,11 +50,28 @@ typedef struct hso_swap_in_args {
   int32_t* miss_count;                                  /* [B] or NULL */
   uint64_t* stats;                                      /* [2] accumulated, or NULL */
   int32_t* status;                                      /* [B] or NULL */
+  /* Optional plan outputs (NULL = not written), for replay onto layers that
+   * share this call's indices: the row's m-th miss (m < miss_count[b]) came
+   * from pool row miss_src[b][m] and was given hot row miss_dst[b][m] (-1 when
+   * it got none); entries past the miss count are left as they were.
+   * miss_mask[b][i] = 1 when top-k entry i was one of the row's misses. */
+  int64_t* miss_src; int32_t* miss_dst; int64_t plan_stride;   /* [B, >=K] */
+  int32_t* miss_mask; int64_t mask_stride;                      /* [B, >=K] */
 } hso_swap_in_args;
 
 /* Returns 0, or -1 when an argument is unusable (the oracle does not try to
  * mirror every synchronous check of the CUDA library). */
 int hso_swap_in(const hso_swap_in_args* a);
+
+/* Replays a swap-in's miss plan onto another layer's pool and hot buffer:
+ * for b < batch, m < min(max(miss_count[b], 0), top_k): d = miss_dst[b][m],
+ * s = miss_src[b][m]; d < 0 is skipped silently; s outside [0,pool_num_rows)
+ * or d >= hot_num_rows is skipped with HSO_ST_BAD_INDEX OR-ed into *status;
+ * otherwise hot row d = pool row s (K, and V when pool_v is not NULL). */
+int hso_gather_misses(const uint8_t* pool_k, const uint8_t* pool_v, int64_t pool_num_rows,
+                      uint8_t* hot_k, uint8_t* hot_v, int64_t hot_num_rows, int64_t row_bytes,
+                      const int64_t* miss_src, const int32_t* miss_dst, int64_t plan_stride,
+                      const int32_t* miss_count, int32_t batch, int32_t top_k, int32_t* status);
 
 /* dst_k[loc[t]] = k_src[t] (and V), tokens in order; loc out of [0,dst_rows)
  * is skipped with HSO_ST_BAD_INDEX OR-ed into *status. */

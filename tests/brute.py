@@ -59,13 +59,18 @@ def writeback_vllm(hits, evict, M, H):
     return new
 
 
-def swap_in_row(ids, seq_len, H, tokens, rows, lru, pool_rows, pool, hot, hot_num_rows):
+def swap_in_row(ids, seq_len, H, tokens, rows, lru, pool_rows, pool, hot, hot_num_rows,
+                plan=None):
     """One batch row.  ``tokens``/``rows`` are lists of length >= H+1, ``lru`` a list
     of length H, ``pool_rows`` a list (token -> pool row), ``pool`` a list of bytes
     rows, ``hot`` a list of bytearray rows.  Mutates tokens, lru, hot.
-    Returns (out, miss_count, hits, status)."""
+    Returns (out, miss_count, hits, status).  When ``plan`` is a dict it receives
+    the miss plan: 'src' (pool row of each miss, in order), 'dst' (the hot row it
+    was given, or -1) and 'mask' (1 for each top-k entry that was a miss)."""
     K = len(ids)
     out = [-1] * K
+    if plan is not None:
+        plan.update(src=[], dst=[], mask=[0] * K)
     if seq_len <= H:
         count = min(seq_len, K)
         for i in range(K):
@@ -125,6 +130,10 @@ def swap_in_row(ids, seq_len, H, tokens, rows, lru, pool_rows, pool, hot, hot_nu
     assert M <= len(evict)
 
     for m, (i, t, pr) in enumerate(misses):
+        if plan is not None:
+            plan["mask"][i] = 1
+            plan["src"].append(pr)
+            plan["dst"].append(-1)
         s, bad = evict[m]
         if bad:
             st |= BAD_LRU
@@ -133,6 +142,8 @@ def swap_in_row(ids, seq_len, H, tokens, rows, lru, pool_rows, pool, hot, hot_nu
         if not (0 <= hr < hot_num_rows):
             st |= BAD_HOT
             continue
+        if plan is not None:
+            plan["dst"][m] = hr
         out[i] = hr
         tokens[s] = t
         hot[hr][:] = pool[pr]
@@ -145,11 +156,16 @@ def swap_in_row(ids, seq_len, H, tokens, rows, lru, pool_rows, pool, hot, hot_nu
     return out, M, len(hits), st
 
 
-def swap_in(ids_rows, seq_lens, req_state, H, state, pool_rows, pool, hot, num_real=-1):
-    """Batch version over dict-of-lists state {'tokens','rows','lru'} keyed by state row."""
+def swap_in(ids_rows, seq_lens, req_state, H, state, pool_rows, pool, hot, num_real=-1,
+            plans=None):
+    """Batch version over dict-of-lists state {'tokens','rows','lru'} keyed by state row.
+    When ``plans`` is a list, one miss-plan dict per batch row is appended to it."""
     outs, miss, status = [], [], []
     stats = [0, 0]
     for b, ids in enumerate(ids_rows):
+        plan = {"src": [], "dst": [], "mask": [0] * len(ids)}
+        if plans is not None:
+            plans.append(plan)
         r = req_state[b]
         if (num_real >= 0 and b >= num_real) or r < 0:
             outs.append([-1] * len(ids)); miss.append(0); status.append(0)
@@ -159,9 +175,24 @@ def swap_in(ids_rows, seq_lens, req_state, H, state, pool_rows, pool, hot, num_r
             continue
         o, m, h, st = swap_in_row(list(ids), seq_lens[b], H, state["tokens"][r],
                                   state["rows"][r], state["lru"][r], pool_rows[r], pool, hot,
-                                  len(hot))
+                                  len(hot), plan=plan)
         outs.append(o); miss.append(m); status.append(st)
         if seq_lens[b] > H:
             stats[0] += h
             stats[1] += m
     return outs, miss, status, stats
+
+
+def gather_misses(plans, miss_count, pool, hot):
+    """Replay per-row miss plans onto another layer's pool/hot rows (lists)."""
+    status = 0
+    for b, plan in enumerate(plans):
+        for m in range(max(0, min(miss_count[b], len(plan["mask"])))):
+            s, d = plan["src"][m], plan["dst"][m]
+            if d < 0:
+                continue
+            if not (0 <= s < len(pool)) or d >= len(hot):
+                status |= 64
+                continue
+            hot[d][:] = pool[s]
+    return status

@@ -82,25 +82,37 @@ def random_ids(rng, case: Case, *, p_invalid=0.1, p_dup=0.1, p_newest=0.1, p_reu
     return out
 
 
-def run_oracle(case: Case, mutant: int = 0):
-    """One oracle step; mutates ``case`` state, returns (out, miss, status, stats)."""
+PLAN_FILL_SRC, PLAN_FILL_DST = 3, 1  # valid-looking values in unwritten plan entries
+
+
+def run_oracle(case: Case, mutant: int = 0, plan: bool = False):
+    """One oracle step; mutates ``case`` state, returns (out, miss, status, stats),
+    plus (miss_src, miss_dst, miss_mask) when ``plan``."""
     import oracle
 
     out = np.full((case.B, case.K), 12345, dtype=np.int32)
     miss = np.full(case.B, 777, dtype=np.int32)
     status = np.full(case.B, 999, dtype=np.int32)
     stats = np.zeros(2, dtype=np.uint64)
+    kw = {}
+    if plan:
+        kw = dict(miss_src=np.full((case.B, case.K), PLAN_FILL_SRC, dtype=np.int64),
+                  miss_dst=np.full((case.B, case.K), PLAN_FILL_DST, dtype=np.int32),
+                  miss_mask=np.full((case.B, case.K), 7, dtype=np.int32))
     oracle.swap_in(topk_ids=case.topk, seq_lens=case.seq_lens, req_state=case.req_state,
                    slot_tokens=case.tokens, slot_rows=case.rows, lru=case.lru,
                    pool_rows=case.pool_rows, pool_k=case.pool_k, pool_v=case.pool_v,
                    hot_k=case.hot_k, hot_v=case.hot_v, out_rows=out, hot_size=case.H,
                    num_real=case.num_real, miss_count=miss, stats=stats, status=status,
-                   mutant=mutant)
+                   mutant=mutant, **kw)
+    if plan:
+        return out, miss, status, stats, kw["miss_src"], kw["miss_dst"], kw["miss_mask"]
     return out, miss, status, stats
 
 
-def run_brute(case: Case):
-    """One brute-force step on list copies; writes the new state back into ``case``."""
+def run_brute(case: Case, plans=None):
+    """One brute-force step on list copies; writes the new state back into ``case``.
+    When ``plans`` is a list it receives one miss-plan dict per batch row."""
     import brute
 
     H = case.H
@@ -114,7 +126,7 @@ def run_brute(case: Case):
     outs, miss, status, stats = brute.swap_in(
         [list(map(int, r)) for r in case.topk], [int(x) for x in case.seq_lens],
         [int(x) for x in case.req_state], H, state, pool_rows, pool, hot,
-        num_real=case.num_real)
+        num_real=case.num_real, plans=plans)
     case.tokens[:] = np.array(state["tokens"], dtype=np.int32)
     case.lru[:, :H] = np.array(state["lru"], dtype=np.int16)
     case.hot_k[:] = np.frombuffer(b"".join(bytes(r) for r in hot), dtype=np.uint8).reshape(
