@@ -117,8 +117,10 @@ __device__ __forceinline__ StagePending stage_bytes(void* dst, const void* src, 
     pend.off = static_cast<int32_t>(head + body + (tid - 32));
     pend.val = sc[pend.off];
   }
-  for (int64_t o = head + static_cast<int64_t>(tid) * 16; o < head + body;
-       o += static_cast<int64_t>(nthreads) * 16)
+  // Offsets fit 32 bits: staged rows are at most a few hundred KB.
+  const uint32_t end = static_cast<uint32_t>(head + body);
+  for (uint32_t o = static_cast<uint32_t>(head) + static_cast<uint32_t>(tid) * 16u; o < end;
+       o += static_cast<uint32_t>(nthreads) * 16u)
     cp_async_16(dc + o, sc + o);
   return pend;
 }

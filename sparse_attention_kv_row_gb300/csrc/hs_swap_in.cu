@@ -146,6 +146,7 @@ struct SwapInParams {
   int32_t* status;
   uint32_t chunks_per_row;  // row_bytes / copy width
   FastDiv div_chunks;
+  Layout lay;               // shared-memory layout, computed once on the host
 };
 
 enum { kMiscFlags = 0, kMiscRepeat = 1, kMiscSlotRepeat = 2, kMiscHits = 3, kMiscMisses = 4 };
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const int b = blockIdx.x / C;
   const int K = p.top_k;
   const int H = p.hot_size;
-  const Layout L = make_layout(K, H, C, p.hash_bits);
+  const Layout& L = p.lay;
   const int p0 = min(H, j * L.slice_p), p1 = min(H, p0 + L.slice_p);  // my LRU positions
   const int e0 = min(K, j * L.slice_e), e1 = min(K, e0 + L.slice_e);  // my entries
 
@@ -307,6 +308,10 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     return;
   }
 
+  // A top-k id t is valid iff 0 <= t < Lb: as one unsigned compare against
+  // min(Lb, 2^31); the newest token is Lb - 1 (no int32 id matches -1 here).
+  const uint32_t lim = Lb < (1ll << 31) ? static_cast<uint32_t>(Lb) : 0x80000000u;
+  const int32_t newest = Lb - 1 <= INT32_MAX ? static_cast<int32_t>(Lb - 1) : -1;
   int32_t* tokens_g = p.slot_tokens + r * p.slot_tokens_stride;
   int16_t* lru_g = p.lru + r * p.lru_stride;
   int16_t* lru = reinterpret_cast<int16_t*>(smem + L.o_lru +
@@ -336,9 +341,15 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     int4* t4 = reinterpret_cast<int4*>(tab);
     for (int i = tid; i < L.hash_size / 2; i += kThreads) t4[i] = make_int4(-1, -1, -1, -1);
   }
-  for (int i = tid; i < K; i += kThreads) claim[i] = kUnclaimed;
-  for (int i = tid; i < (1 << (kBloomBits - 5)); i += kThreads) bloom[i] = 0;
-  for (int i = tid; i < (H + 31) / 32; i += kThreads) sbits[i] = 0;
+  {  // whole 16-byte words: every region is padded to 16 bytes
+    int4* c4 = reinterpret_cast<int4*>(claim);
+    for (int i = tid; i < (K + 3) / 4; i += kThreads)
+      c4[i] = make_int4(kUnclaimed, kUnclaimed, kUnclaimed, kUnclaimed);
+    int4* b4 = reinterpret_cast<int4*>(bloom);
+    for (int i = tid; i < (1 << (kBloomBits - 7)); i += kThreads) b4[i] = make_int4(0, 0, 0, 0);
+    int4* s4 = reinterpret_cast<int4*>(sbits);
+    for (int i = tid; i < ((H + 31) / 32 + 3) / 4; i += kThreads) s4[i] = make_int4(0, 0, 0, 0);
+  }
   if (tid < 8) misc[tid] = 0;
   cp_async_commit_wait_all();
   stage_finish(lru, pend_lru);
@@ -400,7 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       tk[k] = ok[k] ? tok[sl[k]] : -1;
     }
 #pragma unroll
-    for (int k = 0; k < IT; ++k) ok[k] = ok[k] && tk[k] >= 0 && tk[k] < Lb && tk[k] != Lb - 1;
+    for (int k = 0; k < IT; ++k)
+      ok[k] = ok[k] && static_cast<uint32_t>(tk[k]) < lim && tk[k] != newest;
   }
 
   // ---- P1 (request half): the top-k row, written by the preceding kernel.
@@ -417,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const uint32_t hmask = static_cast<uint32_t>(L.hash_size) - 1u;
   for (int i = tid; i < K; i += kThreads) {
     const int32_t t = ids[i];
-    if (t >= 0 && t < Lb) {
+    if (static_cast<uint32_t>(t) < lim) {
       const uint32_t bb = bloom_bit(t);
       atomicOr(&bloom[bb >> 5], 1u << (bb & 31));
       uint32_t h = hash_of(t, bits);
@@ -439,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   if (misc[kMiscRepeat]) {  // rare
     for (int i = tid; i < K; i += kThreads) {
       const int32_t t = ids[i];
-      if (t >= 0 && t < Lb) {
+      if (static_cast<uint32_t>(t) < lim) {
         uint32_t h = hash_of(t, bits);
         for (uint32_t n = 0; n <= hmask; ++n) {
           if (tab[h].x == t) {
@@ -483,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const int64_t* pool_rows_g = p.pool_rows + r * p.pool_rows_stride;
   for (int i = tid; i < K; i += kThreads) {
     const int32_t t = ids[i];
-    const bool cand = t >= 0 && t < Lb && t != Lb - 1 && claim[i] == kUnclaimed &&
+    const bool cand = static_cast<uint32_t>(t) < lim && t != newest && claim[i] == kUnclaimed &&
                       t < p.pool_rows_cols && (!id_repeat || hash_find(tab, t, bits) == i);
     if (cand)
       cp_async_8(&prs[i], pool_rows_g + t);
@@ -537,12 +549,12 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     if (i < K) {
       const int32_t t = ids[i];
       int8_t c;
-      if (t < 0 || t >= Lb) {
+      if (static_cast<uint32_t>(t) >= lim) {
         c = kInvalid;
       } else if (id_repeat && hash_find(tab, t, bits) != i) {
         c = kRepeat;
         my_flags |= HS_ST_DUP_ID;
-      } else if (t == Lb - 1) {
+      } else if (t == newest) {
         c = kNewest;
       } else if (claim[i] != kUnclaimed) {
         c = kHit;
@@ -574,11 +586,13 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const int my_first_miss = e0 < K ? cnte[e0 >> 5] : M;
   // The first state write of the row follows: wait until every CTA has staged.
   cluster_wait();
+  // Only my own entries: their chunks are whole and 32-aligned, so a warp's
+  // ballot covers one chunk.
   int64_t my_pr = 0;
-  for (int base = 0; base < K; base += kThreads) {
+  for (int base = e0; base < e1; base += kThreads) {
     const int i = base + tid;
-    const bool mine = i >= e0 && i < e1;
-    const int8_t c = i < K ? code[i] : kInvalid;
+    const bool mine = i < e1;
+    const int8_t c = mine ? code[i] : kInvalid;
     const unsigned m = __ballot_sync(kFullMask, c == kMiss);
     if (mine) my_pr = c == kMiss ? jsrc[i - e0] : 0;
     __syncthreads();  // jsrc is rewritten in compacted order below
@@ -591,21 +605,25 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
         const int32_t hr = rows[s];
         if (hr >= 0 && hr < p.hot_num_rows) {
           d = hr;
-          if (mine) tokens_g[s] = ids[i];
-        } else {
-          my_flags |= HS_ST_BAD_HOT_ROW;
+          tokens_g[s] = ids[i];
         }
       }
-      if (mine) {
-        out_g[i] = d;
-        jsrc[mm - my_first_miss] = my_pr;
-        jdst[mm - my_first_miss] = d;
-      }
+      out_g[i] = d;
+      jsrc[mm - my_first_miss] = my_pr;
+      jdst[mm - my_first_miss] = d;
     } else if (mine) {
       int32_t o = -1;
       if (c == kNewest) o = rows[H];  // the newest token lives in slot H
       if (c == kHit) o = rows[lru[claim[i]]];
       out_g[i] = o;
+    }
+  }
+  if (j == 0) {  // the row's status covers every miss's hot row
+    for (int mm = tid; mm < M; mm += kThreads) {
+      const int32_t e = evl[mm];
+      if (e >> 16) continue;
+      const int32_t hr = rows[static_cast<int16_t>(e & 0xFFFF)];
+      if (hr < 0 || hr >= p.hot_num_rows) my_flags |= HS_ST_BAD_HOT_ROW;
     }
   }
 
@@ -817,6 +835,7 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   p.status = a->status;
   p.chunks_per_row = static_cast<uint32_t>(cpr);
   p.div_chunks = FastDiv{fastdiv_magic(static_cast<uint32_t>(cpr)), static_cast<uint32_t>(cpr)};
+  p.lay = L;
 
   int items = 1;
   while (items * kThreads < a->hot_size) items *= 2;
