@@ -85,6 +85,65 @@ __device__ __forceinline__ void cp_async_commit_wait_all() {
 // in flight).  Each of the < 16 head bytes and < 16 tail bytes is loaded by one
 // thread into a register and stored by stage_finish() only after the caller's
 // LDGSTS wait, so no thread stalls on it in between.
+// ------------------------------------------------------------------ bulk copies
+// One-dimensional bulk copies global -> shared through the tensor memory
+// accelerator, completed on an mbarrier by transaction bytes.
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Orders this thread's earlier shared-memory accesses before later
+// async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+// One arrival that also announces `bytes` more transaction bytes.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+          smem_addr(bar)),
+      "r"(bytes)
+      : "memory");
+}
+// Polls for the completion of phase `parity`, at most `max_polls` times;
+// returns false if the phase did not complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_polls) {
+  for (uint32_t n = 0; n < max_polls; ++n) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst_smem)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
 // ------------------------------------------------------------------ grid dependency
 // Programmatic dependent launch: a grid launched with programmatic stream
 // serialization may start before the preceding kernel in its stream has
@@ -126,6 +185,42 @@ __device__ __forceinline__ StagePending stage_bytes(void* dst, const void* src, 
 }
 __device__ __forceinline__ void stage_finish(void* dst, StagePending pend) {
   if (pend.off >= 0) static_cast<unsigned char*>(dst)[pend.off] = static_cast<unsigned char>(pend.val);
+}
+
+// Staging by one bulk copy: the 16-byte-aligned body of [src, src + nbytes)
+// goes to dst (dst must be congruent to src modulo 16) through the tensor
+// memory accelerator; the unaligned head and tail bytes are loaded by threads
+// into a StagePending exactly as stage_bytes does.
+struct StageSplit {
+  uint32_t head, body;
+};
+__device__ __forceinline__ StageSplit stage_split(const void* src, int64_t nbytes) {
+  const uintptr_t s = reinterpret_cast<uintptr_t>(src);
+  int64_t head = static_cast<int64_t>((16u - (s & 15u)) & 15u);
+  if (head > nbytes) head = nbytes;
+  return StageSplit{static_cast<uint32_t>(head),
+                    static_cast<uint32_t>(((nbytes - head) >> 4) << 4)};
+}
+__device__ __forceinline__ StagePending stage_edges(const void* src, int64_t nbytes, StageSplit sp,
+                                                    int tid) {
+  const unsigned char* sc = static_cast<const unsigned char*>(src);
+  const uint32_t tail = static_cast<uint32_t>(nbytes) - sp.head - sp.body;
+  StagePending pend{-1, 0};
+  if (static_cast<uint32_t>(tid) < sp.head) {
+    pend.off = tid;
+    pend.val = sc[tid];
+  } else if (tid >= 32 && static_cast<uint32_t>(tid) < 32u + tail) {
+    pend.off = static_cast<int32_t>(sp.head + sp.body + (tid - 32));
+    pend.val = sc[pend.off];
+  }
+  return pend;
+}
+// Issued by one thread after the barrier was armed for the bodies' bytes.
+__device__ __forceinline__ void stage_body(void* dst, const void* src, StageSplit sp,
+                                           uint64_t* bar) {
+  if (sp.body > 0)
+    bulk_load(static_cast<char*>(dst) + sp.head, static_cast<const char*>(src) + sp.head, sp.body,
+              bar);
 }
 
 // ------------------------------------------------------------------ scans

@@ -60,6 +60,7 @@ constexpr int kMaxItems = 8;  // LRU positions per thread: hot_size <= 8192
 constexpr int kCopyUnroll = 4;
 constexpr int kMaxCluster = 8;
 constexpr int32_t kUnclaimed = INT_MAX;
+constexpr uint32_t kMaxPolls = 1u << 22;  // bounded mbarrier waits
 
 // Per-entry classification, stored as one byte per top-k entry.
 enum : int8_t { kInvalid = 0, kRepeat = 1, kNewest = 2, kHit = 3, kBadPool = 4, kMiss = 5 };
@@ -68,7 +69,7 @@ constexpr int kBloomBits = 17;  // request filter: 2^17 bits = 16 KB
 
 struct Layout {
   int hash_bits, hash_size, slice_p, slice_e;
-  int o_hash, o_bloom, o_prs, o_ids, o_lru, o_tok, o_rows, o_mark, o_sbits, o_claim, o_evl, o_cntp, o_cnte, o_code, o_misc, o_jsrc, o_jdst;
+  int o_hash, o_bloom, o_prs, o_ids, o_lru, o_tok, o_rows, o_mark, o_sbits, o_claim, o_evl, o_cntp, o_cnte, o_code, o_misc, o_bar, o_jsrc, o_jdst;
   int total;
 };
 
@@ -110,6 +111,7 @@ __host__ __device__ inline Layout make_layout(int K, int H, int C, int bits) {
   L.o_cnte = take(&o, 4 * chunks_e);      // per-chunk miss counts -> exclusive prefixes
   L.o_code = take(&o, K);                 // per-entry classification
   L.o_misc = take(&o, 4 * 8);
+  L.o_bar = take(&o, 16);                 // mbarriers: [0] top-k row, [1] state row
   L.o_jsrc = take(&o, 8 * L.slice_e);     // my misses: pool row
   L.o_jdst = take(&o, 4 * L.slice_e);     // my misses: hot row or -1
   L.total = o;
@@ -261,13 +263,30 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   // grid may start while the preceding kernel in the stream still runs: until
   // grid_dep_wait() it reads only the request's metadata and state row and
   // writes nothing to global memory; the top-k row is read after the wait.
+  // Rows are staged by bulk copies (their 16-byte-aligned bodies) completed
+  // on two mbarriers, one per row kind, each used for one phase; the
+  // unaligned head and tail bytes go through registers.
   grid_dep_launch_dependents();
   const bool overlap = (p.flags & HS_OVERLAP_PREV) != 0;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.o_bar);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    mbar_init(bar + 1, 1);
+    fence_mbar_init();
+  }
   const int32_t* ids_g = p.topk_ids + static_cast<int64_t>(b) * p.topk_stride;
   int32_t* ids = reinterpret_cast<int32_t*>(smem + L.o_ids +
                                             (reinterpret_cast<uintptr_t>(ids_g) & 15u));
+  const StageSplit sp_ids = stage_split(ids_g, 4LL * K);
   StagePending pend_ids{-1, 0u};
-  if (!overlap) pend_ids = stage_bytes(ids, ids_g, 4LL * K, tid, kThreads);
+  auto stage_ids = [&]() {
+    pend_ids = stage_edges(ids_g, 4LL * K, sp_ids, tid);
+    if (tid == 0) {
+      mbar_arrive_expect_tx(bar, sp_ids.body);
+      stage_body(ids, ids_g, sp_ids, bar);
+    }
+  };
+  if (!overlap) stage_ids();
 
   int32_t* out_g = p.out_rows + static_cast<int64_t>(b) * p.out_stride;
   const bool pad_nr = p.num_real != nullptr && b >= __ldg(p.num_real);
@@ -280,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
 
   if (pad_nr || r < 0 || r >= p.num_states) {  // padding row / bad state row
     grid_dep_wait();
-    cp_async_commit_wait_all();
+    if (!overlap && tid == 0) mbar_wait(bar, 0, kMaxPolls);  // no copy left in flight
     for (int i = e0 + tid; i < e1; i += kThreads) out_g[i] = -1;
     if (j == 0 && tid == 0) {
       if (p.miss_count) p.miss_count[b] = 0;
@@ -292,10 +311,16 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const int32_t* rows_g = p.slot_rows + r * p.slot_rows_stride;
   if (Lb <= H) {  // fast path: the whole sequence sits in the hot buffer in order
     grid_dep_wait();
-    if (overlap) pend_ids = stage_bytes(ids, ids_g, 4LL * K, tid, kThreads);
-    cp_async_commit_wait_all();
+    if (overlap) stage_ids();
+    __syncthreads();  // the barriers' initialisation is visible
     stage_finish(ids, pend_ids);
-    __syncthreads();
+    if (!__syncthreads_and(mbar_wait(bar, 0, kMaxPolls))) {
+      if (tid == 0) {
+        if (p.status) atomicOr(p.status + b, HS_ST_TIMEOUT);
+        mbar_wait(bar, 0, kMaxPolls);
+      }
+      return;
+    }
     const int64_t count = Lb < K ? Lb : K;
     for (int i = e0 + tid; i < e1; i += kThreads) {
       const int32_t t = ids[i];
@@ -320,9 +345,18 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
                                             (reinterpret_cast<uintptr_t>(tokens_g) & 15u));
   int32_t* rows = reinterpret_cast<int32_t*>(smem + L.o_rows +
                                              (reinterpret_cast<uintptr_t>(rows_g) & 15u));
-  const StagePending pend_lru = stage_bytes(lru, lru_g, 2LL * H, tid, kThreads);
-  const StagePending pend_tok = stage_bytes(tok, tokens_g, 4LL * H, tid, kThreads);
-  const StagePending pend_rows = stage_bytes(rows, rows_g, 4LL * (H + 1), tid, kThreads);
+  const StageSplit sp_lru = stage_split(lru_g, 2LL * H);
+  const StageSplit sp_tok = stage_split(tokens_g, 4LL * H);
+  const StageSplit sp_rows = stage_split(rows_g, 4LL * (H + 1));
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar + 1, sp_lru.body + sp_tok.body + sp_rows.body);
+    stage_body(lru, lru_g, sp_lru, bar + 1);
+    stage_body(tok, tokens_g, sp_tok, bar + 1);
+    stage_body(rows, rows_g, sp_rows, bar + 1);
+  }
+  const StagePending pend_lru = stage_edges(lru_g, 2LL * H, sp_lru, tid);
+  const StagePending pend_tok = stage_edges(tokens_g, 4LL * H, sp_tok, tid);
+  const StagePending pend_rows = stage_edges(rows_g, 4LL * (H + 1), sp_rows, tid);
 
   int2* tab = reinterpret_cast<int2*>(smem + L.o_hash);
   uint32_t* bloom = reinterpret_cast<uint32_t*>(smem + L.o_bloom);
@@ -351,14 +385,22 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     for (int i = tid; i < ((H + 31) / 32 + 3) / 4; i += kThreads) s4[i] = make_int4(0, 0, 0, 0);
   }
   if (tid < 8) misc[tid] = 0;
-  cp_async_commit_wait_all();
+  __syncthreads();  // the barriers' initialisation is visible
   stage_finish(lru, pend_lru);
   stage_finish(tok, pend_tok);
   stage_finish(rows, pend_rows);
-  __syncthreads();
+  const bool staged = __syncthreads_and(mbar_wait(bar + 1, 0, kMaxPolls));
   // Every CTA of the row has staged the state once all have arrived here; the
   // matching wait comes right before the first write to that state.
   cluster_arrive();
+  if (!staged) {  // a bounded wait ran out: report it and leave the row alone
+    if (tid == 0) {
+      if (p.status) atomicOr(p.status + b, HS_ST_TIMEOUT);
+      mbar_wait(bar + 1, 0, kMaxPolls);
+      if (!overlap) mbar_wait(bar, 0, kMaxPolls);
+    }
+    return;
+  }
 
   // ---- P1 (state half): check the LRU row is a permutation of the slots.
   int32_t my_flags = 0;
@@ -417,12 +459,15 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
 
   // ---- P1 (request half): the top-k row, written by the preceding kernel.
   grid_dep_wait();
-  if (overlap) {
-    pend_ids = stage_bytes(ids, ids_g, 4LL * K, tid, kThreads);
-    cp_async_commit_wait_all();
-  }
+  if (overlap) stage_ids();
   stage_finish(ids, pend_ids);
-  __syncthreads();
+  if (!__syncthreads_and(mbar_wait(bar, 0, kMaxPolls))) {
+    if (tid == 0) {
+      if (p.status) atomicOr(p.status + b, HS_ST_TIMEOUT);
+      mbar_wait(bar, 0, kMaxPolls);
+    }
+    return;
+  }
   // Hash the valid ids; only when an id repeats does a second pass make its
   // smallest entry index canonical.
   const int bits = L.hash_bits;
