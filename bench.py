@@ -403,18 +403,83 @@ def run_headline(args, dev, rank, world, dist):
     t_seq = timed_graphs(seq_graphs[3:], s)
     seq_misses = int(w.stats[1].item())
     w.overlap = True
+    del seq_graphs, seq_topks
+    shared = run_shared_index(w, args, s)
 
     launches = NL * args.steps
     alg = swapin_alg_bytes(B, K, H, S, launches, misses)
     res = dict(t_dev=t_dev, hits=hits, misses=misses, launches=launches, alg_bytes=alg,
                n_pools=n_pools, t_e2e=t_e2e, wall_e2e=wall_e2e, e2e_misses=e2e_misses,
                e2e_steps=n_e2e, h2d=NL * B * K * 4, d2h=NL * B * K * 4 + NL * B * 4,
-               t_seq=t_seq, seq_steps=n_seq, seq_misses=seq_misses,
+               t_seq=t_seq, seq_steps=n_seq, seq_misses=seq_misses, shared=shared,
                clocks=sampler.summary(smi_summary))
-    del graphs, g_e2e, seq_graphs, seq_topks
+    del graphs, g_e2e
     w.free()
     torch.cuda.empty_cache()
     return res
+
+
+def run_shared_index(w, args, stream, group=4):
+    """The same decode step when layers share their indexer in groups of
+    `group` (the first layer of a group resolves and emits its miss plan; the
+    others replay it with hs_gather_misses into their own hot buffers)."""
+    hs, cfg = w.hs, w.cfg
+    B, K, NL = cfg.batch, cfg.top_k, w.layers
+    dev = w.dev
+    heads = list(range(0, NL, group))
+    plans = {g: (torch.empty((B, K), dtype=torch.int64, device=dev),
+                 torch.empty((B, K), dtype=torch.int32, device=dev)) for g in heads}
+    n = min(args.steps, 50)
+    # one miss-count vector per (step, group): the replayed rows are counted
+    # after the timed region from these
+    misses = torch.zeros((n + 3, len(heads), B), dtype=torch.int32, device=dev)
+
+    shared_layers, ptrs = {}, {}
+    for gi, g in enumerate(heads):
+        ls = list(range(g + 1, min(g + group, NL)))
+        if ls:
+            shared_layers[gi] = ([w.pools[l % w.n_pools] for l in ls], [w.hot[l] for l in ls])
+            ptrs[gi] = tuple(hs.layer_pointer_array(x, dev) for x in shared_layers[gi])
+
+    def capture(k, topk):
+        argv = []
+        for gi, g in enumerate(heads):
+            src, dst = plans[g]
+            a = hs.make_swap_in_args(
+                topk_ids=topk[g], seq_lens=w.seq, req_state=w.req, slot_tokens=w.tokens[g],
+                slot_rows=w.rows[g], lru=w.lru[g], pool_rows=w.pool_rows[g],
+                pool_k=w.pools[g % w.n_pools], hot_k=w.hot[g], out_rows=w.out[g],
+                miss_count=misses[k, gi], stats=w.stats, miss_src=src, miss_dst=dst,
+                overlap_prev=g > 0)
+            argv.append((gi, g, a))
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for gi, g, a in argv:
+                hs.swap_in_args(a, stream)
+                src, dst = plans[g]
+                if gi in shared_layers:  # one replay launch for the group's other layers
+                    pl, hl = shared_layers[gi]
+                    hs.gather_misses(pl, hl, src, dst, misses[k, gi], stream=stream,
+                                     ptrs=ptrs[gi])
+        return gr
+
+    topks = [w.next_topk().clone() for _ in range(n + 3)]
+    graphs = [capture(k, t) for k, t in enumerate(topks)]
+    timed_graphs(graphs[:3], stream)
+    w.stats.zero_()
+    torch.cuda.synchronize()
+    t = timed_graphs(graphs[3:], stream)
+    resolved = int(w.stats[1].item())
+    shared = torch.tensor([min(g + group, NL) - g - 1 for g in heads], device=dev)
+    replayed = int((misses[3:].sum(dim=2).to(torch.int64) * shared).sum().item())
+    del graphs, topks
+    return dict(us_per_decode_step=t / n * 1e6, value=(resolved + replayed) / t, unit="rows/s",
+                steps=n, resolving_layers=len(heads), replaying_layers=NL - len(heads),
+                resolved_rows_per_step=resolved / n, replayed_rows_per_step=replayed / n,
+                how=f"layers share their indexer in groups of {group}: per group one "
+                    "hs_swap_in emitting its miss plan, then one hs_gather_misses launch "
+                    "replaying it into the group's other layers' hot buffers; one CUDA graph "
+                    "per step")
 
 
 # --------------------------------------------------------------------------- other ops
@@ -781,6 +846,7 @@ def main():
                         steps=h["seq_steps"],
                         how="the same decode step with every launch waiting for the one "
                             "before it (no HS_OVERLAP_PREV)"),
+        shared_index=h["shared"],
         gpu_launches=launches,
         clocks=h["clocks"],
         ops=ops,

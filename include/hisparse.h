@@ -112,6 +112,18 @@ typedef enum hs_err {
  *  out_rows    int32 [batch, >=top_k]           stride out_stride
  *  miss_count  int32 [batch] or NULL; stats uint64 [2] (+= hits, misses) or NULL;
  *  status      int32 [batch] or NULL (per-row HS_ST_* bits, overwritten)
+ *  miss_src    int64 [batch, >=top_k] or NULL  stride plan_stride  } the miss plan,
+ *  miss_dst    int32 [batch, >=top_k] or NULL  stride plan_stride  } for replay by
+ *  miss_mask   int32 [batch, >=top_k] or NULL  stride mask_stride  } hs_gather_misses
+ *
+ * Miss plan (optional; vLLM csrc/libtorch_stable/hisparse_kernels.cu,
+ * hisparse_gather_plan_kernel and hisparse_gather_compact_kernel): for the
+ * row's m-th miss (m < miss_count[b], top-k order) miss_src[b][m] is the pool
+ * row it was copied from and miss_dst[b][m] the hot row it was given (-1 when
+ * it was given none); entries past the miss count are not written.
+ * miss_mask[b][i] is 1 when top-k entry i was one of the row's misses, else 0
+ * (all 0 for padding rows and short sequences).  miss_src and miss_dst go
+ * together and need miss_count.
  *
  * Limits: 1 <= top_k <= hot_size <= 32767 (slots are int16).  Each row runs
  * on a cluster of up to 8 CTAs; every CTA holds the row's ids, LRU order, slot
@@ -144,6 +156,8 @@ typedef struct hs_swap_in_args {
   int32_t* miss_count;
   unsigned long long* stats;
   int32_t* status;
+  int64_t* miss_src; int32_t* miss_dst; int64_t plan_stride;
+  int32_t* miss_mask; int64_t mask_stride;
 } hs_swap_in_args;
 
 hs_err hs_swap_in(const hs_swap_in_args* args, hs_stream_t stream);
@@ -201,6 +215,34 @@ hs_err hs_transfer_kv(const uint64_t* src_ptrs, const uint64_t* dst_ptrs, int32_
                       hs_stream_t stream);
 
 /*
+ * hs_gather_misses -- replay a swap-in's miss plan onto the layers that share
+ * the resolving layer's indices (same slot assignment, other bytes): for
+ * b < batch, m < min(max(miss_count[b], 0), top_k) and every pointer pair p in
+ * [0, num_layers * (1 + has_v)), with s = miss_src[b][m], d = miss_dst[b][m]:
+ * d < 0 is skipped; s outside [0, pool_num_rows) or d >= hot_num_rows skips
+ * the miss (for every layer) and ORs HS_ST_BAD_INDEX into *status; otherwise
+ * row d of hot_ptrs[p] = row s of pool_ptrs[p].  With has_v the arrays hold
+ * num_layers K pointers followed by num_layers V pointers, as in
+ * hs_transfer_kv.  No LRU state is read or written.  Defined by: vLLM
+ * csrc/libtorch_stable/hisparse_kernels.cu, hisparse_gather_plan_kernel and
+ * hisparse_gather_compact_kernel (shared-layer plan replay; per-row miss lists
+ * bounded by per-row counts, fixed shape for graph capture).
+ *
+ *  pool_ptrs   device uint64 [num_layers * (1 + has_v)]: pools of
+ *              [pool_num_rows, row_bytes] contiguous rows, device or pinned host
+ *  hot_ptrs    device uint64, same length: device hot buffers [hot_num_rows, row_bytes]
+ *  miss_src    device int64 [batch, >=top_k], miss_dst device int32, both stride plan_stride
+ *  miss_count  device int32 [batch]
+ *  status      device int32 [1] or NULL
+ * Precondition (not checked): the miss_dst values a call copies to are distinct.
+ */
+hs_err hs_gather_misses(const uint64_t* pool_ptrs, const uint64_t* hot_ptrs, int32_t num_layers,
+                        int32_t has_v, int64_t pool_num_rows, int64_t hot_num_rows,
+                        int64_t row_bytes, const int64_t* miss_src, const int32_t* miss_dst,
+                        int64_t plan_stride, const int32_t* miss_count, int32_t batch,
+                        int32_t top_k, int32_t* status, hs_stream_t stream);
+
+/*
  * hs_probe_read -- measurement utility, not part of the method: stream-read
  * `bytes` bytes (16-byte aligned pointer, bytes % 16 == 0) from device or
  * pinned host memory with every SM, folding them into *sink (device uint64
@@ -220,7 +262,7 @@ const char* hs_status_string(int32_t bit);
 const char* hs_last_error(void);
 
 /* ABI version of this header. */
-#define HS_ABI_VERSION 1
+#define HS_ABI_VERSION 2
 int32_t hs_abi_version(void);
 
 #ifdef __cplusplus

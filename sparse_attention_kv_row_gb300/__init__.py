@@ -23,7 +23,7 @@ from . import _capi
 from ._capi import (HisparseError, SwapInArgs, ST_BAD_HOT_ROW, ST_BAD_INDEX,  # noqa: F401
                     ST_BAD_LRU_SLOT, ST_BAD_POOL_ROW, ST_BAD_STATE, ST_DUP_ID, ST_TIMEOUT)
 
-__all__ = ["swap_in", "swap_in_args", "make_swap_in_args", "store_kv", "transfer_kv",
+__all__ = ["swap_in", "swap_in_args", "make_swap_in_args", "gather_misses", "store_kv", "transfer_kv",
            "transfer_kv_layers", "probe_read", "swap_in_smem_bytes", "library_path",
            "HisparseError", "SwapInArgs"]
 
@@ -77,13 +77,19 @@ def swap_in_smem_bytes(top_k: int, hot_size: int) -> int:
 def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_rows,
                       pool_k, hot_k, out_rows, hot_size=None, pool_v=None, hot_v=None,
                       num_real=None, miss_count=None, stats=None, status=None,
+                      miss_src=None, miss_dst=None, miss_mask=None,
                       overlap_prev=False) -> SwapInArgs:
     """Build a reusable ``hs_swap_in_args`` for these tensors (see include/hisparse.h).
 
     ``overlap_prev`` sets HS_OVERLAP_PREV: the launch may start while the
     kernel before it in the stream still runs, reading only the request
     metadata and state rows (seq_lens, req_state, num_real, slot_tokens,
-    slot_rows, lru) until that kernel completes."""
+    slot_rows, lru) until that kernel completes.
+
+    ``miss_src`` (int64) / ``miss_dst`` (int32) [B, >=K] receive the row's miss
+    plan (pool row and hot row of each miss, in order, the first miss_count[b]
+    entries) and ``miss_mask`` (int32 [B, >=K]) marks the entries that missed;
+    ``gather_misses`` replays the plan onto another layer."""
     H = int(hot_size if hot_size is not None else lru.shape[1])
     _need(topk_ids, torch.int32, "topk_ids", 2)
     _need(out_rows, torch.int32, "out_rows", 2)
@@ -102,6 +108,17 @@ def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, 
         _need(miss_count, torch.int32, "miss_count", 1)
     if status is not None:
         _need(status, torch.int32, "status", 1)
+    if (miss_src is None) != (miss_dst is None):
+        raise ValueError("miss_src and miss_dst go together")
+    if miss_src is not None:
+        _need(miss_src, torch.int64, "miss_src", 2)
+        _need(miss_dst, torch.int32, "miss_dst", 2)
+        if miss_src.stride(0) != miss_dst.stride(0):
+            raise ValueError("miss_src and miss_dst need the same row stride")
+        if miss_count is None:
+            raise ValueError("the miss plan needs miss_count")
+    if miss_mask is not None:
+        _need(miss_mask, torch.int32, "miss_mask", 2)
     if stats is not None:
         if stats.dtype not in (torch.int64, getattr(torch, "uint64", torch.int64)) or \
                 stats.numel() < 2:
@@ -141,10 +158,18 @@ def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, 
         pool_k=pk_ptr, pool_v=pv_ptr, pool_num_rows=p_rows,
         hot_k=hk_ptr, hot_v=hv_ptr, hot_num_rows=h_rows,
         row_bytes=row_bytes, out_rows=_ptr(out_rows), out_stride=out_rows.stride(0),
-        miss_count=_ptr(miss_count), stats=_ptr(stats), status=_ptr(status))
+        miss_count=_ptr(miss_count), stats=_ptr(stats), status=_ptr(status),
+        miss_src=_ptr(miss_src), miss_dst=_ptr(miss_dst),
+        plan_stride=miss_src.stride(0) if miss_src is not None else 0,
+        miss_mask=_ptr(miss_mask),
+        mask_stride=miss_mask.stride(0) if miss_mask is not None else 0)
+    for t, name in ((miss_src, "miss_src"), (miss_dst, "miss_dst"), (miss_mask, "miss_mask")):
+        if t is not None and (t.shape[0] < B or t.shape[1] < K):
+            raise ValueError(f"{name} must be at least [batch, top_k]")
     # the struct holds raw pointers: keep the tensors alive as long as it lives
     args.tensors = (topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_rows,
-                    pool_k, pool_v, hot_k, hot_v, out_rows, num_real, miss_count, stats, status)
+                    pool_k, pool_v, hot_k, hot_v, out_rows, num_real, miss_count, stats, status,
+                    miss_src, miss_dst, miss_mask)
     return args
 
 
@@ -156,6 +181,42 @@ def swap_in_args(args: SwapInArgs, stream=None) -> None:
 def swap_in(*, stream=None, **tensors) -> None:
     """One swap-in call; keyword tensors as in ``make_swap_in_args``."""
     swap_in_args(make_swap_in_args(**tensors), stream)
+
+
+def gather_misses(pool_layers, hot_layers, miss_src, miss_dst, miss_count, *, has_v=False,
+                  status=None, stream=None, ptrs=None) -> None:
+    """Replay a swap-in's miss plan onto layers that share its indices: in every
+    layer, hot row miss_dst[b][m] = pool row miss_src[b][m] for m < miss_count[b].
+    ``pool_layers`` / ``hot_layers`` are lists of per-layer tensors [rows, ...]
+    (K layers, then V layers when has_v); ``ptrs`` may pass prebuilt pointer
+    arrays (pool_ptrs, hot_ptrs) from ``layer_pointer_array``; pass them when
+    capturing a CUDA graph (building them copies to the device)."""
+    _need(miss_src, torch.int64, "miss_src", 2)
+    _need(miss_dst, torch.int32, "miss_dst", 2)
+    _need(miss_count, torch.int32, "miss_count", 1)
+    if miss_src.stride(0) != miss_dst.stride(0) or miss_src.shape != miss_dst.shape:
+        raise ValueError("miss_src and miss_dst need the same shape and row stride")
+    if len(pool_layers) != len(hot_layers) or not pool_layers:
+        raise ValueError("need matching non-empty layer lists")
+    if has_v and len(pool_layers) % 2:
+        raise ValueError("with has_v the lists hold K layers then V layers")
+    B, K = miss_src.shape
+    if miss_count.numel() < B:
+        raise ValueError("miss_count needs one entry per batch row")
+    geo_p = {_byte_rows(t, "pool")[2:] for t in pool_layers}
+    geo_h = {_byte_rows(t, "hot")[2:] for t in hot_layers}
+    if len(geo_p) != 1 or len(geo_h) != 1 or geo_p != geo_h or len({*geo_p.pop()}) != 1:
+        raise ValueError("every pool and hot layer needs contiguous rows of one byte width")
+    rb = _byte_rows(pool_layers[0], "pool")[2]
+    if ptrs is None:
+        dev = miss_src.device
+        ptrs = (layer_pointer_array(pool_layers, dev), layer_pointer_array(hot_layers, dev))
+    nl = len(pool_layers) // (2 if has_v else 1)
+    _capi.check(_lib().hs_gather_misses(
+        _ptr(ptrs[0]), _ptr(ptrs[1]), nl, int(bool(has_v)),
+        min(t.shape[0] for t in pool_layers), min(t.shape[0] for t in hot_layers), rb,
+        _ptr(miss_src), _ptr(miss_dst), miss_src.stride(0), _ptr(miss_count), B, K,
+        _ptr(status), C.c_void_p(_stream(stream))), "hs_gather_misses")
 
 
 def store_kv(k_src, v_src, k_dst, v_dst, loc, status=None, stream=None) -> None:

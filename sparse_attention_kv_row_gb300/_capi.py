@@ -23,11 +23,11 @@ ST_BAD_INDEX = 64
 SEQ_LENS_I64 = 1
 REQ_STATE_I64 = 2
 OVERLAP_PREV = 4
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 # Every symbol include/hisparse.h declares.
 EXPORTS = ("hs_swap_in", "hs_swap_in_smem_bytes", "hs_store_kv", "hs_transfer_kv",
-           "hs_probe_read", "hs_err_string", "hs_status_string", "hs_last_error",
+           "hs_gather_misses", "hs_probe_read", "hs_err_string", "hs_status_string", "hs_last_error",
            "hs_abi_version")
 
 
@@ -49,6 +49,8 @@ class SwapInArgs(C.Structure):
         ("row_bytes", C.c_int64),
         ("out_rows", C.c_void_p), ("out_stride", C.c_int64),
         ("miss_count", C.c_void_p), ("stats", C.c_void_p), ("status", C.c_void_p),
+        ("miss_src", C.c_void_p), ("miss_dst", C.c_void_p), ("plan_stride", C.c_int64),
+        ("miss_mask", C.c_void_p), ("mask_stride", C.c_int64),
     ]
 
 
@@ -86,6 +88,9 @@ def load() -> C.CDLL:
         lib.hs_transfer_kv.argtypes = [vp, vp, i32, i32, vp, vp, i64, i64, i64, i64, i64, i64,
                                        vp, vp]
         lib.hs_transfer_kv.restype = C.c_int
+        lib.hs_gather_misses.argtypes = [vp, vp, i32, i32, i64, i64, i64, vp, vp, i64, vp, i32,
+                                         i32, vp, vp]
+        lib.hs_gather_misses.restype = C.c_int
         lib.hs_probe_read.argtypes = [vp, i64, vp, vp]
         lib.hs_probe_read.restype = C.c_int
         lib.hs_err_string.argtypes = [i32]

@@ -3,6 +3,9 @@
 //
 //  store_kv   tokenspeed tokenspeed_kernel/ops/kvcache/triton.py, store_kv_cache:
 //             k_dst[loc[t]] = k_src[t], v_dst[loc[t]] = v_src[t].
+//  gather     vLLM csrc/libtorch_stable/hisparse_kernels.cu, hisparse_gather_plan_kernel /
+//             hisparse_gather_compact_kernel: a resolving layer's miss plan replayed
+//             onto a layer that shares its indices.
 //  transfer   tokenspeed ... transfer_kv_per_layer(_mla) / transfer_kv_all_layer(_mla)
 //             and SGLang jit_kernel/csrc/hisparse.cuh, transfer_cache_dsv4_mla_kernel:
 //             for each index pair, the same row of every layer's cache.
@@ -27,7 +30,9 @@ constexpr int kMoverBlocksPerSm = 8;
 constexpr int kUnroll = 4;
 
 // Copies `bytes` bytes from src to dst with one warp, choosing the widest chunk
-// that all three of (src, dst, bytes) allow.
+// that all three of (src, dst, bytes) allow.  Stores are evict-first, or kept
+// in L2 (kKeepL2) for rows an attention kernel reads next.
+template <bool kKeepL2 = false>
 __device__ __forceinline__ void warp_copy_row(unsigned char* dst, const unsigned char* src,
                                               int64_t bytes, int lane) {
   const uintptr_t al = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) |
@@ -44,7 +49,12 @@ __device__ __forceinline__ void warp_copy_row(unsigned char* dst, const unsigned
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int64_t c = c0 + u * kWarp;
-        if (c < n) st_stream_v4(dst + (c << 4), v[u]);
+        if (c < n) {
+          if (kKeepL2)
+            st_l2_v4(dst + (c << 4), v[u]);
+          else
+            st_stream_v4(dst + (c << 4), v[u]);
+        }
       }
     }
   } else if ((al & 3) == 0) {
@@ -59,7 +69,12 @@ __device__ __forceinline__ void warp_copy_row(unsigned char* dst, const unsigned
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int64_t c = c0 + u * kWarp;
-        if (c < n) st_stream_u32(dst + (c << 2), v[u]);
+        if (c < n) {
+          if (kKeepL2)
+            st_l2_u32(dst + (c << 2), v[u]);
+          else
+            st_stream_u32(dst + (c << 2), v[u]);
+        }
       }
     }
   } else {
@@ -73,7 +88,12 @@ __device__ __forceinline__ void warp_copy_row(unsigned char* dst, const unsigned
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int64_t c = c0 + u * kWarp;
-        if (c < bytes) st_stream_u8(dst + c, v[u]);
+        if (c < bytes) {
+          if (kKeepL2)
+            st_l2_u8(dst + c, v[u]);
+          else
+            st_stream_u8(dst + c, v[u]);
+        }
       }
     }
   }
@@ -144,6 +164,48 @@ __global__ void __launch_bounds__(kMoverThreads) transfer_kernel(const TransferP
     unsigned char* dst =
         reinterpret_cast<unsigned char*>(__ldg(p.dst_ptrs + layer)) + d * p.dst_stride;
     warp_copy_row(dst, src, p.row_bytes, lane);
+  }
+}
+
+struct GatherParams {
+  const uint64_t* pool_ptrs;
+  const uint64_t* hot_ptrs;
+  uint32_t ptr_pairs;  // num_layers * (1 + has_v)
+  int64_t pool_rows, hot_rows, row_bytes;
+  const int64_t* miss_src;
+  const int32_t* miss_dst;
+  int64_t plan_stride;
+  const int32_t* miss_count;
+  int32_t top_k;
+  int32_t* status;
+};
+
+// Block (row, y): warp w takes units u = y*W + w, y*W + w + gridDim.y*W, ...
+// with u = miss * ptr_pairs + pointer pair, below the row's miss count.
+__global__ void __launch_bounds__(kMoverThreads) gather_misses_kernel(const GatherParams p) {
+  constexpr int W = kMoverThreads / kWarp;
+  // The next launch may start now: it reads nothing this kernel writes before
+  // its own grid-dependency wait.
+  grid_dep_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t row = blockIdx.x;
+  int n = __ldg(p.miss_count + row);
+  n = n < 0 ? 0 : (n > p.top_k ? p.top_k : n);
+  const uint32_t units = static_cast<uint32_t>(n) * p.ptr_pairs;
+  for (uint32_t u = blockIdx.y * W + (threadIdx.x >> 5); u < units; u += gridDim.y * W) {
+    const uint32_t m = u / p.ptr_pairs;
+    const uint32_t pp = u - m * p.ptr_pairs;
+    const int32_t d = __ldg(p.miss_dst + row * p.plan_stride + m);
+    if (d < 0) continue;  // this miss was given no hot row
+    const int64_t s = __ldg(p.miss_src + row * p.plan_stride + m);
+    if (s < 0 || s >= p.pool_rows || d >= p.hot_rows) {
+      if (lane == 0 && pp == 0 && p.status) atomicOr(p.status, HS_ST_BAD_INDEX);
+      continue;
+    }
+    const unsigned char* src = reinterpret_cast<const unsigned char*>(__ldg(p.pool_ptrs + pp));
+    unsigned char* dst = reinterpret_cast<unsigned char*>(__ldg(p.hot_ptrs + pp));
+    warp_copy_row<true>(dst + static_cast<int64_t>(d) * p.row_bytes, src + s * p.row_bytes,
+                        p.row_bytes, lane);
   }
 }
 
@@ -281,5 +343,58 @@ extern "C" hs_err hs_probe_read(const void* src, int64_t bytes, unsigned long lo
       static_cast<const uint4*>(src), bytes >> 4, sink);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(HS_ERR_CUDA, "hs_probe_read launch: %s", cudaGetErrorString(e));
+  return HS_OK;
+}
+
+extern "C" hs_err hs_gather_misses(const uint64_t* pool_ptrs, const uint64_t* hot_ptrs,
+                                   int32_t num_layers, int32_t has_v, int64_t pool_num_rows,
+                                   int64_t hot_num_rows, int64_t row_bytes,
+                                   const int64_t* miss_src, const int32_t* miss_dst,
+                                   int64_t plan_stride, const int32_t* miss_count, int32_t batch,
+                                   int32_t top_k, int32_t* status, hs_stream_t stream) {
+  using namespace hs;
+  clear_error();
+  if (batch < 0 || top_k < 0 || num_layers < 0 || row_bytes < 1 || pool_num_rows < 0 ||
+      hot_num_rows < 0)
+    return fail(HS_ERR_ARG, "hs_gather_misses: negative size or row_bytes < 1");
+  if (has_v != 0 && has_v != 1) return fail(HS_ERR_ARG, "hs_gather_misses: has_v must be 0 or 1");
+  if (batch == 0 || top_k == 0 || num_layers == 0) return HS_OK;
+  if (pool_ptrs == nullptr || hot_ptrs == nullptr || miss_src == nullptr ||
+      miss_dst == nullptr || miss_count == nullptr)
+    return fail(HS_ERR_ARG, "hs_gather_misses: pointer arrays and the plan arrays are required");
+  if (plan_stride < top_k) return fail(HS_ERR_ARG, "hs_gather_misses: plan_stride < top_k");
+  const uint64_t pairs = static_cast<uint64_t>(num_layers) * (has_v ? 2u : 1u);
+  if (pairs * static_cast<uint64_t>(top_k) >= (1ull << 32))
+    return fail(HS_ERR_UNSUPPORTED, "hs_gather_misses: top_k * layers must be < 2^32");
+  DeviceInfo dev;
+  hs_err err = current_device(&dev);
+  if (err != HS_OK) return err;
+  GatherParams p;
+  p.pool_ptrs = pool_ptrs;
+  p.hot_ptrs = hot_ptrs;
+  p.ptr_pairs = static_cast<uint32_t>(pairs);
+  p.pool_rows = pool_num_rows;
+  p.hot_rows = hot_num_rows;
+  p.row_bytes = row_bytes;
+  p.miss_src = miss_src;
+  p.miss_dst = miss_dst;
+  p.plan_stride = plan_stride;
+  p.miss_count = miss_count;
+  p.top_k = top_k;
+  p.status = status;
+  // Enough blocks per row to cover the device even for a few rows, at most
+  // one warp per (miss, layer) unit.
+  constexpr int W = kMoverThreads / kWarp;
+  const int64_t units = static_cast<int64_t>(top_k) * static_cast<int64_t>(pairs);
+  int64_t y = static_cast<int64_t>(dev.sm_count) * kMoverBlocksPerSm / batch;
+  const int64_t y_max = (units + W - 1) / W;
+  if (y > y_max) y = y_max;
+  if (y < 1) y = 1;
+  if (y > 65535) y = 65535;
+  gather_misses_kernel<<<dim3(static_cast<unsigned>(batch), static_cast<unsigned>(y)),
+                         kMoverThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return fail(HS_ERR_CUDA, "hs_gather_misses launch: %s", cudaGetErrorString(e));
   return HS_OK;
 }

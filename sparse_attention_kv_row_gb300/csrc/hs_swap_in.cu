@@ -146,6 +146,11 @@ struct SwapInParams {
   int32_t* miss_count;
   unsigned long long* stats;
   int32_t* status;
+  int64_t* miss_src;  // optional miss plan
+  int32_t* miss_dst;
+  int64_t plan_stride;
+  int32_t* miss_mask;
+  int64_t mask_stride;
   uint32_t chunks_per_row;  // row_bytes / copy width
   FastDiv div_chunks;
   Layout lay;               // shared-memory layout, computed once on the host
@@ -300,7 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   if (pad_nr || r < 0 || r >= p.num_states) {  // padding row / bad state row
     grid_dep_wait();
     if (!overlap && tid == 0) mbar_wait(bar, 0, kMaxPolls);  // no copy left in flight
-    for (int i = e0 + tid; i < e1; i += kThreads) out_g[i] = -1;
+    for (int i = e0 + tid; i < e1; i += kThreads) {
+      out_g[i] = -1;
+      if (p.miss_mask) p.miss_mask[b * p.mask_stride + i] = 0;
+    }
     if (j == 0 && tid == 0) {
       if (p.miss_count) p.miss_count[b] = 0;
       if (p.status) p.status[b] = (pad_nr || r < 0) ? 0 : HS_ST_BAD_STATE;
@@ -325,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     for (int i = e0 + tid; i < e1; i += kThreads) {
       const int32_t t = ids[i];
       out_g[i] = (i < count && t >= 0 && t < Lb) ? __ldg(rows_g + t) : -1;
+      if (p.miss_mask) p.miss_mask[b * p.mask_stride + i] = 0;
     }
     if (j == 0 && tid == 0) {
       if (p.miss_count) p.miss_count[b] = 0;
@@ -639,7 +648,10 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     const bool mine = i < e1;
     const int8_t c = mine ? code[i] : kInvalid;
     const unsigned m = __ballot_sync(kFullMask, c == kMiss);
-    if (mine) my_pr = c == kMiss ? jsrc[i - e0] : 0;
+    if (mine) {
+      my_pr = c == kMiss ? jsrc[i - e0] : 0;
+      if (p.miss_mask) p.miss_mask[b * p.mask_stride + i] = c == kMiss;
+    }
     __syncthreads();  // jsrc is rewritten in compacted order below
     if (c == kMiss) {
       const int mm = cnte[i >> 5] + __popc(m & lanes_before);  // the row's mm-th miss
@@ -656,6 +668,10 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       out_g[i] = d;
       jsrc[mm - my_first_miss] = my_pr;
       jdst[mm - my_first_miss] = d;
+      if (p.miss_src) {
+        p.miss_src[b * p.plan_stride + mm] = my_pr;
+        p.miss_dst[b * p.plan_stride + mm] = d;
+      }
     } else if (mine) {
       int32_t o = -1;
       if (c == kNewest) o = rows[H];  // the newest token lives in slot H
@@ -796,6 +812,12 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   if (a->slot_tokens_stride < H + 1 || a->slot_rows_stride < H + 1)
     return fail(HS_ERR_ARG, "hs_swap_in: slot strides must be >= hot_size + 1");
   if (a->lru_stride < H) return fail(HS_ERR_ARG, "hs_swap_in: lru_stride must be >= hot_size");
+  if ((a->miss_src == nullptr) != (a->miss_dst == nullptr))
+    return fail(HS_ERR_ARG, "hs_swap_in: miss_src and miss_dst must both be set or both be NULL");
+  if (a->miss_src != nullptr && (a->miss_count == nullptr || a->plan_stride < K))
+    return fail(HS_ERR_ARG, "hs_swap_in: the miss plan needs miss_count and plan_stride >= top_k");
+  if (a->miss_mask != nullptr && a->mask_stride < K)
+    return fail(HS_ERR_ARG, "hs_swap_in: mask_stride must be >= top_k");
   if (a->pool_rows_cols < 0 || a->pool_rows_stride < a->pool_rows_cols)
     return fail(HS_ERR_ARG, "hs_swap_in: need 0 <= pool_rows_cols <= pool_rows_stride");
   if (a->num_states < 1 || a->pool_num_rows < 0 || a->hot_num_rows < 0)
@@ -878,6 +900,11 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   p.miss_count = a->miss_count;
   p.stats = a->stats;
   p.status = a->status;
+  p.miss_src = a->miss_src;
+  p.miss_dst = a->miss_dst;
+  p.plan_stride = a->plan_stride;
+  p.miss_mask = a->miss_mask;
+  p.mask_stride = a->mask_stride;
   p.chunks_per_row = static_cast<uint32_t>(cpr);
   p.div_chunks = FastDiv{fastdiv_magic(static_cast<uint32_t>(cpr)), static_cast<uint32_t>(cpr)};
   p.lay = L;

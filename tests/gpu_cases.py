@@ -35,7 +35,7 @@ class GpuCase:
         self.seq_dtype, self.req_dtype = seq_dtype, req_dtype
         self.num_real_on_device = num_real_on_device
 
-    def step(self, topk: np.ndarray, stream=None):
+    def step(self, topk: np.ndarray, stream=None, plan=False):
         c = self.case
         B, K = topk.shape
         dev = self.dev
@@ -43,6 +43,11 @@ class GpuCase:
         miss = torch.full((B,), 777, dtype=torch.int32, device=dev)
         status = torch.full((B,), 999, dtype=torch.int32, device=dev)
         stats = torch.zeros(2, dtype=torch.int64, device=dev)
+        kw = {}
+        if plan:
+            kw = dict(miss_src=torch.full((B, K), cases.PLAN_FILL_SRC, dtype=torch.int64, device=dev),
+                      miss_dst=torch.full((B, K), cases.PLAN_FILL_DST, dtype=torch.int32, device=dev),
+                      miss_mask=torch.full((B, K), 7, dtype=torch.int32, device=dev))
         num_real = None
         if c.num_real >= 0:
             num_real = torch.tensor([c.num_real], dtype=torch.int32, device=dev)
@@ -53,10 +58,13 @@ class GpuCase:
                    pool_rows=self.pool_rows, pool_k=self.pool_k, pool_v=self.pool_v,
                    hot_k=self.hot_k, hot_v=self.hot_v, out_rows=out, hot_size=c.H,
                    num_real=num_real, miss_count=miss, stats=stats, status=status,
-                   stream=stream)
+                   stream=stream, **kw)
         torch.cuda.synchronize()
-        return (out.cpu().numpy(), miss.cpu().numpy(), status.cpu().numpy(),
-                stats.cpu().numpy().astype(np.uint64))
+        res = (out.cpu().numpy(), miss.cpu().numpy(), status.cpu().numpy(),
+               stats.cpu().numpy().astype(np.uint64))
+        if plan:
+            res += tuple(kw[k].cpu().numpy() for k in ("miss_src", "miss_dst", "miss_mask"))
+        return res
 
     def assert_matches(self, ref: cases.Case, what=""):
         np.testing.assert_array_equal(self.tokens.cpu().numpy(), ref.tokens,
@@ -76,11 +84,12 @@ class GpuCase:
         self.pool_rows.copy_(torch.from_numpy(ref.pool_rows))
 
 
-def step_both(g: GpuCase, ref: cases.Case, topk: np.ndarray, what=""):
+def step_both(g: GpuCase, ref: cases.Case, topk: np.ndarray, what="", plan=False):
     ref.topk = topk
-    r = cases.run_oracle(ref)
-    o = g.step(topk)
-    for name, x, y in zip(("out", "miss_count", "status", "stats"), o, r):
+    r = cases.run_oracle(ref, plan=plan)
+    o = g.step(topk, plan=plan)
+    names = ("out", "miss_count", "status", "stats", "miss_src", "miss_dst", "miss_mask")
+    for name, x, y in zip(names, o, r):
         np.testing.assert_array_equal(x, y, err_msg=f"{name} {what}")
     g.assert_matches(ref, what)
     return o

@@ -87,6 +87,35 @@ def test_empty_work_is_ok_without_gpu(lib):
     assert lib.hs_transfer_kv(None, None, 3, 0, None, None, 0, 16, 16, 1, 1, 16, None, None) == 0
 
 
+def test_plan_arguments_rejected(lib):
+    """The miss-plan arguments are checked before any device call."""
+    a = _args()
+    for k in ("topk_ids", "seq_lens", "req_state", "slot_tokens", "slot_rows", "lru",
+              "pool_rows", "pool_k", "hot_k", "out_rows"):
+        setattr(a, k, 256)  # never dereferenced: the checks below fail first
+    a.miss_src = 512
+    assert lib.hs_swap_in(C.byref(a), None) == 1   # miss_src without miss_dst
+    assert b"miss_dst" in lib.hs_last_error()
+    a.miss_dst = 768
+    assert lib.hs_swap_in(C.byref(a), None) == 1   # plan without miss_count
+    a.miss_count, a.plan_stride = 1024, 2
+    assert lib.hs_swap_in(C.byref(a), None) == 1   # plan_stride < top_k
+    a.miss_src = a.miss_dst = None
+    a.miss_mask, a.mask_stride = 512, 3
+    assert lib.hs_swap_in(C.byref(a), None) == 1   # mask_stride < top_k
+    assert b"mask_stride" in lib.hs_last_error()
+
+
+def test_gather_rejects(lib):
+    g = lib.hs_gather_misses
+    assert g(None, None, 3, 0, 10, 10, 16, None, None, 4, None, 0, 4, None, None) == 0  # no rows
+    assert g(None, None, 0, 0, 10, 10, 16, None, None, 4, None, 2, 4, None, None) == 0  # no layers
+    assert g(None, None, 3, 0, 10, 10, 16, None, None, 4, None, 2, 4, None, None) == 1  # NULLs
+    assert g(8, 8, 3, 0, 10, 10, 16, 8, 8, 2, 8, 2, 4, None, None) == 1  # plan_stride < top_k
+    assert g(8, 8, 3, 2, 10, 10, 16, 8, 8, 4, 8, 2, 4, None, None) == 1  # has_v not 0/1
+    assert g(8, 8, 3, 0, 10, 10, 0, 8, 8, 4, 8, 2, 4, None, None) == 1  # row_bytes < 1
+
+
 def test_movers_reject(lib):
     assert lib.hs_store_kv(None, None, 16, 16, None, None, 16, 10, None, 5, 16, None, None) == 1
     assert lib.hs_store_kv(1, None, 8, 0, 1, None, 16, 10, 1, 5, 16, None, None) == 1  # stride

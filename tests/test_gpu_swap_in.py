@@ -70,7 +70,7 @@ def test_random_tiny_with_corruption(dev, seed):
         if step >= 3:
             cases.corrupt(np.random.default_rng(seed * 7 + step), ref)
             g.push_state(ref)
-        step_both(g, ref, ids, f"seed={seed} step={step}")
+        step_both(g, ref, ids, f"seed={seed} step={step}", plan=seed % 2 == 0)
 
 
 @pytest.mark.parametrize("H,K,S,B,with_v,host", [
@@ -90,9 +90,9 @@ def test_multi_tile_workloads(dev, H, K, S, B, with_v, host):
     import synth
     ts = synth.TopkStream(H, 0, B, K, L, 0.6)
     for step in range(5):
-        step_both(g, ref, ts.next(), f"H={H} step={step}")
+        step_both(g, ref, ts.next(), f"H={H} step={step}", plan=True)
     # a step with invalid, duplicate and newest ids mixed in
-    step_both(g, ref, cases.random_ids(rng, ref), "mixed")
+    step_both(g, ref, cases.random_ids(rng, ref), "mixed", plan=True)
 
 
 def test_all_rows_padding_and_empty(dev):
