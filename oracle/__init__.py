@@ -76,6 +76,15 @@ def load(mutant: int = 0) -> C.CDLL:
                                           C.c_void_p, C.c_int64, C.c_void_p, C.c_int32,
                                           C.c_int32, C.c_void_p]
         lib.hso_gather_misses.restype = C.c_int
+        lib.hso_e4m3_encode_array.argtypes = [C.c_void_p, C.c_void_p, C.c_int64]
+        lib.hso_e4m3_encode_array.restype = None
+        lib.hso_fp8_store_kv.argtypes = [C.c_void_p, C.c_void_p, C.c_int32, C.c_int64,
+                                         C.c_int64, C.c_int64, C.c_int64, C.c_void_p,
+                                         C.c_void_p, C.c_int64, C.c_int64, C.c_int64,
+                                         C.c_int32, C.c_int64, C.c_void_p, C.c_int64,
+                                         C.c_int32, C.c_int32, C.c_void_p, C.c_void_p,
+                                         C.c_void_p]
+        lib.hso_fp8_store_kv.restype = C.c_int
         _LIBS[mutant] = lib
     return _LIBS[mutant]
 
@@ -178,6 +187,62 @@ def gather_misses(*, pool_k, hot_k, miss_src, miss_dst, miss_count, pool_v=None,
         _ptr(miss_count), B, K, _ptr(status))
     if rc != 0:
         raise ValueError("oracle gather_misses rejected its arguments")
+
+
+_IN_DTYPES = {np.dtype(np.float32): 0, np.dtype(np.float16): 1}
+IN_BF16 = 2  # bf16 inputs are passed as uint16 arrays of their bits
+
+
+def e4m3_encode(x, mutant: int = 0) -> np.ndarray:
+    """FP8 E4M3 codes (uint8) of float32 values: round to nearest even,
+    saturating to +-448, NaN -> 0x7F with the input's sign."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    load(mutant).hso_e4m3_encode_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def fp8_store_kv(*, k, v, k_cache, v_cache, loc, page_size, inv_k_scale=None,
+                 inv_v_scale=None, bf16=False, status=None, mutant: int = 0) -> None:
+    """Quantise k/v [T, heads, dim] to FP8 E4M3 and scatter token t to slot loc[t] of
+    the paged caches (uint8 [pages, page_size, heads, dim] or [slots, heads, dim]).
+    ``bf16``: k and v are uint16 arrays holding bfloat16 bits.  inv_*_scale are
+    float32 scalars (None: no scaling)."""
+    if bf16:
+        _check(k, np.uint16, "k", 3)
+        dt = IN_BF16
+    else:
+        dt = _IN_DTYPES[k.dtype]
+    if v is not None and v.dtype != k.dtype:
+        raise TypeError("k and v must have the same dtype")
+    for n, a in (("k_cache", k_cache), ("v_cache", v_cache)):
+        _check(a, np.uint8, n)
+    _check(loc, np.int64, "loc", 1)
+    T, Hh, D = k.shape
+    for a in (k, v):
+        if a is not None and (a.strides[2] != a.itemsize or a.shape != k.shape):
+            raise ValueError("k/v need shape [T, heads, dim] with contiguous dims")
+    cs = k_cache.strides
+    if k_cache.ndim == 4:
+        c_page, c_off, c_head = cs[0], cs[1], cs[2]
+        num_slots = k_cache.shape[0] * k_cache.shape[1]
+        if k_cache.shape[1] != page_size:
+            raise ValueError("page_size mismatch")
+    else:
+        c_page, c_off, c_head = cs[0] * page_size, cs[0], cs[1]
+        num_slots = k_cache.shape[0] // page_size * page_size
+    if v_cache is not None and v_cache.strides != k_cache.strides:
+        raise ValueError("k_cache and v_cache need the same layout")
+    ik = np.array([inv_k_scale], np.float32) if inv_k_scale is not None else None
+    iv = np.array([inv_v_scale], np.float32) if inv_v_scale is not None else None
+    it = k.itemsize
+    rc = load(mutant).hso_fp8_store_kv(
+        _ptr(k), _ptr(v), dt, k.strides[0] // it, k.strides[1] // it,
+        v.strides[0] // it if v is not None else 0, v.strides[1] // it if v is not None else 0,
+        _ptr(k_cache), _ptr(v_cache), c_page, c_off, c_head, page_size, num_slots, _ptr(loc), T,
+        Hh, D, _ptr(ik), _ptr(iv), _ptr(status))
+    if rc != 0:
+        raise ValueError("oracle fp8_store_kv rejected its arguments")
 
 
 def store_kv(*, k_src, v_src, k_dst, v_dst, loc, status=None) -> None:

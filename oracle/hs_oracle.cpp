@@ -21,6 +21,11 @@
  *    and hisparse_gather_compact_kernel: a resolving layer's miss plan (which
  *    entries missed, which pool row went to which hot row) replayed onto a
  *    layer that shares its indices, with no LRU resolution.
+ *  - tokenspeed tokenspeed_kernel/ops/kvcache/triton.py, fused_fp8_set_kv_buffer:
+ *    K/V rows optionally multiplied by an inverse scale in fp32, converted to
+ *    FP8 E4M3 and scattered into a paged cache (the encoding is written here
+ *    from the format's definition: sign, 4 exponent bits with bias 7, 3
+ *    mantissa bits, subnormals at exponent 0, S.1111.111 = NaN).
  *  - tokenspeed tokenspeed_kernel/ops/kvcache/triton.py, store_kv_cache and
  *    transfer_kv_per_layer / transfer_kv_all_layer(_mla): indexed row scatter
  *    and gather over per-layer pointer arrays.
@@ -46,6 +51,7 @@
  */
 #include "hs_oracle.h"
 
+#include <cmath>
 #include <cstring>
 #include <unordered_map>
 #include <unordered_set>
@@ -329,6 +335,109 @@ extern "C" int hso_transfer_kv(const uint64_t* src_ptrs, const uint64_t* dst_ptr
       const uint8_t* src = reinterpret_cast<const uint8_t*>(src_ptrs[p]);
       uint8_t* dst = reinterpret_cast<uint8_t*>(dst_ptrs[p]);
       std::memcpy(dst + d * dst_stride, src + s * src_stride, (size_t)row_bytes);
+    }
+  }
+  return 0;
+}
+
+namespace {
+
+// Round half to even of a non-negative double.
+double round_half_even(double q) {
+  const double fl = std::floor(q);
+  const double r = q - fl;
+  if (r > 0.5) return fl + 1.0;
+  if (r < 0.5) return fl;
+#if HSO_MUTANT == 13
+  return fl + 1.0;  // planted: ties away from zero
+#else
+  return std::fmod(fl, 2.0) == 0.0 ? fl : fl + 1.0;
+#endif
+}
+
+float decode_input(const void* base, int64_t idx, int32_t dtype) {
+  if (dtype == HSO_IN_F32) {
+    return static_cast<const float*>(base)[idx];
+  }
+  const uint16_t h = static_cast<const uint16_t*>(base)[idx];
+  if (dtype == HSO_IN_BF16) {  // the upper half of an IEEE binary32
+    const uint32_t bits = static_cast<uint32_t>(h) << 16;
+    float f;
+    std::memcpy(&f, &bits, 4);
+    return f;
+  }
+  // IEEE binary16: 1 sign, 5 exponent (bias 15), 10 mantissa bits
+  const int sign = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+  double v;
+  if (e == 0)
+    v = std::ldexp(static_cast<double>(m), -24);
+  else if (e == 31)
+    v = m ? NAN : INFINITY;
+  else
+    v = std::ldexp(1.0 + m / 1024.0, e - 15);
+  return static_cast<float>(sign ? -v : v);
+}
+
+}  // namespace
+
+extern "C" uint8_t hso_e4m3_from_float(float x) {
+  const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+  if (std::isnan(x)) return sign | 0x7F;
+  const double a = std::fabs(static_cast<double>(x));
+  if (a >= 448.0) return sign | 0x7E;  // saturate (finite overflow and infinities)
+  if (a < std::ldexp(1.0, -6)) {
+    // subnormal range: value = m * 2^-9, m in [0, 8]; m == 8 is the first normal
+    const double m = round_half_even(a * 512.0);
+    return sign | static_cast<uint8_t>(m);
+  }
+  int e2;
+  const double fr = std::frexp(a, &e2);  // a = fr * 2^e2, fr in [0.5, 1)
+  int e = e2 - 1;                        // a = (2 fr) * 2^e, 2 fr in [1, 2)
+  double m = round_half_even((2.0 * fr - 1.0) * 8.0);
+  if (m == 8.0) {
+    m = 0.0;
+    ++e;
+  }
+  return sign | static_cast<uint8_t>(((e + 7) << 3) | static_cast<int>(m));
+}
+
+extern "C" void hso_e4m3_encode_array(const float* x, uint8_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = hso_e4m3_from_float(x[i]);
+}
+
+extern "C" int hso_fp8_store_kv(const void* k, const void* v, int32_t in_dtype,
+                                int64_t k_stride_token, int64_t k_stride_head,
+                                int64_t v_stride_token, int64_t v_stride_head, uint8_t* k_cache,
+                                uint8_t* v_cache, int64_t c_page, int64_t c_off, int64_t c_head,
+                                int32_t page_size, int64_t num_slots, const int64_t* loc,
+                                int64_t n_tokens, int32_t num_heads, int32_t head_dim,
+                                const float* inv_k, const float* inv_v, int32_t* status) {
+  if (in_dtype < HSO_IN_F32 || in_dtype > HSO_IN_BF16 || page_size < 1 || n_tokens < 0 ||
+      num_heads < 0 || head_dim < 0 || (v == nullptr) != (v_cache == nullptr))
+    return -1;
+  for (int64_t t = 0; t < n_tokens; ++t) {
+    const int64_t L = loc[t];
+    if (L < 0 || L >= num_slots) {
+      if (status) *status |= HSO_ST_BAD_INDEX;
+      continue;
+    }
+#if HSO_MUTANT == 14
+    const int64_t page = L % page_size, off = L / page_size;  // planted: swapped
+#else
+    const int64_t page = L / page_size, off = L % page_size;
+#endif
+    for (int kv = 0; kv < (v ? 2 : 1); ++kv) {
+      const void* in = kv ? v : k;
+      const int64_t st = kv ? v_stride_token : k_stride_token;
+      const int64_t sh = kv ? v_stride_head : k_stride_head;
+      uint8_t* cache = kv ? v_cache : k_cache;
+      const float* inv = kv ? inv_v : inv_k;
+      for (int32_t h = 0; h < num_heads; ++h)
+        for (int32_t d = 0; d < head_dim; ++d) {
+          const float x = decode_input(in, t * st + h * sh + d, in_dtype);
+          const float y = inv ? x * *inv : x;  // one fp32 multiply, rounded to fp32
+          cache[page * c_page + off * c_off + h * c_head + d] = hso_e4m3_from_float(y);
+        }
     }
   }
   return 0;

@@ -88,6 +88,33 @@ int hso_transfer_kv(const uint64_t* src_ptrs, const uint64_t* dst_ptrs, int32_t 
                     int64_t src_stride, int64_t dst_stride, int64_t src_rows, int64_t dst_rows,
                     int64_t row_bytes, int32_t* status);
 
+/* FP8 (E4M3, OCP "FN" variant: bias 7, no infinities, max finite 448, NaN =
+ * S.1111.111) encoding of a float: round to nearest, ties to even; finite
+ * overflow and infinities saturate to +-448; NaN gives 0x7F | sign << 7. */
+uint8_t hso_e4m3_from_float(float x);
+/* out[i] = hso_e4m3_from_float(x[i]) for i < n. */
+void hso_e4m3_encode_array(const float* x, uint8_t* out, int64_t n);
+
+/* Input element types of hso_fp8_store_kv. */
+#define HSO_IN_F32 0
+#define HSO_IN_F16 1
+#define HSO_IN_BF16 2
+
+/* Quantise K/V rows to FP8 E4M3 and scatter them into a paged cache (tokenspeed
+ * tokenspeed_kernel/ops/kvcache/triton.py, fused_fp8_set_kv_buffer):
+ * for token t with slot L = loc[t] (skipped with HSO_ST_BAD_INDEX when outside
+ * [0, num_slots)), page = L / page_size and offset = L % page_size; for every
+ * head h and dim d, y = x (no scale) or y = fp32(x * inv_scale) and
+ * cache[page*c_page + offset*c_off + h*c_head + d] = e4m3(y).  Input strides
+ * are in elements (dim stride 1), cache strides in bytes (dim stride 1).
+ * v / v_cache may be NULL (K only); inv_k / inv_v NULL means no scaling. */
+int hso_fp8_store_kv(const void* k, const void* v, int32_t in_dtype, int64_t k_stride_token,
+                     int64_t k_stride_head, int64_t v_stride_token, int64_t v_stride_head,
+                     uint8_t* k_cache, uint8_t* v_cache, int64_t c_page, int64_t c_off,
+                     int64_t c_head, int32_t page_size, int64_t num_slots, const int64_t* loc,
+                     int64_t n_tokens, int32_t num_heads, int32_t head_dim, const float* inv_k,
+                     const float* inv_v, int32_t* status);
+
 #ifdef __cplusplus
 }
 #endif
