@@ -202,12 +202,12 @@ def e4m3_encode(x, mutant: int = 0) -> np.ndarray:
     return out
 
 
-def fp8_store_kv(*, k, v, k_cache, v_cache, loc, page_size, inv_k_scale=None,
-                 inv_v_scale=None, bf16=False, status=None, mutant: int = 0) -> None:
+def fp8_store_kv(*, k, v, k_cache, v_cache, loc, page_size, k_scale=None, v_scale=None,
+                 bf16=False, status=None, mutant: int = 0) -> None:
     """Quantise k/v [T, heads, dim] to FP8 E4M3 and scatter token t to slot loc[t] of
     the paged caches (uint8 [pages, page_size, heads, dim] or [slots, heads, dim]).
-    ``bf16``: k and v are uint16 arrays holding bfloat16 bits.  inv_*_scale are
-    float32 scalars (None: no scaling)."""
+    ``bf16``: k and v are uint16 arrays holding bfloat16 bits.  k_scale / v_scale
+    are float32 scalars (None: no scaling); values are multiplied by fp32(1/scale)."""
     if bf16:
         _check(k, np.uint16, "k", 3)
         dt = IN_BF16
@@ -233,8 +233,8 @@ def fp8_store_kv(*, k, v, k_cache, v_cache, loc, page_size, inv_k_scale=None,
         num_slots = k_cache.shape[0] // page_size * page_size
     if v_cache is not None and v_cache.strides != k_cache.strides:
         raise ValueError("k_cache and v_cache need the same layout")
-    ik = np.array([inv_k_scale], np.float32) if inv_k_scale is not None else None
-    iv = np.array([inv_v_scale], np.float32) if inv_v_scale is not None else None
+    ik = np.array([k_scale], np.float32) if k_scale is not None else None
+    iv = np.array([v_scale], np.float32) if v_scale is not None else None
     it = k.itemsize
     rc = load(mutant).hso_fp8_store_kv(
         _ptr(k), _ptr(v), dt, k.strides[0] // it, k.strides[1] // it,

@@ -411,7 +411,12 @@ extern "C" int hso_fp8_store_kv(const void* k, const void* v, int32_t in_dtype,
                                 uint8_t* v_cache, int64_t c_page, int64_t c_off, int64_t c_head,
                                 int32_t page_size, int64_t num_slots, const int64_t* loc,
                                 int64_t n_tokens, int32_t num_heads, int32_t head_dim,
-                                const float* inv_k, const float* inv_v, int32_t* status) {
+                                const float* k_scale, const float* v_scale, int32_t* status) {
+  // the inverse scales, divided in fp32 like the pages' host code
+  const float inv_k_val = k_scale ? 1.0f / *k_scale : 1.0f;
+  const float inv_v_val = v_scale ? 1.0f / *v_scale : 1.0f;
+  const float* inv_k = k_scale ? &inv_k_val : nullptr;
+  const float* inv_v = v_scale ? &inv_v_val : nullptr;
   if (in_dtype < HSO_IN_F32 || in_dtype > HSO_IN_BF16 || page_size < 1 || n_tokens < 0 ||
       num_heads < 0 || head_dim < 0 || (v == nullptr) != (v_cache == nullptr))
     return -1;

@@ -105,15 +105,16 @@ void hso_e4m3_encode_array(const float* x, uint8_t* out, int64_t n);
  * for token t with slot L = loc[t] (skipped with HSO_ST_BAD_INDEX when outside
  * [0, num_slots)), page = L / page_size and offset = L % page_size; for every
  * head h and dim d, y = x (no scale) or y = fp32(x * inv_scale) and
- * cache[page*c_page + offset*c_off + h*c_head + d] = e4m3(y).  Input strides
- * are in elements (dim stride 1), cache strides in bytes (dim stride 1).
- * v / v_cache may be NULL (K only); inv_k / inv_v NULL means no scaling. */
+ * cache[page*c_page + offset*c_off + h*c_head + d] = e4m3(y), where
+ * inv_scale = fp32(1 / scale) as the pages' host code computes it.  Input
+ * strides are in elements (dim stride 1), cache strides in bytes (dim stride
+ * 1).  v / v_cache may be NULL (K only); k_scale / v_scale NULL: no scaling. */
 int hso_fp8_store_kv(const void* k, const void* v, int32_t in_dtype, int64_t k_stride_token,
                      int64_t k_stride_head, int64_t v_stride_token, int64_t v_stride_head,
                      uint8_t* k_cache, uint8_t* v_cache, int64_t c_page, int64_t c_off,
                      int64_t c_head, int32_t page_size, int64_t num_slots, const int64_t* loc,
-                     int64_t n_tokens, int32_t num_heads, int32_t head_dim, const float* inv_k,
-                     const float* inv_v, int32_t* status);
+                     int64_t n_tokens, int32_t num_heads, int32_t head_dim, const float* k_scale,
+                     const float* v_scale, int32_t* status);
 
 #ifdef __cplusplus
 }

@@ -131,13 +131,13 @@ def test_store_matches_index_assignment(dtype, paged, scaled):
     vc = rng.integers(0, 256, shape, dtype=np.uint8)
     loc = rng.choice(pages * ps, size=T, replace=False).astype(np.int64)
     loc[[4, 9]] = [pages * ps, -1]
-    ik, iv = (np.float32(1 / np.float32(0.7)), np.float32(1 / np.float32(2.5))) if scaled \
-        else (None, None)
-    ek = _expected_store(kx, ik, kc, loc, ps, paged)
-    ev = _expected_store(vx, iv, vc, loc, ps, paged)
+    ks, vs = (np.float32(0.7), np.float32(2.5)) if scaled else (None, None)
+    inv = (lambda sc: None if sc is None else np.float32(1) / sc)  # fp32 division
+    ek = _expected_store(kx, inv(ks), kc, loc, ps, paged)
+    ev = _expected_store(vx, inv(vs), vc, loc, ps, paged)
     st = np.zeros(1, np.int32)
     oracle.fp8_store_kv(k=k_in, v=v_in, k_cache=kc, v_cache=vc, loc=loc, page_size=ps,
-                        inv_k_scale=ik, inv_v_scale=iv, bf16=dtype == "bf16", status=st)
+                        k_scale=ks, v_scale=vs, bf16=dtype == "bf16", status=st)
     np.testing.assert_array_equal(kc, ek)
     np.testing.assert_array_equal(vc, ev)
     assert st[0] == oracle.ST_BAD_INDEX
