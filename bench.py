@@ -528,6 +528,39 @@ def run_store_kv(dev, hbm_peak, flush, stream):
                 l2="flushed (256 MiB write) before every launch")
 
 
+def run_fp8_store(dev, hbm_peak, flush, stream):
+    """FP8 KV write of the store_kv workload: bf16 K and V [4096, 8, 128] times
+    fp32(1/scale), to e4m3, into paged caches of 2^20 slots (pages of 16)."""
+    import sparse_attention_kv_row_gb300 as hs
+
+    c = synth.STORE_KV
+    n, heads, hd, slots, ps = c["n_tokens"], c["heads"], c["head_dim"], c["pool_rows"], 16
+    g = torch.Generator(device=dev)
+    g.manual_seed(c["seed"] + 1)
+    k = torch.randn((n, heads, hd), generator=g, device=dev).to(torch.bfloat16)
+    v = torch.randn((n, heads, hd), generator=g, device=dev).to(torch.bfloat16)
+    kc = torch.zeros((slots // ps, ps, heads, hd), dtype=torch.uint8, device=dev)
+    vc = torch.zeros_like(kc)
+    loc = torch.randperm(slots, generator=g, device=dev)[:n]
+    ks = torch.tensor([0.25], device=dev)
+    vs = torch.tensor([1.5], device=dev)
+    fn = lambda: hs.fp8_store_kv(k, v, kc, vc, loc, k_scale=ks, v_scale=vs, page_size=ps,  # noqa
+                                 stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fn()
+    t = time_launches(fn, 30, stream, flush)
+    alg = 2 * n * heads * hd * (2 + 1) + 8 * n
+    del kc, vc
+    torch.cuda.empty_cache()
+    return dict(workload="fp8 KV write: 4096 tokens x [8 x 128] bf16 K and V -> e4m3 paged "
+                         "caches (2^20 slots, pages of 16), scales given",
+                us_per_call=t * 1e6, alg_bytes=alg, gbs=alg / t / 1e9,
+                roofline=dict(bound="hbm", achieved=alg / t / 1e9, peak=hbm_peak,
+                              frac=alg / t / 1e9 / hbm_peak), launches_timed=30,
+                l2="flushed (256 MiB write) before every launch")
+
+
 def run_host_link_peak(dev, stream, pinned):
     import sparse_attention_kv_row_gb300 as hs
 
@@ -785,6 +818,7 @@ def main():
         s = torch.cuda.Stream(dev)
         flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         ops["store_kv"] = run_store_kv(dev, hbm_peak, flush, s)
+        ops["fp8_store_kv"] = run_fp8_store(dev, hbm_peak, flush, s)
         ops["tiny_swap_in"] = run_swapin_cfg(synth.TINY, dev, s, 8, hbm_peak, None, flush=flush,
                                              shared_pool=True)
         probe_buf = torch.empty(2 * GiB, dtype=torch.uint8, pin_memory=True)

@@ -214,6 +214,47 @@ hs_err hs_transfer_kv(const uint64_t* src_ptrs, const uint64_t* dst_ptrs, int32_
                       int64_t dst_rows, int64_t row_bytes, int32_t* status,
                       hs_stream_t stream);
 
+/* Input element types of hs_fp8_store_kv. */
+#define HS_DT_F32 0
+#define HS_DT_F16 1
+#define HS_DT_BF16 2
+
+/*
+ * hs_fp8_store_kv -- quantise K/V to FP8 E4M3 and scatter them into a paged
+ * KV cache.  Defined by: tokenspeed tokenspeed_kernel/ops/kvcache/triton.py,
+ * fused_fp8_set_kv_buffer and _fused_fp8_set_kv_buffer_kernel.  For token t
+ * with slot L = cache_loc[t] (skipped, with HS_ST_BAD_INDEX OR-ed into
+ * *status, when L is outside [0, num_slots)), page = L / page_size and
+ * offset = L % page_size; for every head h < num_kv_heads and d < head_dim:
+ *   y = x                               (k_scale / v_scale NULL), or
+ *   y = fp32(x * fp32(1 / scale))       (the inverse divided in fp32)
+ *   cache[page*cache_stride_page + offset*cache_stride_offset + h*cache_stride_head + d]
+ *     = e4m3(y)
+ * where e4m3 rounds to nearest, ties to even, saturates finite overflow and
+ * infinities to +-448 and keeps NaN a NaN (OCP E4M3 "FN": bias 7, no
+ * infinities, S.1111.111 = NaN).
+ *
+ *  k, v          device [n_tokens, num_kv_heads, head_dim] of in_dtype
+ *                (HS_DT_F32 / F16 / BF16), token and head strides in elements,
+ *                dims contiguous; v NULL = K only (then v_cache NULL)
+ *  k_cache/v_cache  device bytes; strides in bytes (dims contiguous); a flat
+ *                cache [slots, heads, dim] is page_size-row pages with
+ *                cache_stride_page = page_size * cache_stride_offset
+ *  cache_loc     device int64 [n_tokens]
+ *  k_scale/v_scale  device fp32 [1] or NULL
+ *  status        device int32 [1] or NULL
+ * Precondition (not checked): cache_loc values are distinct; inputs and caches
+ * do not overlap.
+ */
+hs_err hs_fp8_store_kv(const void* k, const void* v, int32_t in_dtype, int64_t k_stride_token,
+                       int64_t k_stride_head, int64_t v_stride_token, int64_t v_stride_head,
+                       void* k_cache, void* v_cache, int64_t cache_stride_page,
+                       int64_t cache_stride_offset, int64_t cache_stride_head,
+                       int32_t page_size, int64_t num_slots, const int64_t* cache_loc,
+                       int64_t n_tokens, int32_t num_kv_heads, int32_t head_dim,
+                       const float* k_scale, const float* v_scale, int32_t* status,
+                       hs_stream_t stream);
+
 /*
  * hs_gather_misses -- replay a swap-in's miss plan onto the layers that share
  * the resolving layer's indices (same slot assignment, other bytes): for

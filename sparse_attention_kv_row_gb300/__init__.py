@@ -23,7 +23,8 @@ from . import _capi
 from ._capi import (HisparseError, SwapInArgs, ST_BAD_HOT_ROW, ST_BAD_INDEX,  # noqa: F401
                     ST_BAD_LRU_SLOT, ST_BAD_POOL_ROW, ST_BAD_STATE, ST_DUP_ID, ST_TIMEOUT)
 
-__all__ = ["swap_in", "swap_in_args", "make_swap_in_args", "gather_misses", "store_kv", "transfer_kv",
+__all__ = ["swap_in", "swap_in_args", "make_swap_in_args", "gather_misses", "fp8_store_kv",
+           "store_kv", "transfer_kv",
            "transfer_kv_layers", "probe_read", "swap_in_smem_bytes", "library_path",
            "HisparseError", "SwapInArgs"]
 
@@ -217,6 +218,56 @@ def gather_misses(pool_layers, hot_layers, miss_src, miss_dst, miss_count, *, ha
         min(t.shape[0] for t in pool_layers), min(t.shape[0] for t in hot_layers), rb,
         _ptr(miss_src), _ptr(miss_dst), miss_src.stride(0), _ptr(miss_count), B, K,
         _ptr(status), C.c_void_p(_stream(stream))), "hs_gather_misses")
+
+
+_FP8_IN = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+
+
+def fp8_store_kv(k, v, k_cache, v_cache, cache_loc, *, k_scale=None, v_scale=None,
+                 page_size=16, status=None, stream=None) -> None:
+    """Quantise K/V [T, heads, dim] (or [T, heads*dim]) to FP8 E4M3 and scatter token t
+    to slot cache_loc[t] of a paged cache ([pages, page_size, heads, dim] or
+    [slots, heads, dim]; uint8 or float8_e4m3fn).  With k_scale and v_scale
+    (device fp32 tensors of one element) values are multiplied by fp32(1/scale)."""
+    _need(cache_loc, torch.int64, "cache_loc", 1)
+    if k.dtype not in _FP8_IN or (v is not None and v.dtype != k.dtype):
+        raise TypeError("k and v must both be float32, float16 or bfloat16")
+    if (v is None) != (v_cache is None):
+        raise ValueError("v and v_cache go together")
+    if k_cache.element_size() != 1 or (v_cache is not None and v_cache.element_size() != 1):
+        raise TypeError("caches must be 1-byte tensors (uint8 or float8_e4m3fn)")
+    if k_cache.dim() == 4:
+        _, ps, heads, dim = k_cache.shape
+        if ps != page_size:
+            raise ValueError(f"page_size mismatch: cache has {ps}, expected {page_size}")
+        c_page, c_off, c_head = k_cache.stride(0), k_cache.stride(1), k_cache.stride(2)
+        num_slots = k_cache.shape[0] * ps
+    elif k_cache.dim() == 3:
+        _, heads, dim = k_cache.shape
+        c_page, c_off, c_head = k_cache.stride(0) * page_size, k_cache.stride(0), k_cache.stride(1)
+        num_slots = k_cache.shape[0] // page_size * page_size
+    else:
+        raise ValueError("caches must be 3-D or 4-D")
+    if k_cache.stride(-1) != 1 or (v_cache is not None and v_cache.stride() != k_cache.stride()):
+        raise ValueError("caches need contiguous dims and the same layout")
+    T = k.shape[0]
+    if k.dim() == 2:
+        k = k.view(T, heads, dim)
+        v = v.view(T, heads, dim) if v is not None else None
+    for t, name in ((k, "k"), (v, "v")):
+        if t is not None and (tuple(t.shape) != (T, heads, dim) or t.stride(2) != 1):
+            raise ValueError(f"{name} must be [T, {heads}, {dim}] with a contiguous last dim")
+    if cache_loc.numel() != T:
+        raise ValueError("cache_loc needs one entry per token")
+    for sc, name in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if sc is not None:
+            _need(sc, torch.float32, name)
+    _capi.check(_lib().hs_fp8_store_kv(
+        _ptr(k), _ptr(v), _FP8_IN[k.dtype], k.stride(0), k.stride(1),
+        v.stride(0) if v is not None else 0, v.stride(1) if v is not None else 0,
+        _ptr(k_cache), _ptr(v_cache), c_page, c_off, c_head, page_size, num_slots,
+        _ptr(cache_loc), T, heads, dim, _ptr(k_scale), _ptr(v_scale), _ptr(status),
+        C.c_void_p(_stream(stream))), "hs_fp8_store_kv")
 
 
 def store_kv(k_src, v_src, k_dst, v_dst, loc, status=None, stream=None) -> None:

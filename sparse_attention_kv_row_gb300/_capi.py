@@ -23,11 +23,12 @@ ST_BAD_INDEX = 64
 SEQ_LENS_I64 = 1
 REQ_STATE_I64 = 2
 OVERLAP_PREV = 4
+DT_F32, DT_F16, DT_BF16 = 0, 1, 2
 ABI_VERSION = 2
 
 # Every symbol include/hisparse.h declares.
 EXPORTS = ("hs_swap_in", "hs_swap_in_smem_bytes", "hs_store_kv", "hs_transfer_kv",
-           "hs_gather_misses", "hs_probe_read", "hs_err_string", "hs_status_string", "hs_last_error",
+           "hs_gather_misses", "hs_fp8_store_kv", "hs_probe_read", "hs_err_string", "hs_status_string", "hs_last_error",
            "hs_abi_version")
 
 
@@ -91,6 +92,9 @@ def load() -> C.CDLL:
         lib.hs_gather_misses.argtypes = [vp, vp, i32, i32, i64, i64, i64, vp, vp, i64, vp, i32,
                                          i32, vp, vp]
         lib.hs_gather_misses.restype = C.c_int
+        lib.hs_fp8_store_kv.argtypes = [vp, vp, i32, i64, i64, i64, i64, vp, vp, i64, i64, i64,
+                                        i32, i64, vp, i64, i32, i32, vp, vp, vp, vp]
+        lib.hs_fp8_store_kv.restype = C.c_int
         lib.hs_probe_read.argtypes = [vp, i64, vp, vp]
         lib.hs_probe_read.restype = C.c_int
         lib.hs_err_string.argtypes = [i32]
