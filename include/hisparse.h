@@ -243,6 +243,7 @@ hs_err hs_transfer_kv(const uint64_t* src_ptrs, const uint64_t* dst_ptrs, int32_
  *  cache_loc     device int64 [n_tokens]
  *  k_scale/v_scale  device fp32 [1] or NULL
  *  status        device int32 [1] or NULL
+ * Limits: num_slots < 2^32 (else HS_ERR_UNSUPPORTED).
  * Precondition (not checked): cache_loc values are distinct; inputs and caches
  * do not overlap.
  */

@@ -25,6 +25,7 @@ namespace {
 
 constexpr int kFp8Threads = 256;
 constexpr int kFp8BlocksPerSm = 8;
+constexpr int kFp8Unroll = 2;  // units in flight per thread
 
 struct Fp8Params {
   const unsigned char* in[2];  // K, V inputs
@@ -38,7 +39,7 @@ struct Fp8Params {
   uint32_t chunks;         // chunks per (token, K|V, head) row
   uint32_t rows_per_tok;   // kv * heads
   uint32_t heads;
-  FastDiv div_chunks, div_rows, div_heads;
+  FastDiv div_chunks, div_rows, div_heads, div_page;  // div_page: num_slots < 2^32
   int64_t t_begin;         // first token of this launch
   uint32_t units;          // launch tokens * rows_per_tok * chunks (< 2^32)
   int32_t* status;
@@ -84,66 +85,100 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_store_kernel(const Fp8Params 
   const float inv_k = p.scale[0] != nullptr ? 1.0f / __ldg(p.scale[0]) : 1.0f;
   const float inv_v = p.scale[1] != nullptr ? 1.0f / __ldg(p.scale[1]) : 1.0f;
   const uint32_t stride = gridDim.x * blockDim.x;
-  for (uint32_t u = blockIdx.x * blockDim.x + threadIdx.x; u < p.units; u += stride) {
-    // u = ((t' * rows_per_tok) + kv * heads + h) * chunks + c, t = t_begin + t'
-    const uint32_t row = div_any(u, p.div_chunks);
-    const uint32_t c = u - row * p.chunks;
-    const uint32_t tt = div_any(row, p.div_rows);
-    const uint32_t rk = row - tt * p.rows_per_tok;
-    const int64_t t = p.t_begin + tt;
-    const uint32_t kv = div_any(rk, p.div_heads);
-    const uint32_t h = rk - kv * p.heads;
-    const int64_t L = __ldg(p.loc + t);
-    if (L < 0 || L >= p.num_slots) {
-      if (rk == 0 && c == 0 && p.status) atomicOr(p.status, HS_ST_BAD_INDEX);
-      continue;
-    }
-    const int64_t page = L / p.page_size, off = L - page * p.page_size;
-    const unsigned char* src = (kv ? p.in[1] : p.in[0]) +
-                               t * (kv ? p.stride_token[1] : p.stride_token[0]) +
-                               static_cast<int64_t>(h) * (kv ? p.stride_head[1] : p.stride_head[0]) +
-                               static_cast<int64_t>(c) * E * kInBytes;
-    unsigned char* dst = (kv ? p.cache[1] : p.cache[0]) + page * p.c_page + off * p.c_off +
-                         static_cast<int64_t>(h) * p.c_head + static_cast<int64_t>(c) * E;
-    const float sc = kv ? inv_v : inv_k;
-    const bool scaled = (kv ? p.scale[1] : p.scale[0]) != nullptr;
-    if constexpr (!kVec) {
-      const float x = load_elem<kDtype>(src);
-      *dst = static_cast<unsigned char>(e4m3x2(scaled ? x * sc : x, 0.0f) & 0xFF);
-    } else {
-      const uint4 raw = ld_stream_v4(src);
-      float x[E];
-      if constexpr (kDtype == HS_DT_F32) {
-        x[0] = __uint_as_float(raw.x);
-        x[1] = __uint_as_float(raw.y);
-        x[2] = __uint_as_float(raw.z);
-        x[3] = __uint_as_float(raw.w);
-      } else {
-        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  // kUnroll units per thread per round, all loads issued before any convert.
+  for (uint32_t u0 = blockIdx.x * blockDim.x + threadIdx.x; u0 < p.units;
+       u0 += stride * kFp8Unroll) {
+    const unsigned char* src[kFp8Unroll];
+    unsigned char* dst[kFp8Unroll];
+    int64_t L[kFp8Unroll];
+    uint32_t kvs[kFp8Unroll];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint16_t lo = static_cast<uint16_t>(w[i] & 0xFFFF), hi = static_cast<uint16_t>(w[i] >> 16);
-          if constexpr (kDtype == HS_DT_F16) {
-            x[2 * i] = __half2float(__ushort_as_half(lo));
-            x[2 * i + 1] = __half2float(__ushort_as_half(hi));
-          } else {
-            x[2 * i] = __uint_as_float(static_cast<uint32_t>(lo) << 16);
-            x[2 * i + 1] = __uint_as_float(static_cast<uint32_t>(hi) << 16);
+    for (int j = 0; j < kFp8Unroll; ++j) {
+      // u = ((t' * rows_per_tok) + kv * heads + h) * chunks + c, t = t_begin + t'
+      const uint32_t u = u0 + j * stride;
+      L[j] = -1;
+      src[j] = nullptr;
+      dst[j] = nullptr;
+      kvs[j] = 0;
+      if (u >= p.units) continue;
+      const uint32_t row = div_any(u, p.div_chunks);
+      const uint32_t c = u - row * p.chunks;
+      const uint32_t tt = div_any(row, p.div_rows);
+      const uint32_t rk = row - tt * p.rows_per_tok;
+      const int64_t t = p.t_begin + tt;
+      const uint32_t kv = div_any(rk, p.div_heads);
+      const uint32_t h = rk - kv * p.heads;
+      kvs[j] = kv;
+      L[j] = __ldg(p.loc + t);
+      src[j] = (kv ? p.in[1] : p.in[0]) + t * (kv ? p.stride_token[1] : p.stride_token[0]) +
+               static_cast<int64_t>(h) * (kv ? p.stride_head[1] : p.stride_head[0]) +
+               static_cast<int64_t>(c) * E * kInBytes;
+      dst[j] = (kv ? p.cache[1] : p.cache[0]) + static_cast<int64_t>(h) * p.c_head +
+               static_cast<int64_t>(c) * E;
+      if (rk == 0 && c == 0) kvs[j] |= 2u;  // the token's first unit reports a bad slot
+    }
+    uint4 raw[kFp8Unroll];
+    float x1[kFp8Unroll];
+#pragma unroll
+    for (int j = 0; j < kFp8Unroll; ++j) {
+      if (src[j] == nullptr) continue;
+      if constexpr (kVec)
+        raw[j] = ld_stream_v4(src[j]);
+      else
+        x1[j] = load_elem<kDtype>(src[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < kFp8Unroll; ++j) {
+      if (src[j] == nullptr) continue;
+      if (L[j] < 0 || L[j] >= p.num_slots) {
+        if ((kvs[j] & 2u) && p.status) atomicOr(p.status, HS_ST_BAD_INDEX);
+        continue;
+      }
+      const int64_t page = div_any(static_cast<uint32_t>(L[j]), p.div_page);
+      const int64_t off = L[j] - page * p.page_size;
+      unsigned char* d = dst[j] + page * p.c_page + off * p.c_off;
+      const bool is_v = (kvs[j] & 1u) != 0;
+      const float sc = is_v ? inv_v : inv_k;
+      const bool scaled = (is_v ? p.scale[1] : p.scale[0]) != nullptr;
+      if constexpr (!kVec) {
+        *d = static_cast<unsigned char>(e4m3x2(scaled ? x1[j] * sc : x1[j], 0.0f) & 0xFF);
+      } else {
+        float x[E];
+        if constexpr (kDtype == HS_DT_F32) {
+          x[0] = __uint_as_float(raw[j].x);
+          x[1] = __uint_as_float(raw[j].y);
+          x[2] = __uint_as_float(raw[j].z);
+          x[3] = __uint_as_float(raw[j].w);
+        } else {
+          const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint16_t lo = static_cast<uint16_t>(w[i] & 0xFFFF);
+            const uint16_t hi = static_cast<uint16_t>(w[i] >> 16);
+            if constexpr (kDtype == HS_DT_F16) {
+              x[2 * i] = __half2float(__ushort_as_half(lo));
+              x[2 * i + 1] = __half2float(__ushort_as_half(hi));
+            } else {
+              x[2 * i] = __uint_as_float(static_cast<uint32_t>(lo) << 16);
+              x[2 * i + 1] = __uint_as_float(static_cast<uint32_t>(hi) << 16);
+            }
           }
         }
-      }
-      if (scaled) {
+        if (scaled) {
 #pragma unroll
-        for (int i = 0; i < E; ++i) x[i] = x[i] * sc;  // one fp32 multiply per element
-      }
-      if constexpr (E == 8) {
-        uint2 o;
-        o.x = static_cast<uint32_t>(e4m3x2(x[0], x[1])) | (static_cast<uint32_t>(e4m3x2(x[2], x[3])) << 16);
-        o.y = static_cast<uint32_t>(e4m3x2(x[4], x[5])) | (static_cast<uint32_t>(e4m3x2(x[6], x[7])) << 16);
-        *reinterpret_cast<uint2*>(dst) = o;
-      } else {
-        *reinterpret_cast<uint32_t*>(dst) =
-            static_cast<uint32_t>(e4m3x2(x[0], x[1])) | (static_cast<uint32_t>(e4m3x2(x[2], x[3])) << 16);
+          for (int i = 0; i < E; ++i) x[i] = x[i] * sc;  // one fp32 multiply per element
+        }
+        if constexpr (E == 8) {
+          uint2 o;
+          o.x = static_cast<uint32_t>(e4m3x2(x[0], x[1])) |
+                (static_cast<uint32_t>(e4m3x2(x[2], x[3])) << 16);
+          o.y = static_cast<uint32_t>(e4m3x2(x[4], x[5])) |
+                (static_cast<uint32_t>(e4m3x2(x[6], x[7])) << 16);
+          *reinterpret_cast<uint2*>(d) = o;
+        } else {
+          *reinterpret_cast<uint32_t*>(d) = static_cast<uint32_t>(e4m3x2(x[0], x[1])) |
+                                            (static_cast<uint32_t>(e4m3x2(x[2], x[3])) << 16);
+        }
       }
     }
   }
@@ -165,6 +200,8 @@ extern "C" hs_err hs_fp8_store_kv(const void* k, const void* v, int32_t in_dtype
   clear_error();
   if (in_dtype != HS_DT_F32 && in_dtype != HS_DT_F16 && in_dtype != HS_DT_BF16)
     return fail(HS_ERR_ARG, "hs_fp8_store_kv: unknown input dtype %d", in_dtype);
+  if (num_slots > 0xFFFFFFFFll)
+    return fail(HS_ERR_UNSUPPORTED, "hs_fp8_store_kv: num_slots must be < 2^32");
   if (n_tokens < 0 || page_size < 1 || num_slots < 0 || num_kv_heads < 1 || head_dim < 1)
     return fail(HS_ERR_ARG, "hs_fp8_store_kv: need n_tokens >= 0, page_size >= 1, "
                             "num_slots >= 0, heads >= 1, head_dim >= 1");
@@ -224,6 +261,8 @@ extern "C" hs_err hs_fp8_store_kv(const void* k, const void* v, int32_t in_dtype
   p.div_chunks = FastDiv{fastdiv_magic(chunks), chunks};
   p.div_rows = FastDiv{fastdiv_magic(p.rows_per_tok), p.rows_per_tok};
   p.div_heads = FastDiv{fastdiv_magic(p.heads), p.heads};
+  p.div_page = FastDiv{fastdiv_magic(static_cast<uint32_t>(page_size)),
+                       static_cast<uint32_t>(page_size)};
   p.status = status;
   using Fn = void (*)(const Fp8Params);
   Fn fn;
