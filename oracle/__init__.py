@@ -49,6 +49,10 @@ class _SwapInArgs(C.Structure):
         ("miss_count", C.c_void_p), ("stats", C.c_void_p), ("status", C.c_void_p),
         ("miss_src", C.c_void_p), ("miss_dst", C.c_void_p), ("plan_stride", C.c_int64),
         ("miss_mask", C.c_void_p), ("mask_stride", C.c_int64),
+        ("src_bt", C.c_void_p), ("src_bt_stride", C.c_int64), ("src_bt_blocks", C.c_int32),
+        ("src_block_size", C.c_int32),
+        ("res_bt", C.c_void_p), ("res_bt_stride", C.c_int64), ("res_bt_blocks", C.c_int32),
+        ("res_block_size", C.c_int32), ("res_null_block", C.c_int32),
     ]
 
 
@@ -76,6 +80,9 @@ def load(mutant: int = 0) -> C.CDLL:
                                           C.c_void_p, C.c_int64, C.c_void_p, C.c_int32,
                                           C.c_int32, C.c_void_p]
         lib.hso_gather_misses.restype = C.c_int
+        lib.hso_invalidate_tokens.argtypes = [C.c_void_p, C.c_int64, C.c_int32, C.c_int64,
+                                              C.c_void_p, C.c_void_p, C.c_int64, C.c_void_p]
+        lib.hso_invalidate_tokens.restype = C.c_int
         lib.hso_e4m3_encode_array.argtypes = [C.c_void_p, C.c_void_p, C.c_int64]
         lib.hso_e4m3_encode_array.restype = None
         lib.hso_fp8_store_kv.argtypes = [C.c_void_p, C.c_void_p, C.c_int32, C.c_int64,
@@ -110,7 +117,8 @@ def _check(a, dtype, name, ndim=None):
 def swap_in(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_rows,
             pool_k, hot_k, out_rows, hot_size, pool_v=None, hot_v=None, num_real=-1,
             miss_count=None, stats=None, status=None, miss_src=None, miss_dst=None,
-            miss_mask=None, mutant: int = 0) -> None:
+            miss_mask=None, src_block_table=None, src_block_size=1, res_block_table=None,
+            res_block_size=1, res_null_block=-1, mutant: int = 0) -> None:
     """One swap-in call over B batch rows; mutates slot_tokens, lru, hot_k/hot_v,
     out_rows and the optional outputs in place (all numpy, host memory).
 
@@ -121,6 +129,9 @@ def swap_in(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_
     Optional plan outputs: miss_src int64 [B, >=K] and miss_dst int32 [B, >=K]
     (the row's misses in order; entries past the miss count untouched),
     miss_mask int32 [B, >=K].
+    Optional block tables int32 [R, blocks]: ``src_block_table`` maps token t to
+    pool row bt[r][t // bs] * bs + t % bs (entries <= 0 unmapped) in place of
+    pool_rows; ``res_block_table`` serves tokens of resident blocks directly.
     """
     _check(topk_ids, np.int32, "topk_ids", 2)
     _check(seq_lens, np.int64, "seq_lens", 1)
@@ -128,7 +139,10 @@ def swap_in(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_
     _check(slot_tokens, np.int32, "slot_tokens", 2)
     _check(slot_rows, np.int32, "slot_rows", 2)
     _check(lru, np.int16, "lru", 2)
-    _check(pool_rows, np.int64, "pool_rows", 2)
+    if pool_rows is not None:
+        _check(pool_rows, np.int64, "pool_rows", 2)
+    _check(src_block_table, np.int32, "src_block_table", 2)
+    _check(res_block_table, np.int32, "res_block_table", 2)
     for n, a in (("pool_k", pool_k), ("pool_v", pool_v), ("hot_k", hot_k), ("hot_v", hot_v)):
         _check(a, np.uint8, n, 2)
     _check(out_rows, np.int32, "out_rows", 2)
@@ -153,8 +167,9 @@ def swap_in(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_
         slot_tokens=_ptr(slot_tokens), slot_tokens_stride=_row_stride(slot_tokens),
         slot_rows=_ptr(slot_rows), slot_rows_stride=_row_stride(slot_rows),
         lru=_ptr(lru), lru_stride=_row_stride(lru),
-        pool_rows=_ptr(pool_rows), pool_rows_stride=_row_stride(pool_rows),
-        pool_rows_cols=pool_rows.shape[1],
+        pool_rows=_ptr(pool_rows),
+        pool_rows_stride=_row_stride(pool_rows) if pool_rows is not None else 0,
+        pool_rows_cols=pool_rows.shape[1] if pool_rows is not None else 0,
         pool_k=_ptr(pool_k), pool_v=_ptr(pool_v), pool_num_rows=pool_k.shape[0],
         hot_k=_ptr(hot_k), hot_v=_ptr(hot_v), hot_num_rows=hot_k.shape[0],
         row_bytes=pool_k.shape[1],
@@ -163,10 +178,32 @@ def swap_in(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_
         miss_src=_ptr(miss_src), miss_dst=_ptr(miss_dst),
         plan_stride=_row_stride(miss_src) if miss_src is not None else 0,
         miss_mask=_ptr(miss_mask),
-        mask_stride=_row_stride(miss_mask) if miss_mask is not None else 0)
+        mask_stride=_row_stride(miss_mask) if miss_mask is not None else 0,
+        src_bt=_ptr(src_block_table),
+        src_bt_stride=_row_stride(src_block_table) if src_block_table is not None else 0,
+        src_bt_blocks=src_block_table.shape[1] if src_block_table is not None else 0,
+        src_block_size=src_block_size,
+        res_bt=_ptr(res_block_table),
+        res_bt_stride=_row_stride(res_block_table) if res_block_table is not None else 0,
+        res_bt_blocks=res_block_table.shape[1] if res_block_table is not None else 0,
+        res_block_size=res_block_size, res_null_block=res_null_block)
+    if pool_rows is None and src_block_table is None:
+        raise ValueError("need pool_rows or src_block_table")
     rc = load(mutant).hso_swap_in(C.byref(a))
     if rc != 0:
         raise ValueError("oracle swap_in rejected its arguments")
+
+
+def invalidate_tokens(*, slot_tokens, hot_size, state_rows, tokens, status=None) -> None:
+    """Slots [0, hot_size) of state row state_rows[n] holding token tokens[n] become -1."""
+    _check(slot_tokens, np.int32, "slot_tokens", 2)
+    _check(state_rows, np.int64, "state_rows", 1)
+    _check(tokens, np.int32, "tokens", 1)
+    rc = load().hso_invalidate_tokens(_ptr(slot_tokens), _row_stride(slot_tokens), hot_size,
+                                      slot_tokens.shape[0], _ptr(state_rows), _ptr(tokens),
+                                      tokens.shape[0], _ptr(status))
+    if rc != 0:
+        raise ValueError("oracle invalidate_tokens rejected its arguments")
 
 
 def gather_misses(*, pool_k, hot_k, miss_src, miss_dst, miss_count, pool_v=None, hot_v=None,

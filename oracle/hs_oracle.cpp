@@ -70,6 +70,28 @@ void pad_row(const hso_swap_in_args* a, int32_t b) {
   if (a->status) a->status[b] = 0;
 }
 
+// Block-table lookups (see hso_swap_in_args): -1 when the token has no row.
+int64_t resident_row(const hso_swap_in_args* a, int64_t r, int32_t t) {
+  if (!a->res_bt) return -1;
+  const int64_t blk = t / a->res_block_size;
+  if (blk >= a->res_bt_blocks) return -1;
+  const int32_t e = a->res_bt[r * a->res_bt_stride + blk];
+  if (e < 0 || e == a->res_null_block) return -1;
+  return (int64_t)e * a->res_block_size + t % a->res_block_size;
+}
+int64_t source_row(const hso_swap_in_args* a, int64_t r, int32_t t) {
+  const int64_t blk = t / a->src_block_size;
+  if (blk >= a->src_bt_blocks) return -1;
+  const int32_t e = a->src_bt[r * a->src_bt_stride + blk];
+#if HSO_MUTANT == 15
+  if (e < 0) return -1;  // planted: block 0 taken as mapped
+#else
+  if (e <= 0) return -1;
+#endif
+  const int64_t g = (int64_t)e * a->src_block_size + t % a->src_block_size;
+  return g < a->pool_num_rows ? g : -1;
+}
+
 void swap_in_row(const hso_swap_in_args* a, int32_t b) {
   const int32_t K = a->top_k;
   const int32_t H = a->hot_size;
@@ -91,7 +113,7 @@ void swap_in_row(const hso_swap_in_args* a, int32_t b) {
   int32_t* tokens = a->slot_tokens + r * a->slot_tokens_stride;
   const int32_t* rows = a->slot_rows + r * a->slot_rows_stride;
   int16_t* lru = a->lru + r * a->lru_stride;
-  const int64_t* pool_rows = a->pool_rows + r * a->pool_rows_stride;
+  const int64_t* pool_rows = a->pool_rows ? a->pool_rows + r * a->pool_rows_stride : nullptr;
   int32_t st = 0;
 
   // Step 3: fast path -- the whole sequence fits the hot buffer in order.
@@ -108,6 +130,10 @@ void swap_in_row(const hso_swap_in_args* a, int32_t b) {
 #else
       out[i] = (i < count && t >= 0 && t < Lb) ? rows[t] : -1;
 #endif
+      if (i < count && t >= 0 && t < Lb) {  // a resident block serves the token
+        const int64_t rr = resident_row(a, r, t);
+        if (rr >= 0) out[i] = (int32_t)rr;
+      }
     }
     if (a->miss_count) a->miss_count[b] = 0;
     if (a->status) a->status[b] = 0;
@@ -131,9 +157,12 @@ void swap_in_row(const hso_swap_in_args* a, int32_t b) {
     if (seen.count(t)) { st |= HSO_ST_DUP_ID; continue; }
     seen.insert(t);
 #endif
+    const int64_t rr = resident_row(a, r, t);
+    if (rr >= 0) { out[i] = (int32_t)rr; continue; }  // served from a resident block
 #if HSO_MUTANT != 4
     if ((int64_t)t == Lb - 1) { out[i] = rows[H]; continue; }  // newest slot
 #endif
+    if (a->src_bt && source_row(a, r, t) < 0) continue;  // no source row: invalid
     want[t] = i;
   }
 
@@ -170,7 +199,8 @@ void swap_in_row(const hso_swap_in_args* a, int32_t b) {
     const int32_t t = ids[i];
     auto it = want.find(t);
     if (it == want.end() || it->second != i || resolved[i]) continue;
-    const int64_t pr = ((int64_t)t < a->pool_rows_cols) ? pool_rows[t] : -1;
+    const int64_t pr = a->src_bt ? source_row(a, r, t)
+                                 : (((int64_t)t < a->pool_rows_cols) ? pool_rows[t] : -1);
 #if HSO_MUTANT == 8
     if (pr < 0 || pr > a->pool_num_rows) {
 #else
@@ -266,6 +296,30 @@ extern "C" int hso_swap_in(const hso_swap_in_args* a) {
     return -1;
   if (a->batch <= 0 || a->top_k == 0) return 0;
   for (int32_t b = 0; b < a->batch; ++b) swap_in_row(a, b);
+  return 0;
+}
+
+extern "C" int hso_invalidate_tokens(int32_t* slot_tokens, int64_t slot_tokens_stride,
+                                     int32_t hot_size, int64_t num_states,
+                                     const int64_t* state_rows, const int32_t* tokens, int64_t n,
+                                     int32_t* status) {
+  if (hot_size < 0 || n < 0 || num_states < 0) return -1;
+  for (int64_t q = 0; q < n; ++q) {
+    const int64_t r = state_rows[q];
+    const int32_t t = tokens[q];
+    if (r < 0 || t < 0) continue;
+    if (r >= num_states) {
+      if (status) *status |= HSO_ST_BAD_INDEX;
+      continue;
+    }
+    int32_t* row = slot_tokens + r * slot_tokens_stride;
+#if HSO_MUTANT == 16
+    for (int32_t s = 0; s <= hot_size; ++s)  // planted: slot H included
+#else
+    for (int32_t s = 0; s < hot_size; ++s)
+#endif
+      if (row[s] == t) row[s] = -1;
+  }
   return 0;
 }
 

@@ -57,11 +57,33 @@ typedef struct hso_swap_in_args {
    * miss_mask[b][i] = 1 when top-k entry i was one of the row's misses. */
   int64_t* miss_src; int32_t* miss_dst; int64_t plan_stride;   /* [B, >=K] */
   int32_t* miss_mask; int64_t mask_stride;                      /* [B, >=K] */
+  /* Optional block tables, both indexed by the row's state row r (vLLM
+   * hisparse_resolve_residency_kernel, Phase 1).
+   * Source table (replaces pool_rows when not NULL): the pool row of token t is
+   * g = src_bt[r][t / src_block_size] * src_block_size + t % src_block_size when
+   * the block index is below src_bt_blocks, the entry is > 0 and g <
+   * pool_num_rows; otherwise the entry is invalid (-1, no state change).
+   * Resident table: when e = res_bt[r][t / res_block_size] (block index below
+   * res_bt_blocks) is >= 0 and != res_null_block, token t is served from the
+   * device: out = e * res_block_size + t % res_block_size, and the entry is not
+   * looked up, not a hit and not a miss. */
+  const int32_t* src_bt; int64_t src_bt_stride; int32_t src_bt_blocks; int32_t src_block_size;
+  const int32_t* res_bt; int64_t res_bt_stride; int32_t res_bt_blocks; int32_t res_block_size;
+  int32_t res_null_block;
 } hso_swap_in_args;
 
 /* Returns 0, or -1 when an argument is unusable (the oracle does not try to
  * mirror every synchronous check of the CUDA library). */
 int hso_swap_in(const hso_swap_in_args* a);
+
+/* Invalidates resident copies of rewritten tokens (vLLM
+ * hisparse_invalidate_written_slots_kernel, restated for request-relative slot
+ * tokens): for each n, with r = state_rows[n] and t = tokens[n]: every slot
+ * s < hot_size of state row r with slot_tokens[r][s] == t becomes -1.  r < 0
+ * or t < 0 is skipped; r >= num_states is skipped with HSO_ST_BAD_INDEX. */
+int hso_invalidate_tokens(int32_t* slot_tokens, int64_t slot_tokens_stride, int32_t hot_size,
+                          int64_t num_states, const int64_t* state_rows, const int32_t* tokens,
+                          int64_t n, int32_t* status);
 
 /* Replays a swap-in's miss plan onto another layer's pool and hot buffer:
  * for b < batch, m < min(max(miss_count[b], 0), top_k): d = miss_dst[b][m],

@@ -27,6 +27,7 @@ class Case:
     hot_k: np.ndarray       # uint8 [hot_rows, S]
     hot_v: np.ndarray | None
     num_real: int = -1
+    tables: dict = dataclasses.field(default_factory=dict)  # block tables (read-only)
 
     @property
     def B(self):
@@ -104,7 +105,7 @@ def run_oracle(case: Case, mutant: int = 0, plan: bool = False):
                    pool_rows=case.pool_rows, pool_k=case.pool_k, pool_v=case.pool_v,
                    hot_k=case.hot_k, hot_v=case.hot_v, out_rows=out, hot_size=case.H,
                    num_real=case.num_real, miss_count=miss, stats=stats, status=status,
-                   mutant=mutant, **kw)
+                   mutant=mutant, **kw, **case.tables)
     if plan:
         return out, miss, status, stats, kw["miss_src"], kw["miss_dst"], kw["miss_mask"]
     return out, miss, status, stats
