@@ -115,6 +115,22 @@ typedef enum hs_err {
  *  miss_src    int64 [batch, >=top_k] or NULL  stride plan_stride  } the miss plan,
  *  miss_dst    int32 [batch, >=top_k] or NULL  stride plan_stride  } for replay by
  *  miss_mask   int32 [batch, >=top_k] or NULL  stride mask_stride  } hs_gather_misses
+ *  src_bt      int32 [num_states, >=src_bt_blocks] or NULL   source block table
+ *  res_bt      int32 [num_states, >=res_bt_blocks] or NULL   resident block table
+ *
+ * Block tables (optional; vLLM csrc/libtorch_stable/hisparse_kernels.cu,
+ * hisparse_resolve_residency_kernel, Phase 1), both indexed by the row's
+ * state row r, for a valid id t that is the first copy of its value:
+ *  - resident: when e = res_bt[r][t / res_block_size] (block index below
+ *    res_bt_blocks) is >= 0 and != res_null_block, the entry emits
+ *    e * res_block_size + t % res_block_size and is not looked up, not a hit
+ *    and not a miss (also on the short-sequence path).  This precedes the
+ *    newest-token rule;
+ *  - source (replaces pool_rows, which may then be NULL): the pool row of t is
+ *    g = src_bt[r][t / src_block_size] * src_block_size + t % src_block_size;
+ *    when the block index is not below src_bt_blocks, the entry is <= 0 or
+ *    g >= pool_num_rows, the entry behaves as an invalid id (-1, no status
+ *    bit).  The newest token needs no source row.
  *
  * Miss plan (optional; vLLM csrc/libtorch_stable/hisparse_kernels.cu,
  * hisparse_gather_plan_kernel and hisparse_gather_compact_kernel): for the
@@ -158,6 +174,9 @@ typedef struct hs_swap_in_args {
   int32_t* status;
   int64_t* miss_src; int32_t* miss_dst; int64_t plan_stride;
   int32_t* miss_mask; int64_t mask_stride;
+  const int32_t* src_bt; int64_t src_bt_stride; int32_t src_bt_blocks; int32_t src_block_size;
+  const int32_t* res_bt; int64_t res_bt_stride; int32_t res_bt_blocks; int32_t res_block_size;
+  int32_t res_null_block;
 } hs_swap_in_args;
 
 hs_err hs_swap_in(const hs_swap_in_args* args, hs_stream_t stream);
@@ -257,6 +276,25 @@ hs_err hs_fp8_store_kv(const void* k, const void* v, int32_t in_dtype, int64_t k
                        hs_stream_t stream);
 
 /*
+ * hs_invalidate_tokens -- drop resident copies of rewritten tokens: for each
+ * n < n_tokens, with r = state_rows[n] and t = tokens[n], every slot
+ * s < hot_size of state row r with slot_tokens[r][s] == t becomes -1, so the
+ * next swap-in fetches the new row.  r < 0 or t < 0 is skipped; r >=
+ * num_states is skipped with HS_ST_BAD_INDEX OR-ed into *status.  Slot
+ * hot_size (the newest token's) is not touched.  Defined by: vLLM
+ * csrc/libtorch_stable/hisparse_kernels.cu, hisparse_invalidate_written_slots
+ * (restated for request-relative slot tokens).
+ *
+ *  slot_tokens  device int32 [num_states, >= hot_size + 1], stride in elements
+ *  state_rows   device int64 [n_tokens]; tokens device int32 [n_tokens]
+ *  status       device int32 [1] or NULL
+ */
+hs_err hs_invalidate_tokens(int32_t* slot_tokens, int64_t slot_tokens_stride, int32_t hot_size,
+                            int64_t num_states, const int64_t* state_rows,
+                            const int32_t* tokens, int64_t n_tokens, int32_t* status,
+                            hs_stream_t stream);
+
+/*
  * hs_gather_misses -- replay a swap-in's miss plan onto the layers that share
  * the resolving layer's indices (same slot assignment, other bytes): for
  * b < batch, m < min(max(miss_count[b], 0), top_k) and every pointer pair p in
@@ -304,7 +342,7 @@ const char* hs_status_string(int32_t bit);
 const char* hs_last_error(void);
 
 /* ABI version of this header. */
-#define HS_ABI_VERSION 2
+#define HS_ABI_VERSION 3
 int32_t hs_abi_version(void);
 
 #ifdef __cplusplus

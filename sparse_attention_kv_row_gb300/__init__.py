@@ -24,6 +24,7 @@ from ._capi import (HisparseError, SwapInArgs, ST_BAD_HOT_ROW, ST_BAD_INDEX,  # 
                     ST_BAD_LRU_SLOT, ST_BAD_POOL_ROW, ST_BAD_STATE, ST_DUP_ID, ST_TIMEOUT)
 
 __all__ = ["swap_in", "swap_in_args", "make_swap_in_args", "gather_misses", "fp8_store_kv",
+           "invalidate_tokens",
            "store_kv", "transfer_kv",
            "transfer_kv_layers", "probe_read", "swap_in_smem_bytes", "library_path",
            "HisparseError", "SwapInArgs"]
@@ -79,6 +80,8 @@ def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, 
                       pool_k, hot_k, out_rows, hot_size=None, pool_v=None, hot_v=None,
                       num_real=None, miss_count=None, stats=None, status=None,
                       miss_src=None, miss_dst=None, miss_mask=None,
+                      src_block_table=None, src_block_size=1, res_block_table=None,
+                      res_block_size=1, res_null_block=-1,
                       overlap_prev=False) -> SwapInArgs:
     """Build a reusable ``hs_swap_in_args`` for these tensors (see include/hisparse.h).
 
@@ -90,14 +93,24 @@ def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, 
     ``miss_src`` (int64) / ``miss_dst`` (int32) [B, >=K] receive the row's miss
     plan (pool row and hot row of each miss, in order, the first miss_count[b]
     entries) and ``miss_mask`` (int32 [B, >=K]) marks the entries that missed;
-    ``gather_misses`` replays the plan onto another layer."""
+    ``gather_misses`` replays the plan onto another layer.
+
+    ``src_block_table`` (int32 [R, blocks], pool_rows may then be None) maps token t
+    to pool row bt[r][t // bs] * bs + t % bs; ``res_block_table`` serves tokens of
+    resident blocks directly (see include/hisparse.h)."""
     H = int(hot_size if hot_size is not None else lru.shape[1])
     _need(topk_ids, torch.int32, "topk_ids", 2)
     _need(out_rows, torch.int32, "out_rows", 2)
     _need(slot_tokens, torch.int32, "slot_tokens", 2)
     _need(slot_rows, torch.int32, "slot_rows", 2)
     _need(lru, torch.int16, "lru", 2)
-    _need(pool_rows, torch.int64, "pool_rows", 2)
+    if pool_rows is None and src_block_table is None:
+        raise ValueError("need pool_rows or src_block_table")
+    if pool_rows is not None:
+        _need(pool_rows, torch.int64, "pool_rows", 2)
+    for t, name in ((src_block_table, "src_block_table"), (res_block_table, "res_block_table")):
+        if t is not None:
+            _need(t, torch.int32, name, 2)
     if seq_lens.dtype not in (torch.int32, torch.int64) or req_state.dtype not in (
             torch.int32, torch.int64):
         raise TypeError("seq_lens and req_state must be int32 or int64")
@@ -149,13 +162,15 @@ def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, 
         batch=B, top_k=K, hot_size=H, flags=flags, num_real=_ptr(num_real),
         topk_ids=_ptr(topk_ids), topk_stride=topk_ids.stride(0),
         seq_lens=_ptr(seq_lens), req_state=_ptr(req_state),
-        num_states=min(slot_tokens.shape[0], slot_rows.shape[0], lru.shape[0],
-                       pool_rows.shape[0]),
+        num_states=min([slot_tokens.shape[0], slot_rows.shape[0], lru.shape[0]] +
+                       [t.shape[0] for t in (pool_rows, src_block_table, res_block_table)
+                        if t is not None]),
         slot_tokens=_ptr(slot_tokens), slot_tokens_stride=slot_tokens.stride(0),
         slot_rows=_ptr(slot_rows), slot_rows_stride=slot_rows.stride(0),
         lru=_ptr(lru), lru_stride=lru.stride(0),
-        pool_rows=_ptr(pool_rows), pool_rows_stride=pool_rows.stride(0),
-        pool_rows_cols=pool_rows.shape[1],
+        pool_rows=_ptr(pool_rows),
+        pool_rows_stride=pool_rows.stride(0) if pool_rows is not None else 0,
+        pool_rows_cols=pool_rows.shape[1] if pool_rows is not None else 0,
         pool_k=pk_ptr, pool_v=pv_ptr, pool_num_rows=p_rows,
         hot_k=hk_ptr, hot_v=hv_ptr, hot_num_rows=h_rows,
         row_bytes=row_bytes, out_rows=_ptr(out_rows), out_stride=out_rows.stride(0),
@@ -163,14 +178,22 @@ def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, 
         miss_src=_ptr(miss_src), miss_dst=_ptr(miss_dst),
         plan_stride=miss_src.stride(0) if miss_src is not None else 0,
         miss_mask=_ptr(miss_mask),
-        mask_stride=miss_mask.stride(0) if miss_mask is not None else 0)
+        mask_stride=miss_mask.stride(0) if miss_mask is not None else 0,
+        src_bt=_ptr(src_block_table),
+        src_bt_stride=src_block_table.stride(0) if src_block_table is not None else 0,
+        src_bt_blocks=src_block_table.shape[1] if src_block_table is not None else 0,
+        src_block_size=src_block_size,
+        res_bt=_ptr(res_block_table),
+        res_bt_stride=res_block_table.stride(0) if res_block_table is not None else 0,
+        res_bt_blocks=res_block_table.shape[1] if res_block_table is not None else 0,
+        res_block_size=res_block_size, res_null_block=res_null_block)
     for t, name in ((miss_src, "miss_src"), (miss_dst, "miss_dst"), (miss_mask, "miss_mask")):
         if t is not None and (t.shape[0] < B or t.shape[1] < K):
             raise ValueError(f"{name} must be at least [batch, top_k]")
     # the struct holds raw pointers: keep the tensors alive as long as it lives
     args.tensors = (topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_rows,
                     pool_k, pool_v, hot_k, hot_v, out_rows, num_real, miss_count, stats, status,
-                    miss_src, miss_dst, miss_mask)
+                    miss_src, miss_dst, miss_mask, src_block_table, res_block_table)
     return args
 
 
@@ -182,6 +205,21 @@ def swap_in_args(args: SwapInArgs, stream=None) -> None:
 def swap_in(*, stream=None, **tensors) -> None:
     """One swap-in call; keyword tensors as in ``make_swap_in_args``."""
     swap_in_args(make_swap_in_args(**tensors), stream)
+
+
+def invalidate_tokens(slot_tokens, state_rows, tokens, *, hot_size=None, status=None,
+                      stream=None) -> None:
+    """Slots [0, hot_size) of state row state_rows[n] that hold token tokens[n] become -1."""
+    _need(slot_tokens, torch.int32, "slot_tokens", 2)
+    _need(state_rows, torch.int64, "state_rows", 1)
+    _need(tokens, torch.int32, "tokens", 1)
+    if state_rows.numel() != tokens.numel():
+        raise ValueError("state_rows and tokens differ in length")
+    H = int(hot_size if hot_size is not None else slot_tokens.shape[1] - 1)
+    _capi.check(_lib().hs_invalidate_tokens(
+        _ptr(slot_tokens), slot_tokens.stride(0), H, slot_tokens.shape[0], _ptr(state_rows),
+        _ptr(tokens), tokens.numel(), _ptr(status), C.c_void_p(_stream(stream))),
+        "hs_invalidate_tokens")
 
 
 def gather_misses(pool_layers, hot_layers, miss_src, miss_dst, miss_count, *, has_v=False,

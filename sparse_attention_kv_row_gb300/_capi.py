@@ -24,11 +24,11 @@ SEQ_LENS_I64 = 1
 REQ_STATE_I64 = 2
 OVERLAP_PREV = 4
 DT_F32, DT_F16, DT_BF16 = 0, 1, 2
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 # Every symbol include/hisparse.h declares.
 EXPORTS = ("hs_swap_in", "hs_swap_in_smem_bytes", "hs_store_kv", "hs_transfer_kv",
-           "hs_gather_misses", "hs_fp8_store_kv", "hs_probe_read", "hs_err_string", "hs_status_string", "hs_last_error",
+           "hs_gather_misses", "hs_fp8_store_kv", "hs_invalidate_tokens", "hs_probe_read", "hs_err_string", "hs_status_string", "hs_last_error",
            "hs_abi_version")
 
 
@@ -52,6 +52,10 @@ class SwapInArgs(C.Structure):
         ("miss_count", C.c_void_p), ("stats", C.c_void_p), ("status", C.c_void_p),
         ("miss_src", C.c_void_p), ("miss_dst", C.c_void_p), ("plan_stride", C.c_int64),
         ("miss_mask", C.c_void_p), ("mask_stride", C.c_int64),
+        ("src_bt", C.c_void_p), ("src_bt_stride", C.c_int64), ("src_bt_blocks", C.c_int32),
+        ("src_block_size", C.c_int32),
+        ("res_bt", C.c_void_p), ("res_bt_stride", C.c_int64), ("res_bt_blocks", C.c_int32),
+        ("res_block_size", C.c_int32), ("res_null_block", C.c_int32),
     ]
 
 
@@ -95,6 +99,8 @@ def load() -> C.CDLL:
         lib.hs_fp8_store_kv.argtypes = [vp, vp, i32, i64, i64, i64, i64, vp, vp, i64, i64, i64,
                                         i32, i64, vp, i64, i32, i32, vp, vp, vp, vp]
         lib.hs_fp8_store_kv.restype = C.c_int
+        lib.hs_invalidate_tokens.argtypes = [vp, i64, i32, i64, vp, vp, i64, vp, vp]
+        lib.hs_invalidate_tokens.restype = C.c_int
         lib.hs_probe_read.argtypes = [vp, i64, vp, vp]
         lib.hs_probe_read.restype = C.c_int
         lib.hs_err_string.argtypes = [i32]

@@ -6,6 +6,9 @@
 //  gather     vLLM csrc/libtorch_stable/hisparse_kernels.cu, hisparse_gather_plan_kernel /
 //             hisparse_gather_compact_kernel: a resolving layer's miss plan replayed
 //             onto a layer that shares its indices.
+//  invalidate vLLM csrc/libtorch_stable/hisparse_kernels.cu,
+//             hisparse_invalidate_written_slots_kernel: resident copies of
+//             rewritten tokens are dropped from the slot-token table.
 //  transfer   tokenspeed ... transfer_kv_per_layer(_mla) / transfer_kv_all_layer(_mla)
 //             and SGLang jit_kernel/csrc/hisparse.cuh, transfer_cache_dsv4_mla_kernel:
 //             for each index pair, the same row of every layer's cache.
@@ -209,6 +212,24 @@ __global__ void __launch_bounds__(kMoverThreads) gather_misses_kernel(const Gath
   }
 }
 
+// One block per rewritten token: its threads scan the state row's slots.
+__global__ void __launch_bounds__(256) invalidate_kernel(int32_t* slot_tokens, int64_t stride,
+                                                         int32_t hot_size, int64_t num_states,
+                                                         const int64_t* state_rows,
+                                                         const int32_t* tokens, int32_t* status) {
+  const int64_t q = blockIdx.x;
+  const int64_t r = __ldg(state_rows + q);
+  const int32_t t = __ldg(tokens + q);
+  if (r < 0 || t < 0) return;
+  if (r >= num_states) {
+    if (threadIdx.x == 0 && status) atomicOr(status, HS_ST_BAD_INDEX);
+    return;
+  }
+  int32_t* row = slot_tokens + r * stride;
+  for (int s = threadIdx.x; s < hot_size; s += blockDim.x)
+    if (row[s] == t) row[s] = -1;
+}
+
 __global__ void __launch_bounds__(512) probe_read_kernel(const uint4* src, int64_t n16,
                                                          unsigned long long* sink) {
   uint32_t acc = 0;
@@ -396,5 +417,29 @@ extern "C" hs_err hs_gather_misses(const uint64_t* pool_ptrs, const uint64_t* ho
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess)
     return fail(HS_ERR_CUDA, "hs_gather_misses launch: %s", cudaGetErrorString(e));
+  return HS_OK;
+}
+
+extern "C" hs_err hs_invalidate_tokens(int32_t* slot_tokens, int64_t slot_tokens_stride,
+                                       int32_t hot_size, int64_t num_states,
+                                       const int64_t* state_rows, const int32_t* tokens,
+                                       int64_t n_tokens, int32_t* status, hs_stream_t stream) {
+  using namespace hs;
+  clear_error();
+  if (n_tokens < 0 || hot_size < 0 || num_states < 0)
+    return fail(HS_ERR_ARG, "hs_invalidate_tokens: negative size");
+  if (n_tokens == 0 || hot_size == 0 || num_states == 0) return HS_OK;
+  if (slot_tokens == nullptr || state_rows == nullptr || tokens == nullptr)
+    return fail(HS_ERR_ARG, "hs_invalidate_tokens: slot_tokens, state_rows and tokens are required");
+  if (slot_tokens_stride < static_cast<int64_t>(hot_size) + 1)
+    return fail(HS_ERR_ARG, "hs_invalidate_tokens: slot_tokens_stride must be >= hot_size + 1");
+  if (n_tokens > 2147483647)
+    return fail(HS_ERR_UNSUPPORTED, "hs_invalidate_tokens: n_tokens must fit a grid");
+  invalidate_kernel<<<static_cast<unsigned>(n_tokens), 256, 0,
+                      reinterpret_cast<cudaStream_t>(stream)>>>(
+      slot_tokens, slot_tokens_stride, hot_size, num_states, state_rows, tokens, status);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return fail(HS_ERR_CUDA, "hs_invalidate_tokens launch: %s", cudaGetErrorString(e));
   return HS_OK;
 }

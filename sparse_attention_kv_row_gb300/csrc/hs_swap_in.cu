@@ -63,7 +63,11 @@ constexpr int32_t kUnclaimed = INT_MAX;
 constexpr uint32_t kMaxPolls = 1u << 22;  // bounded mbarrier waits
 
 // Per-entry classification, stored as one byte per top-k entry.
-enum : int8_t { kInvalid = 0, kRepeat = 1, kNewest = 2, kHit = 3, kBadPool = 4, kMiss = 5 };
+enum : int8_t {
+  kInvalid = 0, kRepeat = 1, kNewest = 2, kHit = 3, kBadPool = 4, kMiss = 5,
+  kResident = 6,  // served from a resident block (block tables)
+  kUnmapped = 7   // no source row through the source block table: treated as invalid
+};
 
 constexpr int kBloomBits = 17;  // request filter: 2^17 bits = 16 KB
 
@@ -151,6 +155,12 @@ struct SwapInParams {
   int64_t plan_stride;
   int32_t* miss_mask;
   int64_t mask_stride;
+  const int32_t* src_bt;  // optional block tables, indexed by state row
+  int64_t src_bt_stride;
+  int32_t src_bt_blocks, src_bs;
+  const int32_t* res_bt;
+  int64_t res_bt_stride;
+  int32_t res_bt_blocks, res_bs, res_null;
   uint32_t chunks_per_row;  // row_bytes / copy width
   FastDiv div_chunks;
   Layout lay;               // shared-memory layout, computed once on the host
@@ -332,7 +342,15 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     const int64_t count = Lb < K ? Lb : K;
     for (int i = e0 + tid; i < e1; i += kThreads) {
       const int32_t t = ids[i];
-      out_g[i] = (i < count && t >= 0 && t < Lb) ? __ldg(rows_g + t) : -1;
+      int32_t o = -1;
+      if (i < count && t >= 0 && t < Lb) {
+        o = __ldg(rows_g + t);
+        if (p.res_bt != nullptr && t / p.res_bs < p.res_bt_blocks) {  // a resident block
+          const int32_t e = __ldg(p.res_bt + r * p.res_bt_stride + t / p.res_bs);
+          if (e >= 0 && e != p.res_null) o = e * p.res_bs + t % p.res_bs;
+        }
+      }
+      out_g[i] = o;
       if (p.miss_mask) p.miss_mask[b * p.mask_stride + i] = 0;
     }
     if (j == 0 && tid == 0) {
@@ -477,6 +495,26 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     }
     return;
   }
+  // Block tables: each valid id's entries are loaded with LDGSTS into prs
+  // (free until P2's candidate prefetch), read back after the hash insert by
+  // the thread that loaded them.
+  const bool tables = p.src_bt != nullptr || p.res_bt != nullptr;
+  int2* tbl = reinterpret_cast<int2*>(prs);  // {resident entry, source entry}
+  if (tables) {
+    for (int i = tid; i < K; i += kThreads) {
+      const int32_t t = ids[i];
+      if (static_cast<uint32_t>(t) >= lim) continue;
+      if (p.res_bt != nullptr && t / p.res_bs < p.res_bt_blocks)
+        cp_async_4(&tbl[i].x, p.res_bt + r * p.res_bt_stride + t / p.res_bs);
+      else
+        tbl[i].x = -1;
+      if (p.src_bt != nullptr && t / p.src_bs < p.src_bt_blocks)
+        cp_async_4(&tbl[i].y, p.src_bt + r * p.src_bt_stride + t / p.src_bs);
+      else
+        tbl[i].y = 0;
+    }
+    cp_async_commit();
+  }
   // Hash the valid ids; only when an id repeats does a second pass make its
   // smallest entry index canonical.
   const int bits = L.hash_bits;
@@ -499,6 +537,28 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
         }
         h = (h + 1u) & hmask;
       }
+    }
+  }
+  if (tables) {  // resident ids and ids without a source row are not wanted
+    cp_async_wait_all();
+    for (int i = tid; i < K; i += kThreads) {
+      const int32_t t = ids[i];
+      if (static_cast<uint32_t>(t) >= lim) continue;
+      const int2 e = tbl[i];
+      int8_t c = 0;
+      int64_t row = -1;
+      if (p.res_bt != nullptr && e.x >= 0 && e.x != p.res_null) {
+        c = kResident;
+        row = static_cast<int64_t>(e.x) * p.res_bs + t % p.res_bs;
+      } else if (p.src_bt != nullptr && t != newest) {
+        const int64_t g = static_cast<int64_t>(e.y) * p.src_bs + t % p.src_bs;
+        if (e.y <= 0 || g >= p.pool_num_rows)
+          c = kUnmapped;
+        else
+          row = g;  // the candidate's pool row, if it misses
+      }
+      code[i] = c;
+      prs[i] = row;
     }
   }
   __syncthreads();
@@ -538,6 +598,11 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       else if (kv[k].x != -1)
         f[k] = probe_rest(tab, tk[k], hash_of(tk[k], bits), hmask);
     }
+    if (tables) {  // a resident id or one without a source row is not wanted
+#pragma unroll
+      for (int k = 0; k < IT; ++k)
+        if (f[k] >= 0 && code[f[k]] != 0) f[k] = -1;
+    }
 #pragma unroll
     for (int k = 0; k < IT; ++k)
       if (f[k] >= 0) atomicMin(&claim[f[k]], k * kThreads + tid);
@@ -546,15 +611,23 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   // Pool rows of the miss candidates (wanted, not newest, not claimed), loaded
   // with LDGSTS now so the load overlaps P3.
   const bool id_repeat = misc[kMiscRepeat] != 0;
-  const int64_t* pool_rows_g = p.pool_rows + r * p.pool_rows_stride;
+  // (With a source block table prs already holds the translated rows; for a
+  // resident entry it holds the resident row.)
+  const int64_t* pool_rows_g = p.pool_rows ? p.pool_rows + r * p.pool_rows_stride : nullptr;
   for (int i = tid; i < K; i += kThreads) {
     const int32_t t = ids[i];
-    const bool cand = static_cast<uint32_t>(t) < lim && t != newest && claim[i] == kUnclaimed &&
-                      t < p.pool_rows_cols && (!id_repeat || hash_find(tab, t, bits) == i);
-    if (cand)
+    const bool valid = static_cast<uint32_t>(t) < lim;
+    const int8_t pre = (tables && valid) ? code[i] : 0;
+    if (pre == kResident) continue;
+    const bool cand = valid && t != newest && pre == 0 && claim[i] == kUnclaimed &&
+                      (!id_repeat || hash_find(tab, t, bits) == i);
+    if (p.src_bt != nullptr) {
+      if (!cand) prs[i] = -1;
+    } else if (cand && t < p.pool_rows_cols) {
       cp_async_8(&prs[i], pool_rows_g + t);
-    else
+    } else {
       prs[i] = -1;
+    }
   }
   cp_async_commit();
 
@@ -608,8 +681,12 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       } else if (id_repeat && hash_find(tab, t, bits) != i) {
         c = kRepeat;
         my_flags |= HS_ST_DUP_ID;
+      } else if (tables && code[i] == kResident) {
+        c = kResident;
       } else if (t == newest) {
         c = kNewest;
+      } else if (tables && code[i] == kUnmapped) {
+        c = kInvalid;  // no source row: like an invalid id
       } else if (claim[i] != kUnclaimed) {
         c = kHit;
       } else {
@@ -675,6 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     } else if (mine) {
       int32_t o = -1;
       if (c == kNewest) o = rows[H];  // the newest token lives in slot H
+      if (c == kResident) o = static_cast<int32_t>(prs[i]);
       if (c == kHit) o = rows[lru[claim[i]]];
       out_g[i] = o;
     }
@@ -800,8 +878,8 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   } required[] = {{a->topk_ids, "topk_ids"},   {a->seq_lens, "seq_lens"},
                   {a->req_state, "req_state"}, {a->slot_tokens, "slot_tokens"},
                   {a->slot_rows, "slot_rows"}, {a->lru, "lru"},
-                  {a->pool_rows, "pool_rows"}, {a->pool_k, "pool_k"},
-                  {a->hot_k, "hot_k"},         {a->out_rows, "out_rows"}};
+                  {a->pool_k, "pool_k"},       {a->hot_k, "hot_k"},
+                  {a->out_rows, "out_rows"}};
   for (const auto& q : required)
     if (q.p == nullptr) return fail(HS_ERR_ARG, "hs_swap_in: %s is NULL", q.name);
   if ((a->pool_v == nullptr) != (a->hot_v == nullptr))
@@ -818,8 +896,17 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
     return fail(HS_ERR_ARG, "hs_swap_in: the miss plan needs miss_count and plan_stride >= top_k");
   if (a->miss_mask != nullptr && a->mask_stride < K)
     return fail(HS_ERR_ARG, "hs_swap_in: mask_stride must be >= top_k");
-  if (a->pool_rows_cols < 0 || a->pool_rows_stride < a->pool_rows_cols)
+  if (a->pool_rows == nullptr && a->src_bt == nullptr)
+    return fail(HS_ERR_ARG, "hs_swap_in: pool_rows or src_bt is required");
+  if (a->src_bt == nullptr &&
+      (a->pool_rows_cols < 0 || a->pool_rows_stride < a->pool_rows_cols))
     return fail(HS_ERR_ARG, "hs_swap_in: need 0 <= pool_rows_cols <= pool_rows_stride");
+  if (a->src_bt != nullptr &&
+      (a->src_block_size < 1 || a->src_bt_blocks < 0 || a->src_bt_stride < a->src_bt_blocks))
+    return fail(HS_ERR_ARG, "hs_swap_in: src_bt needs block size >= 1 and stride >= blocks");
+  if (a->res_bt != nullptr &&
+      (a->res_block_size < 1 || a->res_bt_blocks < 0 || a->res_bt_stride < a->res_bt_blocks))
+    return fail(HS_ERR_ARG, "hs_swap_in: res_bt needs block size >= 1 and stride >= blocks");
   if (a->num_states < 1 || a->pool_num_rows < 0 || a->hot_num_rows < 0)
     return fail(HS_ERR_ARG, "hs_swap_in: num_states >= 1, pool/hot row counts >= 0");
   if (a->hot_num_rows > INT32_MAX)
@@ -904,6 +991,15 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   p.miss_dst = a->miss_dst;
   p.plan_stride = a->plan_stride;
   p.miss_mask = a->miss_mask;
+  p.src_bt = a->src_bt;
+  p.src_bt_stride = a->src_bt_stride;
+  p.src_bt_blocks = a->src_bt_blocks;
+  p.src_bs = a->src_block_size;
+  p.res_bt = a->res_bt;
+  p.res_bt_stride = a->res_bt_stride;
+  p.res_bt_blocks = a->res_bt_blocks;
+  p.res_bs = a->res_block_size;
+  p.res_null = a->res_null_block;
   p.mask_stride = a->mask_stride;
   p.chunks_per_row = static_cast<uint32_t>(cpr);
   p.div_chunks = FastDiv{fastdiv_magic(static_cast<uint32_t>(cpr)), static_cast<uint32_t>(cpr)};

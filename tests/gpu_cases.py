@@ -34,6 +34,8 @@ class GpuCase:
         self.hot_v = t(case.hot_v) if case.hot_v is not None else None
         self.seq_dtype, self.req_dtype = seq_dtype, req_dtype
         self.num_real_on_device = num_real_on_device
+        self.tables = {k: (t(v) if isinstance(v, np.ndarray) else v)
+                       for k, v in case.tables.items()}
 
     def step(self, topk: np.ndarray, stream=None, plan=False):
         c = self.case
@@ -58,7 +60,7 @@ class GpuCase:
                    pool_rows=self.pool_rows, pool_k=self.pool_k, pool_v=self.pool_v,
                    hot_k=self.hot_k, hot_v=self.hot_v, out_rows=out, hot_size=c.H,
                    num_real=num_real, miss_count=miss, stats=stats, status=status,
-                   stream=stream, **kw)
+                   stream=stream, **kw, **self.tables)
         torch.cuda.synchronize()
         res = (out.cpu().numpy(), miss.cpu().numpy(), status.cpu().numpy(),
                stats.cpu().numpy().astype(np.uint64))
