@@ -258,7 +258,8 @@ __device__ __forceinline__ int32_t probe_rest(const int2* tab, int32_t key, uint
 // IT = LRU positions per thread (position k * 1024 + tid for k < IT); their
 // slot, claimed entry and hit flag stay in registers from P1 to P5, and each
 // phase handles them as batched, independent loads.
-template <int IT, int G>
+// kTables: the call passes block tables (compiled out of the common case).
+template <int IT, int G, bool kTables>
 __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x;
@@ -498,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   // Block tables: each valid id's entries are loaded with LDGSTS into prs
   // (free until P2's candidate prefetch), read back after the hash insert by
   // the thread that loaded them.
-  const bool tables = p.src_bt != nullptr || p.res_bt != nullptr;
+  constexpr bool tables = kTables;
   int2* tbl = reinterpret_cast<int2*>(prs);  // {resident entry, source entry}
   if (tables) {
     for (int i = tid; i < K; i += kThreads) {
@@ -800,12 +801,20 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
 using KernelFn = void (*)(const SwapInParams);
 
 template <int G>
-KernelFn pick_items(int items) {
+KernelFn pick_items(int items, bool tables) {
+  if (tables) {
+    switch (items) {
+      case 1: return swap_in_kernel<1, G, true>;
+      case 2: return swap_in_kernel<2, G, true>;
+      case 4: return swap_in_kernel<4, G, true>;
+      default: return swap_in_kernel<8, G, true>;
+    }
+  }
   switch (items) {
-    case 1: return swap_in_kernel<1, G>;
-    case 2: return swap_in_kernel<2, G>;
-    case 4: return swap_in_kernel<4, G>;
-    default: return swap_in_kernel<8, G>;
+    case 1: return swap_in_kernel<1, G, false>;
+    case 2: return swap_in_kernel<2, G, false>;
+    case 4: return swap_in_kernel<4, G, false>;
+    default: return swap_in_kernel<8, G, false>;
   }
 }
 
@@ -1007,8 +1016,9 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
 
   int items = 1;
   while (items * kThreads < a->hot_size) items *= 2;
-  KernelFn fn = G == 16 ? pick_items<16>(items)
-                        : (G == 4 ? pick_items<4>(items) : pick_items<1>(items));
+  const bool tables = a->src_bt != nullptr || a->res_bt != nullptr;
+  KernelFn fn = G == 16 ? pick_items<16>(items, tables)
+                        : (G == 4 ? pick_items<4>(items, tables) : pick_items<1>(items, tables));
   err = ensure_smem(fn, dev.device, L.total);
   if (err != HS_OK) return err;
 
