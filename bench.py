@@ -216,6 +216,7 @@ class SwapInWorkload:
 
         self.hs = hs
         self.overlap = True
+        self.tables = {}  # optional block tables passed to every call
         self.cfg, self.dev, self.layers = cfg, dev, layers
         B, H, S, L = cfg.batch, cfg.hot_size, cfg.row_bytes, cfg.seq_len
         self.n_pools = n_pools or layers
@@ -276,7 +277,7 @@ class SwapInWorkload:
             pool_k=self.pools[l % self.n_pools], hot_k=self.hot[l],
             out_rows=self.out[l] if out is None else out,
             miss_count=self.miss[l] if miss is None else miss, stats=self.stats,
-            overlap_prev=self.overlap and l > 0)
+            overlap_prev=self.overlap and l > 0, **self.tables)
 
     def eager_step(self, topk, stream):
         for l in range(self.layers):
@@ -585,10 +586,14 @@ def run_host_link_peak(dev, stream, pinned):
                               "cudaMemcpyAsync; measured in this run")
 
 
-def run_swapin_cfg(cfg, dev, stream, steps, hbm_peak, link_peak, flush=None, shared_pool=False):
-    """A single-layer swap-in workload timed as graphs of one launch per step."""
+def run_swapin_cfg(cfg, dev, stream, steps, hbm_peak, link_peak, flush=None, shared_pool=False,
+                   tables=None):
+    """A single-layer swap-in workload timed as graphs of one launch per step;
+    ``tables(w)`` may return block tables passed to every call."""
     B, K, H, S = cfg.batch, cfg.top_k, cfg.hot_size, cfg.row_bytes
     w = SwapInWorkload(cfg, dev, 1, 0, pool_host=cfg.pool_in_host, shared_pool=shared_pool)
+    if tables is not None:
+        w.tables = tables(w)
     with torch.cuda.stream(stream):
         for _ in range(cfg.warm_steps):
             w.eager_step(w.next_topk(), stream)
@@ -619,10 +624,36 @@ def run_swapin_cfg(cfg, dev, stream, steps, hbm_peak, link_peak, flush=None, sha
     else:
         res["roofline"] = dict(bound="hbm", achieved=alg / t / 1e9, peak=hbm_peak,
                                frac=alg / t / 1e9 / hbm_peak, unit="GB/s")
+    if tables is not None:  # invalidate each row's newest token, as after a KV write
+        hs = w.hs
+        rows_ = w.req.to(torch.int64)
+        toks = torch.full((B,), cfg.seq_len - 1, dtype=torch.int32, device=dev)
+        fn = lambda: hs.invalidate_tokens(w.tokens[0], rows_, toks, hot_size=H,  # noqa: E731
+                                          stream=stream)
+        fn()
+        res["invalidate_us_per_call"] = time_launches(fn, 20, stream, flush) * 1e6 \
+            if flush is not None else None
     del graphs
     w.free()
     torch.cuda.empty_cache()
     return res
+
+
+def dsv32_block_tables(w, bs=64, recent=4096):
+    """Block tables for the DeepSeek-V3.2 layer: token blocks of 64 map to the pool
+    blocks that pool_rows uses, shifted by one so that no live block is the null
+    block 0 (the last block of the last row wraps onto it and is unmapped); the
+    last `recent` tokens of every request sit in resident device blocks."""
+    cfg, dev = w.cfg, w.dev
+    B, L = cfg.batch, cfg.seq_len
+    nb = L // bs
+    blocks = torch.arange(B * nb, device=dev, dtype=torch.int64)
+    src = ((blocks + 1) % (B * nb)).view(B, nb).to(torch.int32)
+    res = torch.full((B, nb), -1, dtype=torch.int32, device=dev)
+    nr = recent // bs
+    res[:, nb - nr:] = torch.arange(B * nr, device=dev, dtype=torch.int32).view(B, nr)
+    return dict(src_block_table=src, src_block_size=bs, res_block_table=res,
+                res_block_size=bs, res_null_block=-1)
 
 
 def run_transfer(dev, stream, link_peak, hot_rows_target):
@@ -832,6 +863,15 @@ def main():
                                                 link["peak_gbs"])
         ops["stress_swap_in"] = run_swapin_cfg(synth.STRESS, dev, s, 10, hbm_peak,
                                                link["peak_gbs"])
+        one = run_swapin_cfg(synth.DSV32, dev, s, 30, hbm_peak, None, flush=flush)
+        one["workload"] += " [one layer; L2 flushed before each launch]"
+        ops["dsv32_layer_swap_in"] = one
+        tb = run_swapin_cfg(synth.DSV32, dev, s, 30, hbm_peak, None, flush=flush,
+                            tables=dsv32_block_tables)
+        tb["workload"] += (" [one layer; source block table of 64-token blocks, resident "
+                           "table for each request's last 4096 tokens; L2 flushed before "
+                           "each launch]")
+        ops["tables_swap_in"] = tb
         ops["transfer_all_layer"] = run_transfer(dev, s, link["peak_gbs"],
                                                  synth.STRESS.batch * (synth.STRESS.hot_size + 1))
 
