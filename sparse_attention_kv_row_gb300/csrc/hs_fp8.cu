@@ -75,6 +75,93 @@ __host__ __device__ constexpr int chunk_elems() {
   return kDtype == HS_DT_F32 ? 4 : 8;
 }
 
+// Converts one 16-byte input chunk and stores its E codes at d.
+template <int kDtype>
+__device__ __forceinline__ void convert_store(uint4 raw, float sc, bool scaled, unsigned char* d) {
+  constexpr int E = chunk_elems<kDtype>();
+  float x[E];
+  if constexpr (kDtype == HS_DT_F32) {
+    x[0] = __uint_as_float(raw.x);
+    x[1] = __uint_as_float(raw.y);
+    x[2] = __uint_as_float(raw.z);
+    x[3] = __uint_as_float(raw.w);
+  } else {
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint16_t lo = static_cast<uint16_t>(w[i] & 0xFFFF);
+      const uint16_t hi = static_cast<uint16_t>(w[i] >> 16);
+      if constexpr (kDtype == HS_DT_F16) {
+        x[2 * i] = __half2float(__ushort_as_half(lo));
+        x[2 * i + 1] = __half2float(__ushort_as_half(hi));
+      } else {
+        x[2 * i] = __uint_as_float(static_cast<uint32_t>(lo) << 16);
+        x[2 * i + 1] = __uint_as_float(static_cast<uint32_t>(hi) << 16);
+      }
+    }
+  }
+  if (scaled) {
+#pragma unroll
+    for (int i = 0; i < E; ++i) x[i] = x[i] * sc;  // one fp32 multiply per element
+  }
+  if constexpr (E == 8) {
+    uint2 o;
+    o.x = static_cast<uint32_t>(e4m3x2(x[0], x[1])) |
+          (static_cast<uint32_t>(e4m3x2(x[2], x[3])) << 16);
+    o.y = static_cast<uint32_t>(e4m3x2(x[4], x[5])) |
+          (static_cast<uint32_t>(e4m3x2(x[6], x[7])) << 16);
+    *reinterpret_cast<uint2*>(d) = o;
+  } else {
+    *reinterpret_cast<uint32_t*>(d) = static_cast<uint32_t>(e4m3x2(x[0], x[1])) |
+                                      (static_cast<uint32_t>(e4m3x2(x[2], x[3])) << 16);
+  }
+}
+
+// Rows whose heads are contiguous in the input and in the cache: one warp per
+// (token, K|V), the token's slot computed once, every lane moving 16-byte
+// chunks of the [heads x dim] row.  p.chunks = chunks per row, p.units =
+// tokens x (1 + has_v).
+template <int kDtype>
+__global__ void __launch_bounds__(kFp8Threads) fp8_row_kernel(const Fp8Params p) {
+  constexpr int E = chunk_elems<kDtype>();
+  constexpr int U = 4;  // chunks per lane in flight
+  const int lane = threadIdx.x & 31;
+  const float inv_k = p.scale[0] != nullptr ? 1.0f / __ldg(p.scale[0]) : 1.0f;
+  const float inv_v = p.scale[1] != nullptr ? 1.0f / __ldg(p.scale[1]) : 1.0f;
+  const uint32_t kvn = p.rows_per_tok / p.heads;  // 1 (K only) or 2
+  const uint32_t warps = gridDim.x * (kFp8Threads / kWarp);
+  for (uint32_t u = blockIdx.x * (kFp8Threads / kWarp) + (threadIdx.x >> 5); u < p.units;
+       u += warps) {
+    const bool is_v = kvn == 2 && (u & 1u);
+    const int64_t t = p.t_begin + (kvn == 2 ? (u >> 1) : u);
+    const int64_t L = __ldg(p.loc + t);
+    if (L < 0 || L >= p.num_slots) {
+      if (!is_v && lane == 0 && p.status) atomicOr(p.status, HS_ST_BAD_INDEX);
+      continue;
+    }
+    const int64_t page = div_any(static_cast<uint32_t>(L), p.div_page);
+    const int64_t off = L - page * p.page_size;
+    const unsigned char* src = (is_v ? p.in[1] : p.in[0]) +
+                               t * (is_v ? p.stride_token[1] : p.stride_token[0]);
+    unsigned char* dst = (is_v ? p.cache[1] : p.cache[0]) + page * p.c_page + off * p.c_off;
+    const float sc = is_v ? inv_v : inv_k;
+    const bool scaled = (is_v ? p.scale[1] : p.scale[0]) != nullptr;
+    for (uint32_t c0 = lane; c0 < p.chunks; c0 += kWarp * U) {
+      uint4 raw[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + j * kWarp;
+        if (c < p.chunks) raw[j] = ld_stream_v4(src + static_cast<int64_t>(c) * 16);
+      }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + j * kWarp;
+        if (c < p.chunks) convert_store<kDtype>(raw[j], sc, scaled, dst + static_cast<int64_t>(c) * E);
+      }
+    }
+  }
+}
+
 // kVec: 16-byte input chunks and 8- or 4-byte stores (host checked the
 // alignment); otherwise one element per unit.
 template <int kDtype, bool kVec>
@@ -143,42 +230,7 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_store_kernel(const Fp8Params 
       if constexpr (!kVec) {
         *d = static_cast<unsigned char>(e4m3x2(scaled ? x1[j] * sc : x1[j], 0.0f) & 0xFF);
       } else {
-        float x[E];
-        if constexpr (kDtype == HS_DT_F32) {
-          x[0] = __uint_as_float(raw[j].x);
-          x[1] = __uint_as_float(raw[j].y);
-          x[2] = __uint_as_float(raw[j].z);
-          x[3] = __uint_as_float(raw[j].w);
-        } else {
-          const uint32_t w[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint16_t lo = static_cast<uint16_t>(w[i] & 0xFFFF);
-            const uint16_t hi = static_cast<uint16_t>(w[i] >> 16);
-            if constexpr (kDtype == HS_DT_F16) {
-              x[2 * i] = __half2float(__ushort_as_half(lo));
-              x[2 * i + 1] = __half2float(__ushort_as_half(hi));
-            } else {
-              x[2 * i] = __uint_as_float(static_cast<uint32_t>(lo) << 16);
-              x[2 * i + 1] = __uint_as_float(static_cast<uint32_t>(hi) << 16);
-            }
-          }
-        }
-        if (scaled) {
-#pragma unroll
-          for (int i = 0; i < E; ++i) x[i] = x[i] * sc;  // one fp32 multiply per element
-        }
-        if constexpr (E == 8) {
-          uint2 o;
-          o.x = static_cast<uint32_t>(e4m3x2(x[0], x[1])) |
-                (static_cast<uint32_t>(e4m3x2(x[2], x[3])) << 16);
-          o.y = static_cast<uint32_t>(e4m3x2(x[4], x[5])) |
-                (static_cast<uint32_t>(e4m3x2(x[6], x[7])) << 16);
-          *reinterpret_cast<uint2*>(d) = o;
-        } else {
-          *reinterpret_cast<uint32_t*>(d) = static_cast<uint32_t>(e4m3x2(x[0], x[1])) |
-                                            (static_cast<uint32_t>(e4m3x2(x[2], x[3])) << 16);
-        }
+        convert_store<kDtype>(raw[j], sc, scaled, d);
       }
     }
   }
@@ -265,7 +317,31 @@ extern "C" hs_err hs_fp8_store_kv(const void* k, const void* v, int32_t in_dtype
                        static_cast<uint32_t>(page_size)};
   p.status = status;
   using Fn = void (*)(const Fp8Params);
+  // Heads contiguous in the input and in the cache: one warp per (token, K|V) row.
+  const bool rows = vec && k_stride_head == head_dim && (!v || v_stride_head == head_dim) &&
+                    cache_stride_head == head_dim;
   Fn fn;
+  if (rows) {
+    p.chunks = static_cast<uint32_t>(static_cast<int64_t>(num_kv_heads) * head_dim / E);
+    fn = in_dtype == HS_DT_F32 ? fp8_row_kernel<HS_DT_F32>
+                               : (in_dtype == HS_DT_F16 ? fp8_row_kernel<HS_DT_F16>
+                                                        : fp8_row_kernel<HS_DT_BF16>);
+    for (int64_t begin = 0; begin < n_tokens; begin += (1ll << 30)) {
+      const int64_t nt = (n_tokens - begin) < (1ll << 30) ? (n_tokens - begin) : (1ll << 30);
+      p.t_begin = begin;
+      p.units = static_cast<uint32_t>(nt * kv);
+      int64_t blocks = (static_cast<int64_t>(p.units) + kFp8Threads / kWarp - 1) /
+                       (kFp8Threads / kWarp);
+      const int64_t cap = static_cast<int64_t>(dev.sm_count) * kFp8BlocksPerSm;
+      if (blocks > cap) blocks = cap;
+      fn<<<static_cast<unsigned>(blocks), kFp8Threads, 0,
+           reinterpret_cast<cudaStream_t>(stream)>>>(p);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess)
+        return fail(HS_ERR_CUDA, "hs_fp8_store_kv launch: %s", cudaGetErrorString(e));
+    }
+    return HS_OK;
+  }
   if (in_dtype == HS_DT_F32)
     fn = vec ? fp8_store_kernel<HS_DT_F32, true> : fp8_store_kernel<HS_DT_F32, false>;
   else if (in_dtype == HS_DT_F16)

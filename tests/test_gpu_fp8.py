@@ -46,16 +46,19 @@ def _specials(n, rng):
     return np.resize(base, n) * np.where(rng.random(n) < 0.5, 1, 1).astype(np.float32)
 
 
-def _run(dev, dtype, paged, scaled, T, Hh, D, ps, pages, with_v=True, specials=False, seed=0):
+def _run(dev, dtype, paged, scaled, T, Hh, D, ps, pages, with_v=True, specials=False, seed=0,
+         head_step=1):
     hs = _hs()
     rng = np.random.default_rng(seed)
-    x = (rng.standard_normal((T, 2 * Hh + 1, D)) * 40).astype(np.float32)
+    x = (rng.standard_normal((T, 2 * Hh * head_step + 1, D)) * 40).astype(np.float32)
     if specials:
         flat = x.reshape(-1)
         idx = rng.choice(flat.size, size=flat.size // 3, replace=False)
         flat[idx] = _specials(idx.size, rng)
     xt = torch.from_numpy(x).to(TORCH_DT[dtype]).to(dev)
-    k, v = xt[:, :Hh], xt[:, Hh + 1:]  # strided head views of one buffer
+    # views of one buffer; head_step 2 spaces the heads out (head stride != dim)
+    k = xt[:, : Hh * head_step : head_step]
+    v = xt[:, Hh * head_step + 1:: head_step][:, :Hh]
     shape = (pages, ps, Hh, D) if paged else (pages * ps, Hh, D)
     kc = rng.integers(0, 256, shape, dtype=np.uint8)
     vc = rng.integers(0, 256, shape, dtype=np.uint8)
@@ -88,6 +91,12 @@ def _run(dev, dtype, paged, scaled, T, Hh, D, ps, pages, with_v=True, specials=F
 @pytest.mark.parametrize("paged,scaled", [(True, True), (False, False), (True, False)])
 def test_fp8_store_parity(dev, dtype, paged, scaled):
     _run(dev, dtype, paged, scaled, T=300, Hh=8, D=128, ps=16, pages=40, seed=hash(dtype) % 97)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_fp8_store_chunk_path_spaced_heads(dev, dtype):
+    """Heads not contiguous in the input: the per-chunk kernel instead of the row kernel."""
+    _run(dev, dtype, True, True, T=120, Hh=4, D=64, ps=8, pages=30, seed=21, head_step=2)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
