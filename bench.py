@@ -824,6 +824,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: fewer layers than the workload's 61")
+    ap.add_argument("--op", choices=["store_kv", "fp8_store_kv"], default=None,
+                    help="profiling only: run this one secondary line and print it")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -868,6 +870,13 @@ def main():
         torch.distributed.barrier()
         __graft_entry__.build()
     hbm_peak, peak_src = peaks()
+
+    if args.op is not None:  # one secondary line on its own (for ncu)
+        s_ = torch.cuda.Stream(dev)
+        flush_ = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        fn_ = run_store_kv if args.op == "store_kv" else run_fp8_store
+        print(json.dumps({args.op: fn_(dev, hbm_peak, flush_, s_)}), flush=True)
+        return
 
     h = run_headline(args, dev, rank, world, dist)
     t_dev = h["t_dev"]
