@@ -277,7 +277,7 @@ class SwapInWorkload:
             pool_k=self.pools[l % self.n_pools], hot_k=self.hot[l],
             out_rows=self.out[l] if out is None else out,
             miss_count=self.miss[l] if miss is None else miss, stats=self.stats,
-            overlap_prev=self.overlap and l > 0, **self.tables)
+            overlap_prev=self.overlap and l > 0, max_seq_len=self.cfg.seq_len, **self.tables)
 
     def eager_step(self, topk, stream):
         for l in range(self.layers):
@@ -479,7 +479,7 @@ def run_shared_index(w, args, stream, group=4):
                 slot_rows=w.rows[g], lru=w.lru[g], pool_rows=w.pool_rows[g],
                 pool_k=w.pools[g % w.n_pools], hot_k=w.hot[g], out_rows=w.out[g],
                 miss_count=misses[k, gi], stats=w.stats, miss_src=src, miss_dst=dst,
-                overlap_prev=g > 0)
+                overlap_prev=g > 0, max_seq_len=cfg.seq_len)
             argv.append((gi, g, a))
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=stream):

@@ -115,6 +115,10 @@ typedef enum hs_err {
  *  miss_src    int64 [batch, >=top_k] or NULL  stride plan_stride  } the miss plan,
  *  miss_dst    int32 [batch, >=top_k] or NULL  stride plan_stride  } for replay by
  *  miss_mask   int32 [batch, >=top_k] or NULL  stride mask_stride  } hs_gather_misses
+ *  max_seq_len 0 (unknown) or a bound on the sequence lengths: a row with
+ *              seq_lens[b] > max_seq_len emits -1 with HS_ST_BAD_STATE and
+ *              changes no state.  A bound lets the library use a more compact
+ *              request hash (faster); results are the same.
  *  src_bt      int32 [num_states, >=src_bt_blocks] or NULL   source block table
  *  res_bt      int32 [num_states, >=res_bt_blocks] or NULL   resident block table
  *
@@ -177,6 +181,7 @@ typedef struct hs_swap_in_args {
   const int32_t* src_bt; int64_t src_bt_stride; int32_t src_bt_blocks; int32_t src_block_size;
   const int32_t* res_bt; int64_t res_bt_stride; int32_t res_bt_blocks; int32_t res_block_size;
   int32_t res_null_block;
+  int64_t max_seq_len; /* 0, or a bound on every seq_lens[b] (lets the library pack its hash) */
 } hs_swap_in_args;
 
 hs_err hs_swap_in(const hs_swap_in_args* args, hs_stream_t stream);
@@ -342,7 +347,7 @@ const char* hs_status_string(int32_t bit);
 const char* hs_last_error(void);
 
 /* ABI version of this header. */
-#define HS_ABI_VERSION 3
+#define HS_ABI_VERSION 4
 int32_t hs_abi_version(void);
 
 #ifdef __cplusplus

@@ -53,6 +53,7 @@ class _SwapInArgs(C.Structure):
         ("src_block_size", C.c_int32),
         ("res_bt", C.c_void_p), ("res_bt_stride", C.c_int64), ("res_bt_blocks", C.c_int32),
         ("res_block_size", C.c_int32), ("res_null_block", C.c_int32),
+        ("max_seq_len", C.c_int64),
     ]
 
 
@@ -118,7 +119,7 @@ def swap_in(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_
             pool_k, hot_k, out_rows, hot_size, pool_v=None, hot_v=None, num_real=-1,
             miss_count=None, stats=None, status=None, miss_src=None, miss_dst=None,
             miss_mask=None, src_block_table=None, src_block_size=1, res_block_table=None,
-            res_block_size=1, res_null_block=-1, mutant: int = 0) -> None:
+            res_block_size=1, res_null_block=-1, max_seq_len=0, mutant: int = 0) -> None:
     """One swap-in call over B batch rows; mutates slot_tokens, lru, hot_k/hot_v,
     out_rows and the optional outputs in place (all numpy, host memory).
 
@@ -186,7 +187,8 @@ def swap_in(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, lru, pool_
         res_bt=_ptr(res_block_table),
         res_bt_stride=_row_stride(res_block_table) if res_block_table is not None else 0,
         res_bt_blocks=res_block_table.shape[1] if res_block_table is not None else 0,
-        res_block_size=res_block_size, res_null_block=res_null_block)
+        res_block_size=res_block_size, res_null_block=res_null_block,
+        max_seq_len=max_seq_len)
     if pool_rows is None and src_block_table is None:
         raise ValueError("need pool_rows or src_block_table")
     rc = load(mutant).hso_swap_in(C.byref(a))

@@ -110,6 +110,11 @@ void swap_in_row(const hso_swap_in_args* a, int32_t b) {
     return;
   }
   const int64_t Lb = a->seq_lens[b];
+  if (a->max_seq_len > 0 && Lb > a->max_seq_len) {  // outside the caller's bound
+    pad_row(a, b);
+    if (a->status) a->status[b] = HSO_ST_BAD_STATE;
+    return;
+  }
   int32_t* tokens = a->slot_tokens + r * a->slot_tokens_stride;
   const int32_t* rows = a->slot_rows + r * a->slot_rows_stride;
   int16_t* lru = a->lru + r * a->lru_stride;

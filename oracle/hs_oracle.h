@@ -70,6 +70,9 @@ typedef struct hso_swap_in_args {
   const int32_t* src_bt; int64_t src_bt_stride; int32_t src_bt_blocks; int32_t src_block_size;
   const int32_t* res_bt; int64_t res_bt_stride; int32_t res_bt_blocks; int32_t res_block_size;
   int32_t res_null_block;
+  /* 0, or a bound on the sequence lengths: a row with seq_len > max_seq_len is
+   * a bad-state row (-1, miss_count 0, HSO_ST_BAD_STATE, no state change). */
+  int64_t max_seq_len;
 } hso_swap_in_args;
 
 /* Returns 0, or -1 when an argument is unusable (the oracle does not try to

@@ -81,7 +81,7 @@ def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, 
                       num_real=None, miss_count=None, stats=None, status=None,
                       miss_src=None, miss_dst=None, miss_mask=None,
                       src_block_table=None, src_block_size=1, res_block_table=None,
-                      res_block_size=1, res_null_block=-1,
+                      res_block_size=1, res_null_block=-1, max_seq_len=0,
                       overlap_prev=False) -> SwapInArgs:
     """Build a reusable ``hs_swap_in_args`` for these tensors (see include/hisparse.h).
 
@@ -97,7 +97,10 @@ def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, 
 
     ``src_block_table`` (int32 [R, blocks], pool_rows may then be None) maps token t
     to pool row bt[r][t // bs] * bs + t % bs; ``res_block_table`` serves tokens of
-    resident blocks directly (see include/hisparse.h)."""
+    resident blocks directly (see include/hisparse.h).
+
+    ``max_seq_len`` (0 = unknown) bounds every row's sequence length; rows above it
+    report HS_ST_BAD_STATE.  Giving it lets the kernel use its compact hash."""
     H = int(hot_size if hot_size is not None else lru.shape[1])
     _need(topk_ids, torch.int32, "topk_ids", 2)
     _need(out_rows, torch.int32, "out_rows", 2)
@@ -186,7 +189,8 @@ def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, 
         res_bt=_ptr(res_block_table),
         res_bt_stride=res_block_table.stride(0) if res_block_table is not None else 0,
         res_bt_blocks=res_block_table.shape[1] if res_block_table is not None else 0,
-        res_block_size=res_block_size, res_null_block=res_null_block)
+        res_block_size=res_block_size, res_null_block=res_null_block,
+        max_seq_len=int(max_seq_len))
     for t, name in ((miss_src, "miss_src"), (miss_dst, "miss_dst"), (miss_mask, "miss_mask")):
         if t is not None and (t.shape[0] < B or t.shape[1] < K):
             raise ValueError(f"{name} must be at least [batch, top_k]")

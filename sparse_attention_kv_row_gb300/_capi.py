@@ -24,7 +24,7 @@ SEQ_LENS_I64 = 1
 REQ_STATE_I64 = 2
 OVERLAP_PREV = 4
 DT_F32, DT_F16, DT_BF16 = 0, 1, 2
-ABI_VERSION = 3
+ABI_VERSION = 4
 
 # Every symbol include/hisparse.h declares.
 EXPORTS = ("hs_swap_in", "hs_swap_in_smem_bytes", "hs_store_kv", "hs_transfer_kv",
@@ -56,6 +56,7 @@ class SwapInArgs(C.Structure):
         ("src_block_size", C.c_int32),
         ("res_bt", C.c_void_p), ("res_bt_stride", C.c_int64), ("res_bt_blocks", C.c_int32),
         ("res_block_size", C.c_int32), ("res_null_block", C.c_int32),
+        ("max_seq_len", C.c_int64),
     ]
 
 

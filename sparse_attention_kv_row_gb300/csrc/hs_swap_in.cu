@@ -85,7 +85,7 @@ __host__ __device__ inline int take(int* o, int bytes) {
 
 // Hash-table size exponent: the smallest power of two >= mult * K.
 __host__ __device__ inline int hash_bits_for(int K, int mult) {
-  int bits = 1;
+  int bits = 2;  // the wide form keeps at least two pairs
   while ((1 << bits) < mult * K) ++bits;
   return bits;
 }
@@ -100,7 +100,7 @@ __host__ __device__ inline Layout make_layout(int K, int H, int C, int bits) {
   L.slice_e = ((K + C - 1) / C + 31) & ~31;
   const int chunks_p = (H + 31) / 32, chunks_e = (K + 31) / 32;
   int o = 0;
-  L.o_hash = take(&o, 8 * L.hash_size);   // int2 {key, canonical entry}
+  L.o_hash = take(&o, 4 * L.hash_size);   // the request hash (ReqHash)
   L.o_bloom = take(&o, 4 << (kBloomBits - 5));  // one bit per hashed requested id
   L.o_prs = take(&o, 8 * K);              // pool row of each miss candidate (LDGSTS)
   L.o_ids = take(&o, 4 * K + 16);         // staged top-k row
@@ -164,6 +164,9 @@ struct SwapInParams {
   uint32_t chunks_per_row;  // row_bytes / copy width
   FastDiv div_chunks;
   Layout lay;               // shared-memory layout, computed once on the host
+  int32_t entry_bits;       // bits of a top-k entry index in the packed hash
+  int64_t max_seq_len;      // 0, or a bound on every row's sequence length
+  int32_t copy_width;       // 16, 4 or 1 bytes per copy chunk
 };
 
 enum { kMiscFlags = 0, kMiscRepeat = 1, kMiscSlotRepeat = 2, kMiscHits = 3, kMiscMisses = 4 };
@@ -177,18 +180,88 @@ __device__ __forceinline__ uint32_t bloom_bit(int32_t key) {
   return (static_cast<uint32_t>(key) * 0x85EBCA6Bu) >> (32 - kBloomBits);
 }
 
-// Canonical entry index stored for `key`, or -1 when the key is absent.
-__device__ __forceinline__ int32_t hash_find(const int2* tab, int32_t key, int bits) {
-  const uint32_t mask = (1u << bits) - 1u;
-  uint32_t h = hash_of(key, bits);
-  for (uint32_t n = 0; n <= mask; ++n) {
-    const int2 kv = tab[h];
-    if (kv.x == key) return kv.y;
-    if (kv.x == -1) return -1;
-    h = (h + 1u) & mask;
+// The request hash: valid ids -> their canonical (smallest) top-k entry, by
+// open addressing with linear probing in one shared-memory region of
+// 4 * 2^bits bytes.  Packed form, used when the caller bounds every sequence
+// so that each valid id is below 2^(32 - eb) - 1: 2^bits words
+// `id << eb | entry`.  Wide form otherwise: 2^(bits - 1) pairs {id, entry}.
+// Empty slots are all ones in both forms, so one fill clears either.
+template <bool packed>
+struct ReqHash {
+  uint32_t* w;
+  int bits, eb;
+
+  static constexpr uint32_t kEmpty = 0xFFFFFFFFu;
+  __device__ __forceinline__ int nbits() const { return packed ? bits : bits - 1; }
+  __device__ __forceinline__ uint32_t mask() const { return (1u << nbits()) - 1u; }
+  __device__ __forceinline__ uint32_t first(int32_t key) const { return hash_of(key, nbits()); }
+  __device__ __forceinline__ int2* pairs() const { return reinterpret_cast<int2*>(w); }
+
+  // Inserts (key, i); true when the key was already present.
+  __device__ __forceinline__ bool insert(int32_t key, int32_t i) const {
+    const uint32_t m = mask();
+    uint32_t h = first(key);
+    if (packed) {
+      const uint32_t v = (static_cast<uint32_t>(key) << eb) | i;
+      for (uint32_t n = 0; n <= m; ++n) {
+        const uint32_t old = atomicCAS(&w[h], kEmpty, v);
+        if (old == kEmpty) return false;
+        if ((old >> eb) == static_cast<uint32_t>(key)) return true;
+        h = (h + 1u) & m;
+      }
+      return false;
+    }
+    for (uint32_t n = 0; n <= m; ++n) {
+      const int32_t old = atomicCAS(&pairs()[h].x, -1, key);
+      if (old == -1) {
+        pairs()[h].y = i;
+        return false;
+      }
+      if (old == key) return true;
+      h = (h + 1u) & m;
+    }
+    return false;
   }
-  return -1;
-}
+  // Lowers key's entry to i if i is smaller (the key is present).
+  __device__ __forceinline__ void make_min(int32_t key, int32_t i) const {
+    const uint32_t m = mask();
+    uint32_t h = first(key);
+    for (uint32_t n = 0; n <= m; ++n) {
+      if (packed) {
+        if ((w[h] >> eb) == static_cast<uint32_t>(key)) {
+          atomicMin(&w[h], (static_cast<uint32_t>(key) << eb) | i);
+          return;
+        }
+      } else if (pairs()[h].x == key) {
+        atomicMin(&pairs()[h].y, i);
+        return;
+      }
+      h = (h + 1u) & m;
+    }
+  }
+  // Entry of `key` looked up from slot h on; -1 when absent.
+  __device__ __forceinline__ int32_t find_from(int32_t key, uint32_t h) const {
+    const uint32_t m = mask();
+    if (packed) {
+      const uint32_t emask = (1u << eb) - 1u;
+      for (uint32_t n = 0; n <= m; ++n) {
+        const uint32_t v = w[h];
+        if (v == kEmpty) return -1;
+        if ((v >> eb) == static_cast<uint32_t>(key)) return static_cast<int32_t>(v & emask);
+        h = (h + 1u) & m;
+      }
+      return -1;
+    }
+    for (uint32_t n = 0; n <= m; ++n) {
+      const int2 kv = pairs()[h];
+      if (kv.x == key) return kv.y;
+      if (kv.x == -1) return -1;
+      h = (h + 1u) & m;
+    }
+    return -1;
+  }
+  __device__ __forceinline__ int32_t find(int32_t key) const { return find_from(key, first(key)); }
+};
 
 template <int G>
 struct Chunk;
@@ -243,23 +316,12 @@ __device__ __forceinline__ void copy_rows(const SwapInParams& p, const unsigned 
   }
 }
 
-// Continues a linear probe for `key` after its first slot `h` held another key.
-__device__ __forceinline__ int32_t probe_rest(const int2* tab, int32_t key, uint32_t h,
-                                              uint32_t mask) {
-  for (uint32_t n = 1; n <= mask; ++n) {
-    h = (h + 1u) & mask;
-    const int2 kv = tab[h];
-    if (kv.x == key) return kv.y;
-    if (kv.x == -1) return -1;
-  }
-  return -1;
-}
-
 // IT = LRU positions per thread (position k * 1024 + tid for k < IT); their
 // slot, claimed entry and hit flag stay in registers from P1 to P5, and each
 // phase handles them as batched, independent loads.
 // kTables: the call passes block tables (compiled out of the common case).
-template <int IT, int G, bool kTables>
+// kPacked: the packed request hash (the caller bounds the sequence lengths).
+template <int IT, bool kTables, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x;
@@ -313,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
                          ? __ldg(static_cast<const int64_t*>(p.seq_lens) + b)
                          : static_cast<int64_t>(__ldg(static_cast<const int32_t*>(p.seq_lens) + b));
 
-  if (pad_nr || r < 0 || r >= p.num_states) {  // padding row / bad state row
+  const bool too_long = p.max_seq_len > 0 && Lb > p.max_seq_len;  // outside the caller's bound
+  if (pad_nr || r < 0 || r >= p.num_states || too_long) {  // padding / bad state row
     grid_dep_wait();
     if (!overlap && tid == 0) mbar_wait(bar, 0, kMaxPolls);  // no copy left in flight
     for (int i = e0 + tid; i < e1; i += kThreads) {
@@ -386,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const StagePending pend_tok = stage_edges(tokens_g, 4LL * H, sp_tok, tid);
   const StagePending pend_rows = stage_edges(rows_g, 4LL * (H + 1), sp_rows, tid);
 
-  int2* tab = reinterpret_cast<int2*>(smem + L.o_hash);
+  uint32_t* tab = reinterpret_cast<uint32_t*>(smem + L.o_hash);
   uint32_t* bloom = reinterpret_cast<uint32_t*>(smem + L.o_bloom);
   int64_t* prs = reinterpret_cast<int64_t*>(smem + L.o_prs);
   int32_t* mark = reinterpret_cast<int32_t*>(smem + L.o_mark);
@@ -401,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   int32_t* jdst = reinterpret_cast<int32_t*>(smem + L.o_jdst);
   {
     int4* t4 = reinterpret_cast<int4*>(tab);
-    for (int i = tid; i < L.hash_size / 2; i += kThreads) t4[i] = make_int4(-1, -1, -1, -1);
+    for (int i = tid; i < L.hash_size / 4; i += kThreads) t4[i] = make_int4(-1, -1, -1, -1);
   }
   {  // whole 16-byte words: every region is padded to 16 bytes
     int4* c4 = reinterpret_cast<int4*>(claim);
@@ -518,26 +581,13 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   }
   // Hash the valid ids; only when an id repeats does a second pass make its
   // smallest entry index canonical.
-  const int bits = L.hash_bits;
-  const uint32_t hmask = static_cast<uint32_t>(L.hash_size) - 1u;
+  const ReqHash<kPacked> hsh{tab, L.hash_bits, p.entry_bits};
   for (int i = tid; i < K; i += kThreads) {
     const int32_t t = ids[i];
     if (static_cast<uint32_t>(t) < lim) {
       const uint32_t bb = bloom_bit(t);
       atomicOr(&bloom[bb >> 5], 1u << (bb & 31));
-      uint32_t h = hash_of(t, bits);
-      for (uint32_t n = 0; n <= hmask; ++n) {
-        const int32_t old = atomicCAS(&tab[h].x, -1, t);
-        if (old == -1) {
-          tab[h].y = i;
-          break;
-        }
-        if (old == t) {
-          misc[kMiscRepeat] = 1;  // a repeated id: resolved below
-          break;
-        }
-        h = (h + 1u) & hmask;
-      }
+      if (hsh.insert(t, i)) misc[kMiscRepeat] = 1;  // a repeated id: resolved below
     }
   }
   if (tables) {  // resident ids and ids without a source row are not wanted
@@ -566,16 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   if (misc[kMiscRepeat]) {  // rare
     for (int i = tid; i < K; i += kThreads) {
       const int32_t t = ids[i];
-      if (static_cast<uint32_t>(t) < lim) {
-        uint32_t h = hash_of(t, bits);
-        for (uint32_t n = 0; n <= hmask; ++n) {
-          if (tab[h].x == t) {
-            atomicMin(&tab[h].y, i);
-            break;
-          }
-          h = (h + 1u) & hmask;
-        }
-      }
+      if (static_cast<uint32_t>(t) < lim) hsh.make_min(t, i);
     }
     __syncthreads();
   }
@@ -585,19 +626,25 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     uint32_t bw[IT];
 #pragma unroll
     for (int k = 0; k < IT; ++k) bw[k] = ok[k] ? bloom[bloom_bit(tk[k]) >> 5] : 0u;
-    int2 kv[IT];
 #pragma unroll
-    for (int k = 0; k < IT; ++k) {
-      ok[k] = ok[k] && ((bw[k] >> (bloom_bit(tk[k]) & 31)) & 1u);
-      kv[k] = ok[k] ? tab[hash_of(tk[k], bits)] : make_int2(-1, -1);
-    }
+    for (int k = 0; k < IT; ++k) ok[k] = ok[k] && ((bw[k] >> (bloom_bit(tk[k]) & 31)) & 1u);
+    if constexpr (kPacked) {  // first probes batched, the rare longer chains after
+      uint32_t kv[IT];
 #pragma unroll
-    for (int k = 0; k < IT; ++k) {
-      if (!ok[k]) continue;
-      if (kv[k].x == tk[k])
-        f[k] = kv[k].y;
-      else if (kv[k].x != -1)
-        f[k] = probe_rest(tab, tk[k], hash_of(tk[k], bits), hmask);
+      for (int k = 0; k < IT; ++k) kv[k] = ok[k] ? tab[hsh.first(tk[k])] : ReqHash<true>::kEmpty;
+      const uint32_t emask = (1u << hsh.eb) - 1u;
+#pragma unroll
+      for (int k = 0; k < IT; ++k) {
+        if (!ok[k] || kv[k] == ReqHash<true>::kEmpty) continue;
+        if ((kv[k] >> hsh.eb) == static_cast<uint32_t>(tk[k]))
+          f[k] = static_cast<int32_t>(kv[k] & emask);
+        else
+          f[k] = hsh.find_from(tk[k], (hsh.first(tk[k]) + 1u) & hsh.mask());
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < IT; ++k)
+        if (ok[k]) f[k] = hsh.find(tk[k]);
     }
     if (tables) {  // a resident id or one without a source row is not wanted
 #pragma unroll
@@ -621,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     const int8_t pre = (tables && valid) ? code[i] : 0;
     if (pre == kResident) continue;
     const bool cand = valid && t != newest && pre == 0 && claim[i] == kUnclaimed &&
-                      (!id_repeat || hash_find(tab, t, bits) == i);
+                      (!id_repeat || hsh.find(t) == i);
     if (p.src_bt != nullptr) {
       if (!cand) prs[i] = -1;
     } else if (cand && t < p.pool_rows_cols) {
@@ -679,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       int8_t c;
       if (static_cast<uint32_t>(t) >= lim) {
         c = kInvalid;
-      } else if (id_repeat && hash_find(tab, t, bits) != i) {
+      } else if (id_repeat && hsh.find(t) != i) {
         c = kRepeat;
         my_flags |= HS_ST_DUP_ID;
       } else if (tables && code[i] == kResident) {
@@ -794,27 +841,27 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
 
   // ---- P6: copy my misses' rows.
   const int my_m = (e1 < K ? cnte[e1 >> 5] : M) - my_first_miss;
-  copy_rows<G>(p, p.pool_k, p.hot_k, my_m, jsrc, jdst);
-  if (p.pool_v != nullptr) copy_rows<G>(p, p.pool_v, p.hot_v, my_m, jsrc, jdst);
+  if (p.copy_width == 16) {
+    copy_rows<16>(p, p.pool_k, p.hot_k, my_m, jsrc, jdst);
+    if (p.pool_v != nullptr) copy_rows<16>(p, p.pool_v, p.hot_v, my_m, jsrc, jdst);
+  } else if (p.copy_width == 4) {
+    copy_rows<4>(p, p.pool_k, p.hot_k, my_m, jsrc, jdst);
+    if (p.pool_v != nullptr) copy_rows<4>(p, p.pool_v, p.hot_v, my_m, jsrc, jdst);
+  } else {
+    copy_rows<1>(p, p.pool_k, p.hot_k, my_m, jsrc, jdst);
+    if (p.pool_v != nullptr) copy_rows<1>(p, p.pool_v, p.hot_v, my_m, jsrc, jdst);
+  }
 }
 
 using KernelFn = void (*)(const SwapInParams);
 
-template <int G>
-KernelFn pick_items(int items, bool tables) {
-  if (tables) {
-    switch (items) {
-      case 1: return swap_in_kernel<1, G, true>;
-      case 2: return swap_in_kernel<2, G, true>;
-      case 4: return swap_in_kernel<4, G, true>;
-      default: return swap_in_kernel<8, G, true>;
-    }
-  }
+template <bool kTables, bool kPacked>
+KernelFn pick_items(int items) {
   switch (items) {
-    case 1: return swap_in_kernel<1, G, false>;
-    case 2: return swap_in_kernel<2, G, false>;
-    case 4: return swap_in_kernel<4, G, false>;
-    default: return swap_in_kernel<8, G, false>;
+    case 1: return swap_in_kernel<1, kTables, kPacked>;
+    case 2: return swap_in_kernel<2, kTables, kPacked>;
+    case 4: return swap_in_kernel<4, kTables, kPacked>;
+    default: return swap_in_kernel<8, kTables, kPacked>;
   }
 }
 
@@ -916,6 +963,7 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   if (a->res_bt != nullptr &&
       (a->res_block_size < 1 || a->res_bt_blocks < 0 || a->res_bt_stride < a->res_bt_blocks))
     return fail(HS_ERR_ARG, "hs_swap_in: res_bt needs block size >= 1 and stride >= blocks");
+  if (a->max_seq_len < 0) return fail(HS_ERR_ARG, "hs_swap_in: max_seq_len must be >= 0");
   if (a->num_states < 1 || a->pool_num_rows < 0 || a->hot_num_rows < 0)
     return fail(HS_ERR_ARG, "hs_swap_in: num_states >= 1, pool/hot row counts >= 0");
   if (a->hot_num_rows > INT32_MAX)
@@ -924,12 +972,14 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   DeviceInfo dev;
   hs_err err = current_device(&dev);
   if (err != HS_OK) return err;
-  // A hash table of >= 4K entries (load <= 1/4) keeps probe chains short; fall
-  // back to >= 2K entries where shared memory is tight.
-  int bits = hash_bits_for(a->top_k, 4);
+  // A request hash of >= 8 slots per id in its packed form (load <= 1/8)
+  // keeps probe chains short; smaller where shared memory is tight.
+  int bits = hash_bits_for(a->top_k, 8);
   int C = pick_cluster(a->batch, a->top_k, a->hot_size, bits, dev);
-  if (make_layout(a->top_k, a->hot_size, C, bits).total > dev.max_smem_optin) {
-    bits = hash_bits_for(a->top_k, 2);
+  for (int mult = 4; mult >= 2 && make_layout(a->top_k, a->hot_size, C, bits).total >
+                                       dev.max_smem_optin;
+       mult /= 2) {
+    bits = hash_bits_for(a->top_k, mult);
     C = pick_cluster(a->batch, a->top_k, a->hot_size, bits, dev);
   }
   const Layout L = make_layout(a->top_k, a->hot_size, C, bits);
@@ -1013,12 +1063,20 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   p.chunks_per_row = static_cast<uint32_t>(cpr);
   p.div_chunks = FastDiv{fastdiv_magic(static_cast<uint32_t>(cpr)), static_cast<uint32_t>(cpr)};
   p.lay = L;
+  int eb = 1;  // bits of an entry index (K <= 2^eb)
+  while ((1 << eb) < a->top_k) ++eb;
+  p.entry_bits = eb;
+  p.max_seq_len = a->max_seq_len;
+  p.copy_width = G;
 
   int items = 1;
   while (items * kThreads < a->hot_size) items *= 2;
   const bool tables = a->src_bt != nullptr || a->res_bt != nullptr;
-  KernelFn fn = G == 16 ? pick_items<16>(items, tables)
-                        : (G == 4 ? pick_items<4>(items, tables) : pick_items<1>(items, tables));
+  // The packed hash needs every valid id (< max_seq_len) below 2^(32 - eb) - 1.
+  const bool packed = a->max_seq_len > 0 &&
+                      static_cast<uint64_t>(a->max_seq_len) - 1 < (1ull << (32 - p.entry_bits)) - 1;
+  KernelFn fn = tables ? (packed ? pick_items<true, true>(items) : pick_items<true, false>(items))
+                       : (packed ? pick_items<false, true>(items) : pick_items<false, false>(items));
   err = ensure_smem(fn, dev.device, L.total);
   if (err != HS_OK) return err;
 

@@ -27,6 +27,7 @@ class Case:
     hot_k: np.ndarray       # uint8 [hot_rows, S]
     hot_v: np.ndarray | None
     num_real: int = -1
+    max_seq_len: int = 0  # 0, or a bound on seq_lens (rows above it are bad-state rows)
     tables: dict = dataclasses.field(default_factory=dict)  # block tables (read-only)
 
     @property
@@ -105,7 +106,7 @@ def run_oracle(case: Case, mutant: int = 0, plan: bool = False):
                    pool_rows=case.pool_rows, pool_k=case.pool_k, pool_v=case.pool_v,
                    hot_k=case.hot_k, hot_v=case.hot_v, out_rows=out, hot_size=case.H,
                    num_real=case.num_real, miss_count=miss, stats=stats, status=status,
-                   mutant=mutant, **kw, **case.tables)
+                   mutant=mutant, max_seq_len=case.max_seq_len, **kw, **case.tables)
     if plan:
         return out, miss, status, stats, kw["miss_src"], kw["miss_dst"], kw["miss_mask"]
     return out, miss, status, stats
@@ -166,3 +167,8 @@ def corrupt(rng, case: Case, kinds=("lru_range", "lru_dup", "pool_row", "hot_row
                                                                  1 << 30]))
         elif k == "state" and case.B > 0:
             case.req_state[int(rng.integers(case.B))] = int(rng.choice([-1, R, R + 4]))
+
+
+def oracle_st_bad_state():
+    import oracle
+    return oracle.ST_BAD_STATE

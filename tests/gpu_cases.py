@@ -15,7 +15,9 @@ import sparse_attention_kv_row_gb300 as hs
 
 class GpuCase:
     def __init__(self, case: cases.Case, dev, *, pool_in_host=False, seq_dtype=torch.int64,
-                 req_dtype=torch.int64, num_real_on_device=True):
+                 req_dtype=torch.int64, num_real_on_device=True, seq_bound="auto"):
+        # seq_bound: the max_seq_len passed to the library; "auto" passes the case's
+        # own bound, or its longest sequence when it has none (the compact hash)
         self.case = case
         self.dev = dev
         t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
@@ -34,6 +36,7 @@ class GpuCase:
         self.hot_v = t(case.hot_v) if case.hot_v is not None else None
         self.seq_dtype, self.req_dtype = seq_dtype, req_dtype
         self.num_real_on_device = num_real_on_device
+        self.seq_bound = seq_bound
         self.tables = {k: (t(v) if isinstance(v, np.ndarray) else v)
                        for k, v in case.tables.items()}
 
@@ -60,13 +63,18 @@ class GpuCase:
                    pool_rows=self.pool_rows, pool_k=self.pool_k, pool_v=self.pool_v,
                    hot_k=self.hot_k, hot_v=self.hot_v, out_rows=out, hot_size=c.H,
                    num_real=num_real, miss_count=miss, stats=stats, status=status,
-                   stream=stream, **kw, **self.tables)
+                   stream=stream, max_seq_len=self._bound(), **kw, **self.tables)
         torch.cuda.synchronize()
         res = (out.cpu().numpy(), miss.cpu().numpy(), status.cpu().numpy(),
                stats.cpu().numpy().astype(np.uint64))
         if plan:
             res += tuple(kw[k].cpu().numpy() for k in ("miss_src", "miss_dst", "miss_mask"))
         return res
+
+    def _bound(self):
+        if self.seq_bound != "auto":
+            return int(self.seq_bound)
+        return int(self.case.max_seq_len or max(1, int(np.max(self.case.seq_lens))))
 
     def assert_matches(self, ref: cases.Case, what=""):
         np.testing.assert_array_equal(self.tokens.cpu().numpy(), ref.tokens,

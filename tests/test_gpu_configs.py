@@ -88,7 +88,8 @@ def _run_swapin_config(dev, cfg, steps, *, shared_pool=False, check_every=1, war
         ids = ts.next()
         hs.swap_in(topk_ids=ids, seq_lens=g["seq"], req_state=g["req"], slot_tokens=g["tokens"],
                    slot_rows=g["rows"], lru=g["lru"], pool_rows=g["pool_rows"], pool_k=pool_t,
-                   hot_k=g["hot"], out_rows=out, miss_count=miss, status=status, stats=stats)
+                   hot_k=g["hot"], out_rows=out, miss_count=miss, status=status, stats=stats,
+                   max_seq_len=L)  # as the benchmark launches it
         oracle.swap_in(topk_ids=ids.cpu().numpy(), seq_lens=seq, req_state=req,
                        slot_tokens=tokens, slot_rows=rows, lru=lru, pool_rows=pool_rows,
                        pool_k=pool_np, hot_k=hot, out_rows=r_out, hot_size=H,

@@ -256,3 +256,39 @@ def test_overlap_prev(dev, mode):
             np.testing.assert_array_equal(outs[l].cpu().numpy(), r_out, f"{mode} {step} {l}")
             np.testing.assert_array_equal(miss[l].cpu().numpy(), r_miss)
             gpus[l].assert_matches(refs[l], f"{mode} step {step} layer {l}")
+
+
+def test_wide_hash_long_sequences(dev):
+    """Ids beyond 2^(32 - entry bits) - 1 (here K=2100, so ids >= 2^20 - 1) take the wide
+    {id, entry} form of the request hash; the results match the oracle all the same."""
+    rng = np.random.default_rng(2024)
+    B, K, H, L = 2, 2100, 2300, 1_200_000
+    ref = cases.random_case(rng, B=B, K=K, H=H, S=16, R=B + 1, seq_len=L)
+    ref.seq_lens[1] = 600_000   # this row stays in the packed form
+    g = GpuCase(ref.copy(), dev, seq_bound=0)   # no bound given: the wide form
+    g.case = ref
+    import synth
+    ts = synth.TopkStream(77, 0, B, K, 600_000, 0.7)
+    for step in range(4):
+        ids = ts.next().copy()
+        ids[0] += rng.integers(0, 2, K, dtype=np.int32) * 590_000   # row 0: ids up to ~1.19M
+        step_both(g, ref, ids, f"step {step}", plan=True)
+    step_both(g, ref, cases.random_ids(rng, ref), "mixed", plan=True)
+
+
+def test_sequence_bound(dev):
+    """Rows longer than the caller's max_seq_len are bad-state rows on both sides;
+    the others are resolved with the compact hash."""
+    rng = np.random.default_rng(31)
+    ref = cases.random_case(rng, B=4, K=64, H=200, S=16, R=5, seq_len=2000)
+    ref.seq_lens[2] = 2500
+    ref.max_seq_len = 2200
+    g = GpuCase(ref.copy(), dev)
+    g.case = ref
+    prev = None
+    for step in range(3):
+        ids = cases.random_ids(rng, ref, prev=prev)
+        prev = ids
+        res = step_both(g, ref, ids, f"step {step}", plan=True)
+        out, status = res[0], res[2]
+        assert status[2] == cases.oracle_st_bad_state() and np.all(out[2] == -1)

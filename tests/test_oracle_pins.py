@@ -364,3 +364,25 @@ def test_planted_mistake_is_caught(mutant):
         except AssertionError:
             caught.append(name)
     assert caught, f"mutant {mutant} ({MUTANTS[mutant]}) passed every pin"
+
+
+def test_sequence_bound_makes_bad_state_rows():
+    """A row longer than max_seq_len is rejected exactly like a state row past the
+    table (R7): -1, no miss, HS_ST_BAD_STATE, state untouched; other rows as usual."""
+    rng = np.random.default_rng(12)
+    a = cases.random_case(rng, B=3, K=20, H=50, S=4, R=4, seq_len=400)
+    a.seq_lens[1] = 600
+    b = a.copy()
+    a.max_seq_len = 500
+    b.req_state[1] = 99                        # the reference: a state row past the table
+    before = a.copy()
+    for step in range(3):
+        ids = cases.random_ids(rng, a)
+        a.topk, b.topk = ids, ids.copy()
+        ra, rb = cases.run_oracle(a), cases.run_oracle(b)
+        for x, y in zip(ra, rb):
+            np.testing.assert_array_equal(x, y)
+        assert ra[2][1] == oracle.ST_BAD_STATE
+    r1 = int(before.req_state[1])
+    np.testing.assert_array_equal(a.tokens[r1], before.tokens[r1])
+    np.testing.assert_array_equal(a.lru[r1], before.lru[r1])
