@@ -180,22 +180,31 @@ def test_row_subsets_match_whole_batch(dev):
             assert torch.equal(a, b), f"step {step}"
 
 
-@pytest.mark.parametrize("mode", ["chain", "interleaved", "graph"])
-def test_overlap_prev(dev, mode):
+@pytest.mark.parametrize("mode,shape", [("chain", "small"), ("interleaved", "small"),
+                                        ("graph", "small"), ("chain", "clusters")])
+def test_overlap_prev(dev, mode, shape):
     """HS_OVERLAP_PREV: launches that may start before the preceding kernel
     finishes still match the oracle.  'chain': one kernel writes every layer's
     top-k rows, then the layers' swap-ins run back to back (each may overlap
     the one before); 'interleaved': a kernel writes layer l's top-k rows right
     before layer l's swap-in; 'graph': the chain captured in a CUDA graph.
-    Rows include a padding row and a short sequence (the fast path)."""
+    Rows include a padding row and a short sequence (the fast path).  'small'
+    has no sequence bound (the wide request hash); 'clusters' is the decode
+    shape (32 rows, top-k 2048, hot size 4096: 128 CTAs, so part of each launch
+    starts while the previous one runs) with the bound given (the packed hash),
+    and every row's status must be clean."""
     import sparse_attention_kv_row_gb300 as hs
     import synth
 
     rng = np.random.default_rng(123)
-    NL, B, K, H, L = 4, 5, 300, 1000, 9000
+    if shape == "small":
+        NL, B, K, H, L, bound = 4, 5, 300, 1000, 9000, 0
+    else:
+        NL, B, K, H, L, bound = 3, 32, 2048, 4096, 20000, 20000
     refs, gpus = [], []
     for l in range(NL):
-        ref = cases.random_case(rng, B=B, K=K, H=H, S=132, R=B + 2, seq_len=L)
+        ref = cases.random_case(rng, B=B, K=K, H=H, S=132 if shape == "small" else 16,
+                                R=B + 2, seq_len=L)
         ref.seq_lens[1] = H - 3  # fast path
         ref.num_real = B - 1     # last row is padding
         refs.append(ref)
@@ -208,13 +217,15 @@ def test_overlap_prev(dev, mode):
     topk = dst[big:].view(NL, B, K)
     outs = torch.zeros((NL, B, K), dtype=torch.int32, device=dev)
     miss = torch.zeros((NL, B), dtype=torch.int32, device=dev)
+    status = torch.zeros((NL, B), dtype=torch.int32, device=dev)
     num_real = torch.tensor([B - 1], dtype=torch.int32, device=dev)
     args = [hs.make_swap_in_args(
         topk_ids=topk[l], seq_lens=torch.from_numpy(refs[l].seq_lens).to(dev),
         req_state=torch.from_numpy(refs[l].req_state).to(dev), slot_tokens=gpus[l].tokens,
         slot_rows=gpus[l].rows, lru=gpus[l].lru, pool_rows=gpus[l].pool_rows,
         pool_k=gpus[l].pool_k, hot_k=gpus[l].hot_k, out_rows=outs[l], miss_count=miss[l],
-        num_real=num_real, overlap_prev=True) for l in range(NL)]
+        num_real=num_real, overlap_prev=True, status=status[l], max_seq_len=bound)
+        for l in range(NL)]
     s = torch.cuda.Stream()
 
     def step_chain():
@@ -256,6 +267,8 @@ def test_overlap_prev(dev, mode):
             np.testing.assert_array_equal(outs[l].cpu().numpy(), r_out, f"{mode} {step} {l}")
             np.testing.assert_array_equal(miss[l].cpu().numpy(), r_miss)
             gpus[l].assert_matches(refs[l], f"{mode} step {step} layer {l}")
+        if shape == "clusters":
+            assert int(status.abs().max()) == 0, status.cpu().numpy()
 
 
 def test_wide_hash_long_sequences(dev):
