@@ -293,6 +293,7 @@ hs_err hs_fp8_store_kv(const void* k, const void* v, int32_t in_dtype, int64_t k
  *  slot_tokens  device int32 [num_states, >= hot_size + 1], stride in elements
  *  state_rows   device int64 [n_tokens]; tokens device int32 [n_tokens]
  *  status       device int32 [1] or NULL
+ * Limits: n_tokens * ceil(hot_size / 1024) < 2^31 (else HS_ERR_UNSUPPORTED).
  */
 hs_err hs_invalidate_tokens(int32_t* slot_tokens, int64_t slot_tokens_stride, int32_t hot_size,
                             int64_t num_states, const int64_t* state_rows,

@@ -269,6 +269,10 @@ struct FastDiv {
 __device__ __forceinline__ uint32_t fast_div(uint32_t n, FastDiv f) {
   return static_cast<uint32_t>(__umul64hi(f.magic, static_cast<uint64_t>(n)));
 }
+// floor(n / f.d), also for d == 1 (whose multiplier is not representable).
+__device__ __forceinline__ uint32_t div_any(uint32_t n, FastDiv f) {
+  return f.d == 1 ? n : fast_div(n, f);
+}
 
 }  // namespace hs
 

@@ -64,11 +64,6 @@ __device__ __forceinline__ float load_elem(const unsigned char* p) {
   }
 }
 
-// floor(n / f.d), also for d == 1 (whose multiplier is not representable).
-__device__ __forceinline__ uint32_t div_any(uint32_t n, FastDiv f) {
-  return f.d == 1 ? n : fast_div(n, f);
-}
-
 // Elements per 16-byte chunk.
 template <int kDtype>
 __host__ __device__ constexpr int chunk_elems() {

@@ -212,22 +212,39 @@ __global__ void __launch_bounds__(kMoverThreads) gather_misses_kernel(const Gath
   }
 }
 
-// One block per rewritten token: its threads scan the state row's slots.
-__global__ void __launch_bounds__(256) invalidate_kernel(int32_t* slot_tokens, int64_t stride,
-                                                         int32_t hot_size, int64_t num_states,
-                                                         const int64_t* state_rows,
-                                                         const int32_t* tokens, int32_t* status) {
-  const int64_t q = blockIdx.x;
+// Block (token q, chunk c) scans slots [c * kInvSlots, (c + 1) * kInvSlots) of
+// token q's state row: each thread loads its kInvPer slots first, then clears
+// the ones that hold the token, so a block costs one memory round trip.
+constexpr int kInvThreads = 256;
+constexpr int kInvPer = 4;
+constexpr int kInvSlots = kInvThreads * kInvPer;
+__global__ void __launch_bounds__(kInvThreads) invalidate_kernel(int32_t* slot_tokens, int64_t stride,
+                                                                 int32_t hot_size, int64_t num_states,
+                                                                 const int64_t* state_rows,
+                                                                 const int32_t* tokens,
+                                                                 int32_t* status, int32_t chunks) {
+  const int64_t q = blockIdx.x / chunks;
+  const int64_t c = blockIdx.x - q * chunks;
   const int64_t r = __ldg(state_rows + q);
   const int32_t t = __ldg(tokens + q);
   if (r < 0 || t < 0) return;
   if (r >= num_states) {
-    if (threadIdx.x == 0 && status) atomicOr(status, HS_ST_BAD_INDEX);
+    if (c == 0 && threadIdx.x == 0 && status) atomicOr(status, HS_ST_BAD_INDEX);
     return;
   }
   int32_t* row = slot_tokens + r * stride;
-  for (int s = threadIdx.x; s < hot_size; s += blockDim.x)
-    if (row[s] == t) row[s] = -1;
+  const int64_t s0 = c * kInvSlots + threadIdx.x;
+  int32_t v[kInvPer];
+#pragma unroll
+  for (int u = 0; u < kInvPer; ++u) {
+    const int64_t s = s0 + u * kInvThreads;
+    v[u] = s < hot_size ? row[s] : -1;
+  }
+#pragma unroll
+  for (int u = 0; u < kInvPer; ++u) {
+    const int64_t s = s0 + u * kInvThreads;
+    if (s < hot_size && v[u] == t) row[s] = -1;
+  }
 }
 
 __global__ void __launch_bounds__(512) probe_read_kernel(const uint4* src, int64_t n16,
@@ -433,11 +450,14 @@ extern "C" hs_err hs_invalidate_tokens(int32_t* slot_tokens, int64_t slot_tokens
     return fail(HS_ERR_ARG, "hs_invalidate_tokens: slot_tokens, state_rows and tokens are required");
   if (slot_tokens_stride < static_cast<int64_t>(hot_size) + 1)
     return fail(HS_ERR_ARG, "hs_invalidate_tokens: slot_tokens_stride must be >= hot_size + 1");
-  if (n_tokens > 2147483647)
-    return fail(HS_ERR_UNSUPPORTED, "hs_invalidate_tokens: n_tokens must fit a grid");
-  invalidate_kernel<<<static_cast<unsigned>(n_tokens), 256, 0,
+  const int64_t chunks = (static_cast<int64_t>(hot_size) + kInvSlots - 1) / kInvSlots;
+  if (n_tokens * chunks > 2147483647)
+    return fail(HS_ERR_UNSUPPORTED, "hs_invalidate_tokens: n_tokens * ceil(hot_size / %d) must fit a grid",
+                kInvSlots);
+  invalidate_kernel<<<static_cast<unsigned>(n_tokens * chunks), kInvThreads, 0,
                       reinterpret_cast<cudaStream_t>(stream)>>>(
-      slot_tokens, slot_tokens_stride, hot_size, num_states, state_rows, tokens, status);
+      slot_tokens, slot_tokens_stride, hot_size, num_states, state_rows, tokens, status,
+      static_cast<int32_t>(chunks));
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess)
     return fail(HS_ERR_CUDA, "hs_invalidate_tokens launch: %s", cudaGetErrorString(e));

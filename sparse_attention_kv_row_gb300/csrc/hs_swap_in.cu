@@ -17,14 +17,16 @@
 // the row's LRU order or slot tokens before every CTA has staged them.
 //
 //   P0 stage    the row's LRU order, slot tokens and slot rows into shared
-//               memory with LDGSTS (head and tail bytes asynchronously);
+//               memory by TMA bulk copies completed on an mbarrier (head and
+//               tail bytes through registers); thread 0 alone polls it;
 //   P1 state    check the LRU row is a permutation of the slots (one atomicOr
 //               bitmap pass; a lowest-position pass only if a slot repeats)
 //               and gather each position's slot token into registers;
 //      request  then the top-k row: all valid ids into an open-addressing
-//               table (Knuth multiplicative hash, linear probing, one CAS per
-//               id) and a 16 KB bitmap filter; only when an id repeats does a
-//               second pass make its smallest entry index canonical;
+//               table (Knuth multiplicative hash, linear probing, a thread's
+//               first CASes issued together) and a 16 KB bitmap filter; only
+//               when an id repeats does a second pass make its smallest entry
+//               index canonical;
 //   P2 walk     every position probes its slot's token; the lowest position
 //               holding a wanted token claims the entry (atomicMin);
 //   P3 hits     position-ordered ballot/popc + one warp scan of chunk counts:
@@ -61,6 +63,15 @@ constexpr int kCopyUnroll = 4;
 constexpr int kMaxCluster = 8;
 constexpr int32_t kUnclaimed = INT_MAX;
 constexpr uint32_t kMaxPolls = 1u << 22;  // bounded mbarrier waits
+
+// Waits until the phase of `bar` with the given parity has completed: thread
+// 0 polls (a bounded wait) while the other threads wait at the block barrier,
+// which then makes the staged bytes visible to all of them.  (Threads polling
+// a barrier that is not armed yet would take shared-memory bandwidth from the
+// thread about to arm it.)  False in every thread when the wait ran out.
+__device__ __forceinline__ bool block_wait(uint64_t* bar, uint32_t parity) {
+  return __syncthreads_and(threadIdx.x == 0 ? mbar_wait(bar, parity, kMaxPolls) : 1) != 0;
+}
 
 // Per-entry classification, stored as one byte per top-k entry.
 enum : int8_t {
@@ -161,6 +172,7 @@ struct SwapInParams {
   const int32_t* res_bt;
   int64_t res_bt_stride;
   int32_t res_bt_blocks, res_bs, res_null;
+  FastDiv div_src_bs, div_res_bs;  // dividers by the two block sizes
   uint32_t chunks_per_row;  // row_bytes / copy width
   FastDiv div_chunks;
   Layout lay;               // shared-memory layout, computed once on the host
@@ -218,6 +230,18 @@ struct ReqHash {
         return false;
       }
       if (old == key) return true;
+      h = (h + 1u) & m;
+    }
+    return false;
+  }
+  // Packed form: inserts (key, i) from slot h on; true when the key was already present.
+  __device__ __forceinline__ bool insert_from(int32_t key, int32_t i, uint32_t h) const {
+    const uint32_t m = mask();
+    const uint32_t v = (static_cast<uint32_t>(key) << eb) | i;
+    for (uint32_t n = 0; n < m; ++n) {
+      const uint32_t old = atomicCAS(&w[h], kEmpty, v);
+      if (old == kEmpty) return false;
+      if ((old >> eb) == static_cast<uint32_t>(key)) return true;
       h = (h + 1u) & m;
     }
     return false;
@@ -396,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     if (overlap) stage_ids();
     __syncthreads();  // the barriers' initialisation is visible
     stage_finish(ids, pend_ids);
-    if (!__syncthreads_and(mbar_wait(bar, 0, kMaxPolls))) {
+    if (!block_wait(bar, 0)) {
       if (tid == 0) {
         if (p.status) atomicOr(p.status + b, HS_ST_TIMEOUT);
         mbar_wait(bar, 0, kMaxPolls);
@@ -409,9 +433,10 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       int32_t o = -1;
       if (i < count && t >= 0 && t < Lb) {
         o = __ldg(rows_g + t);
-        if (p.res_bt != nullptr && t / p.res_bs < p.res_bt_blocks) {  // a resident block
-          const int32_t e = __ldg(p.res_bt + r * p.res_bt_stride + t / p.res_bs);
-          if (e >= 0 && e != p.res_null) o = e * p.res_bs + t % p.res_bs;
+        const uint32_t rb = p.res_bt != nullptr ? div_any(t, p.div_res_bs) : 0u;
+        if (p.res_bt != nullptr && rb < static_cast<uint32_t>(p.res_bt_blocks)) {  // a resident block
+          const int32_t e = __ldg(p.res_bt + r * p.res_bt_stride + rb);
+          if (e >= 0 && e != p.res_null) o = e * p.res_bs + (t - static_cast<int32_t>(rb) * p.res_bs);
         }
       }
       out_g[i] = o;
@@ -480,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   stage_finish(lru, pend_lru);
   stage_finish(tok, pend_tok);
   stage_finish(rows, pend_rows);
-  const bool staged = __syncthreads_and(mbar_wait(bar + 1, 0, kMaxPolls));
+  const bool staged = block_wait(bar + 1, 0);
   // Every CTA of the row has staged the state once all have arrived here; the
   // matching wait comes right before the first write to that state.
   cluster_arrive();
@@ -552,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   grid_dep_wait();
   if (overlap) stage_ids();
   stage_finish(ids, pend_ids);
-  if (!__syncthreads_and(mbar_wait(bar, 0, kMaxPolls))) {
+  if (!block_wait(bar, 0)) {
     if (tid == 0) {
       if (p.status) atomicOr(p.status + b, HS_ST_TIMEOUT);
       mbar_wait(bar, 0, kMaxPolls);
@@ -568,12 +593,14 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     for (int i = tid; i < K; i += kThreads) {
       const int32_t t = ids[i];
       if (static_cast<uint32_t>(t) >= lim) continue;
-      if (p.res_bt != nullptr && t / p.res_bs < p.res_bt_blocks)
-        cp_async_4(&tbl[i].x, p.res_bt + r * p.res_bt_stride + t / p.res_bs);
+      const uint32_t rb = p.res_bt != nullptr ? div_any(t, p.div_res_bs) : 0u;
+      if (p.res_bt != nullptr && rb < static_cast<uint32_t>(p.res_bt_blocks))
+        cp_async_4(&tbl[i].x, p.res_bt + r * p.res_bt_stride + rb);
       else
         tbl[i].x = -1;
-      if (p.src_bt != nullptr && t / p.src_bs < p.src_bt_blocks)
-        cp_async_4(&tbl[i].y, p.src_bt + r * p.src_bt_stride + t / p.src_bs);
+      const uint32_t sb = p.src_bt != nullptr ? div_any(t, p.div_src_bs) : 0u;
+      if (p.src_bt != nullptr && sb < static_cast<uint32_t>(p.src_bt_blocks))
+        cp_async_4(&tbl[i].y, p.src_bt + r * p.src_bt_stride + sb);
       else
         tbl[i].y = 0;
     }
@@ -582,12 +609,39 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   // Hash the valid ids; only when an id repeats does a second pass make its
   // smallest entry index canonical.
   const ReqHash<kPacked> hsh{tab, L.hash_bits, p.entry_bits};
-  for (int i = tid; i < K; i += kThreads) {
-    const int32_t t = ids[i];
-    if (static_cast<uint32_t>(t) < lim) {
-      const uint32_t bb = bloom_bit(t);
+  if constexpr (kPacked && IT <= 4) {  // my entries' first probes batched, collisions after
+    int32_t tv[IT];
+    uint32_t h0[IT], old[IT];
+#pragma unroll
+    for (int k = 0; k < IT; ++k) tv[k] = k * kThreads + tid < K ? ids[k * kThreads + tid] : -1;
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      old[k] = ReqHash<true>::kEmpty;
+      if (static_cast<uint32_t>(tv[k]) >= lim) continue;
+      const uint32_t bb = bloom_bit(tv[k]);
       atomicOr(&bloom[bb >> 5], 1u << (bb & 31));
-      if (hsh.insert(t, i)) misc[kMiscRepeat] = 1;  // a repeated id: resolved below
+      h0[k] = hsh.first(tv[k]);
+      old[k] = atomicCAS(&tab[h0[k]], ReqHash<true>::kEmpty,
+                         (static_cast<uint32_t>(tv[k]) << hsh.eb) | (k * kThreads + tid));
+    }
+    bool rep = false;
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      if (old[k] == ReqHash<true>::kEmpty) continue;  // inserted (or not valid)
+      if ((old[k] >> hsh.eb) == static_cast<uint32_t>(tv[k]))
+        rep = true;
+      else
+        rep |= hsh.insert_from(tv[k], k * kThreads + tid, (h0[k] + 1u) & hsh.mask());
+    }
+    if (rep) misc[kMiscRepeat] = 1;  // a repeated id: resolved below
+  } else {
+    for (int i = tid; i < K; i += kThreads) {
+      const int32_t t = ids[i];
+      if (static_cast<uint32_t>(t) < lim) {
+        const uint32_t bb = bloom_bit(t);
+        atomicOr(&bloom[bb >> 5], 1u << (bb & 31));
+        if (hsh.insert(t, i)) misc[kMiscRepeat] = 1;  // a repeated id: resolved below
+      }
     }
   }
   if (tables) {  // resident ids and ids without a source row are not wanted
@@ -600,9 +654,11 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       int64_t row = -1;
       if (p.res_bt != nullptr && e.x >= 0 && e.x != p.res_null) {
         c = kResident;
-        row = static_cast<int64_t>(e.x) * p.res_bs + t % p.res_bs;
+        const int32_t off = t - static_cast<int32_t>(div_any(t, p.div_res_bs)) * p.res_bs;
+        row = static_cast<int64_t>(e.x) * p.res_bs + off;
       } else if (p.src_bt != nullptr && t != newest) {
-        const int64_t g = static_cast<int64_t>(e.y) * p.src_bs + t % p.src_bs;
+        const int32_t off = t - static_cast<int32_t>(div_any(t, p.div_src_bs)) * p.src_bs;
+        const int64_t g = static_cast<int64_t>(e.y) * p.src_bs + off;
         if (e.y <= 0 || g >= p.pool_num_rows)
           c = kUnmapped;
         else
@@ -1059,6 +1115,12 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   p.res_bt_blocks = a->res_bt_blocks;
   p.res_bs = a->res_block_size;
   p.res_null = a->res_null_block;
+  {
+    const uint32_t sbs = a->src_bt != nullptr ? static_cast<uint32_t>(a->src_block_size) : 1u;
+    const uint32_t rbs = a->res_bt != nullptr ? static_cast<uint32_t>(a->res_block_size) : 1u;
+    p.div_src_bs = FastDiv{fastdiv_magic(sbs), sbs};
+    p.div_res_bs = FastDiv{fastdiv_magic(rbs), rbs};
+  }
   p.mask_stride = a->mask_stride;
   p.chunks_per_row = static_cast<uint32_t>(cpr);
   p.div_chunks = FastDiv{fastdiv_magic(static_cast<uint32_t>(cpr)), static_cast<uint32_t>(cpr)};

@@ -68,11 +68,12 @@ def test_tables_multi_tile(dev):
         step_both(g, ref, ts.next(), f"step {step}", plan=True)
 
 
-def test_invalidate_parity(dev):
+@pytest.mark.parametrize("H", [700, 2500])  # one chunk of 1024 slots; three with a ragged tail
+def test_invalidate_parity(dev, H):
     import sparse_attention_kv_row_gb300 as hs
 
-    rng = np.random.default_rng(8)
-    R, H = 9, 700
+    rng = np.random.default_rng(8 + H)
+    R = 9
     tok = rng.integers(-1, 500, (R, H + 4)).astype(np.int32)
     rows = rng.integers(-1, R + 2, 300).astype(np.int64)
     toks = rng.integers(-3, 500, 300).astype(np.int32)
