@@ -389,10 +389,11 @@ def run_headline(args, dev, rank, world, dist):
     w.stats.zero_()
     torch.cuda.synchronize()
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev = lambda: torch.cuda.Event()  # noqa: E731
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     comp_done = [None, None]  # the step that last used buffer i finished computing
     out_done = [None, None]   # ... and its outputs reached the host
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = []  # per step: (compute start, compute end, outputs on the host)
     wall0 = time.perf_counter()
     e0.record(s)
     s_in.wait_event(e0)
@@ -409,6 +410,8 @@ def run_headline(args, dev, rank, world, dist):
             s.wait_event(up)
             if out_done[i] is not None:
                 s.wait_event(out_done[i])  # the buffer's previous outputs have left
+            c0 = ev()
+            c0.record(s)
             g_e2e[i].replay()
             comp_done[i] = ev()
             comp_done[i].record(s)
@@ -418,6 +421,8 @@ def run_headline(args, dev, rank, world, dist):
             miss_host[i].copy_(miss_dev[i], non_blocking=True)
             out_done[i] = ev()
             out_done[i].record(s_out)
+        marks.append((c0, comp_done[i], out_done[i]))
+    enqueue_ms = (time.perf_counter() - wall0) * 1e3
     for d in out_done:
         if d is not None:
             s.wait_event(d)
@@ -425,6 +430,16 @@ def run_headline(args, dev, rank, world, dist):
     torch.cuda.synchronize()
     t_e2e = e0.elapsed_time(e1) / 1e3
     wall_e2e = time.perf_counter() - wall0
+    # where the window went: the steps' compute, the GPU idle between steps, read-backs
+    comp_us = [a.elapsed_time(b) * 1e3 for a, b, _ in marks]
+    idle_us = e0.elapsed_time(marks[0][0]) * 1e3 + sum(
+        marks[k - 1][1].elapsed_time(marks[k][0]) * 1e3 for k in range(1, len(marks)))
+    d2h_us = [b.elapsed_time(c) * 1e3 for _, b, c in marks]
+    e2e_detail = dict(compute_us_per_step_median=statistics.median(comp_us),
+                      compute_us_per_step_max=max(comp_us),
+                      idle_us_between_steps_total=idle_us,
+                      readback_us_median=statistics.median(d2h_us), readback_us_max=max(d2h_us),
+                      host_enqueue_ms=enqueue_ms)
     e2e_misses = int(w.stats[1].item())
     smi_summary = stop_smi(smi, smi_f, smi_path)
 
@@ -446,7 +461,7 @@ def run_headline(args, dev, rank, world, dist):
     alg = swapin_alg_bytes(B, K, H, S, launches, misses)
     res = dict(t_dev=t_dev, hits=hits, misses=misses, launches=launches, alg_bytes=alg,
                n_pools=n_pools, t_e2e=t_e2e, wall_e2e=wall_e2e, e2e_misses=e2e_misses,
-               e2e_steps=n_e2e, h2d=NL * B * K * 4, d2h=NL * B * K * 4 + NL * B * 4,
+               e2e_steps=n_e2e, e2e_detail=e2e_detail, h2d=NL * B * K * 4, d2h=NL * B * K * 4 + NL * B * 4,
                t_seq=t_seq, seq_steps=n_seq, seq_misses=seq_misses, shared=shared,
                clocks=sampler.summary(smi_summary))
     del graphs, g_e2e
@@ -966,7 +981,7 @@ def main():
                           sample=cpu["sample"], cpu=cpu["cpu"], nproc=cpu["nproc"]),
         e2e=dict(value=e2e_all / t_e2e, unit="rows/s", h2d_bytes_per_step=h["h2d"],
                  d2h_bytes_per_step=h["d2h"], steps=h["e2e_steps"],
-                 us_per_step=t_e2e / h["e2e_steps"] * 1e6,
+                 us_per_step=t_e2e / h["e2e_steps"] * 1e6, detail=h["e2e_detail"],
                  how="every step: pinned-host top-k -> device, the step's 61 swap-ins "
                      "(CUDA graph through the C ABI), out rows and miss counts -> pinned host; "
                      "uploads and read-backs on their own streams, double-buffered, so they "
