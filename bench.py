@@ -847,7 +847,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: fewer layers than the workload's 61")
     ap.add_argument("--op", choices=["store_kv", "fp8_store_kv", "dsv32_layer_swap_in",
-                                     "tables_swap_in"], default=None,
+                                     "tables_swap_in", "indexer_swap_in", "stress_swap_in"],
+                    default=None,
                     help="profiling only: run this one secondary line and print it")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -900,6 +901,13 @@ def main():
         if args.op in ("store_kv", "fp8_store_kv"):
             fn_ = run_store_kv if args.op == "store_kv" else run_fp8_store
             out_ = fn_(dev, hbm_peak, flush_, s_)
+        elif args.op in ("indexer_swap_in", "stress_swap_in"):
+            probe_ = torch.empty(2 * GiB, dtype=torch.uint8, pin_memory=True)
+            link_ = run_host_link_peak(dev, s_, probe_)
+            del probe_
+            cfg_ = synth.INDEXER if args.op == "indexer_swap_in" else synth.STRESS
+            out_ = run_swapin_cfg(cfg_, dev, s_, 20 if cfg_ is synth.INDEXER else 10, hbm_peak,
+                                  link_["peak_gbs"])
         else:
             out_ = run_swapin_cfg(synth.DSV32, dev, s_, 30, hbm_peak, None, flush=flush_,
                                   tables=dsv32_block_tables if args.op == "tables_swap_in"
