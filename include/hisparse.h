@@ -348,7 +348,22 @@ const char* hs_status_string(int32_t bit);
 const char* hs_last_error(void);
 
 /* ABI version of this header. */
-#define HS_ABI_VERSION 4
+/*
+ * hs_wait_selftest -- checks that a bounded wait that runs out hands control
+ * back: one block initialises an mbarrier that nothing arms and waits on it
+ * with the swap-in's bounded mbarrier wait (the one behind HS_ST_TIMEOUT, see
+ * hs_swap_in), at most max_polls polls, then ORs HS_ST_TIMEOUT into *status.
+ * No copy is in flight on that barrier, so giving up is safe; the context
+ * stays usable for the calls that follow.  Defined by this library (the
+ * pages bound no waits).
+ *
+ *  max_polls  >= 0 (each poll may suspend the thread briefly; ~1e3 is quick)
+ *  status     device int32 [1], required
+ * Errors: HS_ERR_ARG for max_polls < 0 or a NULL status.
+ */
+hs_err hs_wait_selftest(int32_t max_polls, int32_t* status, hs_stream_t stream);
+
+#define HS_ABI_VERSION 5
 int32_t hs_abi_version(void);
 
 #ifdef __cplusplus

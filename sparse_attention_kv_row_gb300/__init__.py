@@ -24,7 +24,7 @@ from ._capi import (HisparseError, SwapInArgs, ST_BAD_HOT_ROW, ST_BAD_INDEX,  # 
                     ST_BAD_LRU_SLOT, ST_BAD_POOL_ROW, ST_BAD_STATE, ST_DUP_ID, ST_TIMEOUT)
 
 __all__ = ["swap_in", "swap_in_args", "make_swap_in_args", "gather_misses", "fp8_store_kv",
-           "invalidate_tokens",
+           "invalidate_tokens", "wait_selftest",
            "store_kv", "transfer_kv",
            "transfer_kv_layers", "probe_read", "swap_in_smem_bytes", "library_path",
            "HisparseError", "SwapInArgs"]
@@ -224,6 +224,14 @@ def invalidate_tokens(slot_tokens, state_rows, tokens, *, hot_size=None, status=
         _ptr(slot_tokens), slot_tokens.stride(0), H, slot_tokens.shape[0], _ptr(state_rows),
         _ptr(tokens), tokens.numel(), _ptr(status), C.c_void_p(_stream(stream))),
         "hs_invalidate_tokens")
+
+
+def wait_selftest(max_polls, status, *, stream=None) -> None:
+    """Run the bounded mbarrier wait on a barrier that nothing arms (at most
+    max_polls polls); HS_ST_TIMEOUT is OR-ed into ``status`` (int32 [1])."""
+    _need(status, torch.int32, "status", 1)
+    _capi.check(_lib().hs_wait_selftest(int(max_polls), _ptr(status),
+                                        C.c_void_p(_stream(stream))), "hs_wait_selftest")
 
 
 def gather_misses(pool_layers, hot_layers, miss_src, miss_dst, miss_count, *, has_v=False,

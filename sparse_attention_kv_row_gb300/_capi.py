@@ -24,12 +24,12 @@ SEQ_LENS_I64 = 1
 REQ_STATE_I64 = 2
 OVERLAP_PREV = 4
 DT_F32, DT_F16, DT_BF16 = 0, 1, 2
-ABI_VERSION = 4
+ABI_VERSION = 5
 
 # Every symbol include/hisparse.h declares.
 EXPORTS = ("hs_swap_in", "hs_swap_in_smem_bytes", "hs_store_kv", "hs_transfer_kv",
            "hs_gather_misses", "hs_fp8_store_kv", "hs_invalidate_tokens", "hs_probe_read", "hs_err_string", "hs_status_string", "hs_last_error",
-           "hs_abi_version")
+           "hs_abi_version", "hs_wait_selftest")
 
 
 class SwapInArgs(C.Structure):
@@ -110,6 +110,8 @@ def load() -> C.CDLL:
         lib.hs_status_string.restype = C.c_char_p
         lib.hs_last_error.argtypes = []
         lib.hs_last_error.restype = C.c_char_p
+        lib.hs_wait_selftest.argtypes = [i32, vp, vp]
+        lib.hs_wait_selftest.restype = i32
         lib.hs_abi_version.argtypes = []
         lib.hs_abi_version.restype = i32
         if lib.hs_abi_version() != ABI_VERSION:

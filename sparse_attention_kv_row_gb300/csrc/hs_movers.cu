@@ -247,6 +247,19 @@ __global__ void __launch_bounds__(kInvThreads) invalidate_kernel(int32_t* slot_t
   }
 }
 
+// The bounded wait of the swap-in's staging, run on an mbarrier that nothing
+// arms: thread 0 initialises it and polls at most max_polls times, and the
+// block reports the wait that ran out.  No copy is in flight on the barrier.
+__global__ void __launch_bounds__(32) wait_selftest_kernel(uint32_t max_polls, int32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, max_polls)) atomicOr(status, HS_ST_TIMEOUT);
+}
+
 __global__ void __launch_bounds__(512) probe_read_kernel(const uint4* src, int64_t n16,
                                                          unsigned long long* sink) {
   uint32_t acc = 0;
@@ -461,5 +474,18 @@ extern "C" hs_err hs_invalidate_tokens(int32_t* slot_tokens, int64_t slot_tokens
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess)
     return fail(HS_ERR_CUDA, "hs_invalidate_tokens launch: %s", cudaGetErrorString(e));
+  return HS_OK;
+}
+
+extern "C" hs_err hs_wait_selftest(int32_t max_polls, int32_t* status, hs_stream_t stream) {
+  using namespace hs;
+  clear_error();
+  if (max_polls < 0 || status == nullptr)
+    return fail(HS_ERR_ARG, "hs_wait_selftest: needs max_polls >= 0 and a status word");
+  wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint32_t>(max_polls), status);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return fail(HS_ERR_CUDA, "hs_wait_selftest launch: %s", cudaGetErrorString(e));
   return HS_OK;
 }

@@ -123,6 +123,8 @@ def test_movers_reject(lib):
     assert lib.hs_transfer_kv(1, 1, 3, 2, 1, 1, 5, 16, 16, 1, 1, 16, None, None) == 1  # has_v
     assert lib.hs_transfer_kv(1, 1, 3, 0, 1, 1, 5, 8, 16, 1, 1, 16, None, None) == 1  # stride
     assert lib.hs_probe_read(8, 32, 16, None) == 1  # misaligned source
+    assert lib.hs_wait_selftest(-1, 8, None) == 1   # negative poll budget
+    assert lib.hs_wait_selftest(10, None, None) == 1  # no status word
 
 
 def test_smem_bytes(lib):

@@ -305,3 +305,24 @@ def test_sequence_bound(dev):
         res = step_both(g, ref, ids, f"step {step}", plan=True)
         out, status = res[0], res[2]
         assert status[2] == cases.oracle_st_bad_state() and np.all(out[2] == -1)
+
+
+def test_bounded_wait_runs_out_and_context_stays_usable(dev):
+    """A wait that runs out hands control back with HS_ST_TIMEOUT: the library's
+    bounded mbarrier wait on a barrier that nothing arms (no copy in flight).
+    The swap-ins that follow on the same context still match the oracle."""
+    import oracle
+    import sparse_attention_kv_row_gb300 as hs
+
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    hs.wait_selftest(1000, st)
+    torch.cuda.synchronize()
+    assert st.item() == oracle.ST_TIMEOUT
+    rng = np.random.default_rng(31)
+    ref = cases.random_case(rng, B=3, K=40, H=100, S=32)
+    g = GpuCase(ref.copy(), dev)
+    prev = None
+    for step in range(3):
+        ids = cases.random_ids(rng, ref, prev=prev)
+        prev = ids
+        step_both(g, ref, ids, f"after the timeout, step {step}")
