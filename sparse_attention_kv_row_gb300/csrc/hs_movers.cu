@@ -181,34 +181,96 @@ struct GatherParams {
   const int32_t* miss_count;
   int32_t top_k;
   int32_t* status;
+  uint32_t chunks16;   // row_bytes / 16 when row_bytes is a multiple of 16, else 0
+  FastDiv div_chunks16;
+  FastDiv div_ptr_pairs;
 };
 
-// Block (row, y): warp w takes units u = y*W + w, y*W + w + gridDim.y*W, ...
-// with u = miss * ptr_pairs + pointer pair, below the row's miss count.
-__global__ void __launch_bounds__(kMoverThreads) gather_misses_kernel(const GatherParams p) {
+constexpr int kGatherUnits = 256;  // (miss, pointer pair) units a block stages per round
+constexpr int kGatherBlocksPerSm = 4;  // resident blocks of the replay (<= 64 registers)
+constexpr int kGatherUnroll = 4;       // 16-byte chunks in flight per thread
+
+// Block (row, y) replays misses [y*mb, (y+1)*mb) of its row, mb = ceil(n /
+// gridDim.y): units u = (miss - first miss) * ptr_pairs + pointer pair, in
+// rounds of kGatherUnits.  A round first stages each unit's source and
+// destination row addresses in shared memory (its plan entries and layer
+// pointers are independent loads: one round trip), then copies them: as flat
+// (unit, 16-byte chunk) items, kGatherUnroll per thread with all loads before
+// the stores, when every staged unit is 16-byte aligned; else one warp per unit.
+__global__ void __launch_bounds__(kMoverThreads, kGatherBlocksPerSm)
+    gather_misses_kernel(const GatherParams p) {
   constexpr int W = kMoverThreads / kWarp;
+  __shared__ const unsigned char* s_src[kGatherUnits];
+  __shared__ unsigned char* s_dst[kGatherUnits];
+  __shared__ int s_unaligned;
   // The next launch may start now: it reads nothing this kernel writes before
   // its own grid-dependency wait.
   grid_dep_launch_dependents();
-  const int lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
   const int64_t row = blockIdx.x;
   int n = __ldg(p.miss_count + row);
   n = n < 0 ? 0 : (n > p.top_k ? p.top_k : n);
-  const uint32_t units = static_cast<uint32_t>(n) * p.ptr_pairs;
-  for (uint32_t u = blockIdx.y * W + (threadIdx.x >> 5); u < units; u += gridDim.y * W) {
-    const uint32_t m = u / p.ptr_pairs;
-    const uint32_t pp = u - m * p.ptr_pairs;
-    const int32_t d = __ldg(p.miss_dst + row * p.plan_stride + m);
-    if (d < 0) continue;  // this miss was given no hot row
-    const int64_t s = __ldg(p.miss_src + row * p.plan_stride + m);
-    if (s < 0 || s >= p.pool_rows || d >= p.hot_rows) {
-      if (lane == 0 && pp == 0 && p.status) atomicOr(p.status, HS_ST_BAD_INDEX);
-      continue;
+  const uint32_t mb = (static_cast<uint32_t>(n) + gridDim.y - 1) / gridDim.y;
+  const uint32_t m0 = blockIdx.y * mb;
+  const uint32_t m1 = m0 + mb < static_cast<uint32_t>(n) ? m0 + mb : static_cast<uint32_t>(n);
+  const uint32_t units = m1 > m0 ? (m1 - m0) * p.ptr_pairs : 0u;
+  const int64_t* src_g = p.miss_src + row * p.plan_stride;
+  const int32_t* dst_g = p.miss_dst + row * p.plan_stride;
+  for (uint32_t u0 = 0; u0 < units; u0 += kGatherUnits) {
+    const int nu = units - u0 < kGatherUnits ? static_cast<int>(units - u0) : kGatherUnits;
+    if (tid == 0) s_unaligned = 0;
+    __syncthreads();  // the previous round's copies are done with the staged units
+    if (tid < nu) {
+      const uint32_t u = u0 + tid;
+      const uint32_t k = p.ptr_pairs == 1 ? u : fast_div(u, p.div_ptr_pairs);
+      const uint32_t pp = u - k * p.ptr_pairs;
+      const int32_t d = __ldg(dst_g + m0 + k);
+      const int64_t sr = __ldg(src_g + m0 + k);
+      const uintptr_t pool = static_cast<uintptr_t>(__ldg(p.pool_ptrs + pp));
+      const uintptr_t hot = static_cast<uintptr_t>(__ldg(p.hot_ptrs + pp));
+      const unsigned char* from = nullptr;
+      unsigned char* to = nullptr;
+      if (d >= 0) {  // a miss given no hot row is skipped
+        if (sr < 0 || sr >= p.pool_rows || d >= p.hot_rows) {
+          if (pp == 0 && p.status) atomicOr(p.status, HS_ST_BAD_INDEX);
+        } else {
+          from = reinterpret_cast<const unsigned char*>(pool) + sr * p.row_bytes;
+          to = reinterpret_cast<unsigned char*>(hot) + static_cast<int64_t>(d) * p.row_bytes;
+          if (((reinterpret_cast<uintptr_t>(from) | reinterpret_cast<uintptr_t>(to)) & 15) != 0)
+            s_unaligned = 1;
+        }
+      }
+      s_src[tid] = from;
+      s_dst[tid] = to;
     }
-    const unsigned char* src = reinterpret_cast<const unsigned char*>(__ldg(p.pool_ptrs + pp));
-    unsigned char* dst = reinterpret_cast<unsigned char*>(__ldg(p.hot_ptrs + pp));
-    warp_copy_row<true>(dst + static_cast<int64_t>(d) * p.row_bytes, src + s * p.row_bytes,
-                        p.row_bytes, lane);
+    __syncthreads();
+    if (p.chunks16 != 0 && s_unaligned == 0) {
+      const uint32_t items = static_cast<uint32_t>(nu) * p.chunks16;
+      for (uint32_t w0 = tid; w0 < items; w0 += kMoverThreads * kGatherUnroll) {
+        uint4 v[kGatherUnroll];
+        unsigned char* to[kGatherUnroll];
+#pragma unroll
+        for (int j = 0; j < kGatherUnroll; ++j) {
+          const uint32_t w = w0 + j * kMoverThreads;
+          to[j] = nullptr;
+          if (w < items) {
+            const uint32_t k = fast_div(w, p.div_chunks16);
+            const uint32_t off = (w - k * p.chunks16) << 4;
+            const unsigned char* from = s_src[k];
+            if (from != nullptr) {
+              v[j] = ld_stream_v4(from + off);
+              to[j] = s_dst[k] + off;
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kGatherUnroll; ++j)
+          if (to[j] != nullptr) st_l2_v4(to[j], v[j]);
+      }
+    } else {
+      for (int k = tid >> 5; k < nu; k += W)
+        if (s_src[k] != nullptr) warp_copy_row<true>(s_dst[k], s_src[k], p.row_bytes, tid & 31);
+    }
   }
 }
 
@@ -433,11 +495,16 @@ extern "C" hs_err hs_gather_misses(const uint64_t* pool_ptrs, const uint64_t* ho
   p.miss_count = miss_count;
   p.top_k = top_k;
   p.status = status;
+  p.chunks16 = row_bytes % 16 == 0 && row_bytes / 16 < (1ll << 31)
+                   ? static_cast<uint32_t>(row_bytes / 16) : 0u;
+  p.div_chunks16 = FastDiv{fastdiv_magic(p.chunks16 > 0 ? p.chunks16 : 1u),
+                           p.chunks16 > 0 ? p.chunks16 : 1u};
+  p.div_ptr_pairs = FastDiv{fastdiv_magic(p.ptr_pairs), p.ptr_pairs};
   // Enough blocks per row to cover the device even for a few rows, at most
   // one warp per (miss, layer) unit.
   constexpr int W = kMoverThreads / kWarp;
   const int64_t units = static_cast<int64_t>(top_k) * static_cast<int64_t>(pairs);
-  int64_t y = static_cast<int64_t>(dev.sm_count) * kMoverBlocksPerSm / batch;
+  int64_t y = static_cast<int64_t>(dev.sm_count) * kGatherBlocksPerSm / batch;
   const int64_t y_max = (units + W - 1) / W;
   if (y > y_max) y = y_max;
   if (y < 1) y = 1;
