@@ -511,7 +511,7 @@ def run_shared_index(w, args, stream, group=4):
                 if gi in shared_layers:  # one replay launch for the group's other layers
                     pl, hl = shared_layers[gi]
                     hs.gather_misses(pl, hl, src, dst, misses[k, gi], stream=stream,
-                                     ptrs=ptrs[gi])
+                                     ptrs=ptrs[gi], overlap_prev=True)
         return gr
 
     topks = [w.next_topk().clone() for _ in range(n + 3)]
@@ -529,8 +529,9 @@ def run_shared_index(w, args, stream, group=4):
                 resolved_rows_per_step=resolved / n, replayed_rows_per_step=replayed / n,
                 how=f"layers share their indexer in groups of {group}: per group one "
                     "hs_swap_in emitting its miss plan, then one hs_gather_misses launch "
-                    "replaying it into the group's other layers' hot buffers; one CUDA graph "
-                    "per step")
+                    "replaying it into the group's other layers' hot buffers (launched with "
+                    "HS_OVERLAP_PREV: it starts during the swap-in and reads the plan after "
+                    "it); one CUDA graph per step")
 
 
 # --------------------------------------------------------------------------- other ops

@@ -320,10 +320,17 @@ hs_err hs_invalidate_tokens(int32_t* slot_tokens, int64_t slot_tokens_stride, in
  *  miss_src    device int64 [batch, >=top_k], miss_dst device int32, both stride plan_stride
  *  miss_count  device int32 [batch]
  *  status      device int32 [1] or NULL
+ *  flags       HS_GATHER_HAS_V (the V pointers follow the K pointers; written
+ *              has_v above) | HS_OVERLAP_PREV (the launch may start while the
+ *              preceding kernel in the stream still runs; it reads the plan, the
+ *              counts and the pointer arrays, and writes, only after that kernel
+ *              has finished, so the plan may come from the swap-in right before
+ *              it).  Other bits: HS_ERR_ARG.
  * Precondition (not checked): the miss_dst values a call copies to are distinct.
  */
+#define HS_GATHER_HAS_V 1
 hs_err hs_gather_misses(const uint64_t* pool_ptrs, const uint64_t* hot_ptrs, int32_t num_layers,
-                        int32_t has_v, int64_t pool_num_rows, int64_t hot_num_rows,
+                        int32_t flags, int64_t pool_num_rows, int64_t hot_num_rows,
                         int64_t row_bytes, const int64_t* miss_src, const int32_t* miss_dst,
                         int64_t plan_stride, const int32_t* miss_count, int32_t batch,
                         int32_t top_k, int32_t* status, hs_stream_t stream);
@@ -363,7 +370,7 @@ const char* hs_last_error(void);
  */
 hs_err hs_wait_selftest(int32_t max_polls, int32_t* status, hs_stream_t stream);
 
-#define HS_ABI_VERSION 5
+#define HS_ABI_VERSION 6
 int32_t hs_abi_version(void);
 
 #ifdef __cplusplus

@@ -235,13 +235,15 @@ def wait_selftest(max_polls, status, *, stream=None) -> None:
 
 
 def gather_misses(pool_layers, hot_layers, miss_src, miss_dst, miss_count, *, has_v=False,
-                  status=None, stream=None, ptrs=None) -> None:
+                  status=None, stream=None, ptrs=None, overlap_prev=False) -> None:
     """Replay a swap-in's miss plan onto layers that share its indices: in every
     layer, hot row miss_dst[b][m] = pool row miss_src[b][m] for m < miss_count[b].
     ``pool_layers`` / ``hot_layers`` are lists of per-layer tensors [rows, ...]
     (K layers, then V layers when has_v); ``ptrs`` may pass prebuilt pointer
     arrays (pool_ptrs, hot_ptrs) from ``layer_pointer_array``; pass them when
-    capturing a CUDA graph (building them copies to the device)."""
+    capturing a CUDA graph (building them copies to the device).  With
+    ``overlap_prev`` the launch may start while the preceding kernel in the
+    stream still runs; it reads the plan only once that kernel has finished."""
     _need(miss_src, torch.int64, "miss_src", 2)
     _need(miss_dst, torch.int32, "miss_dst", 2)
     _need(miss_count, torch.int32, "miss_count", 1)
@@ -264,7 +266,8 @@ def gather_misses(pool_layers, hot_layers, miss_src, miss_dst, miss_count, *, ha
         ptrs = (layer_pointer_array(pool_layers, dev), layer_pointer_array(hot_layers, dev))
     nl = len(pool_layers) // (2 if has_v else 1)
     _capi.check(_lib().hs_gather_misses(
-        _ptr(ptrs[0]), _ptr(ptrs[1]), nl, int(bool(has_v)),
+        _ptr(ptrs[0]), _ptr(ptrs[1]), nl,
+        (1 if has_v else 0) | (_capi.OVERLAP_PREV if overlap_prev else 0),
         min(t.shape[0] for t in pool_layers), min(t.shape[0] for t in hot_layers), rb,
         _ptr(miss_src), _ptr(miss_dst), miss_src.stride(0), _ptr(miss_count), B, K,
         _ptr(status), C.c_void_p(_stream(stream))), "hs_gather_misses")

@@ -24,7 +24,7 @@ SEQ_LENS_I64 = 1
 REQ_STATE_I64 = 2
 OVERLAP_PREV = 4
 DT_F32, DT_F16, DT_BF16 = 0, 1, 2
-ABI_VERSION = 5
+ABI_VERSION = 6
 
 # Every symbol include/hisparse.h declares.
 EXPORTS = ("hs_swap_in", "hs_swap_in_smem_bytes", "hs_store_kv", "hs_transfer_kv",

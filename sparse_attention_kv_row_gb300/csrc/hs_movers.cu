@@ -184,6 +184,7 @@ struct GatherParams {
   uint32_t chunks16;   // row_bytes / 16 when row_bytes is a multiple of 16, else 0
   FastDiv div_chunks16;
   FastDiv div_ptr_pairs;
+  int32_t overlap;     // launched with programmatic stream serialization
 };
 
 constexpr int kGatherUnits = 256;  // (miss, pointer pair) units a block stages per round
@@ -206,9 +207,13 @@ __global__ void __launch_bounds__(kMoverThreads, kGatherBlocksPerSm)
   // The next launch may start now: it reads nothing this kernel writes before
   // its own grid-dependency wait.
   grid_dep_launch_dependents();
+  if (p.overlap) grid_dep_wait();  // the plan may come from the kernel before this one
+  // The plan and the counts are read through L2 (ld.global.cg), not the
+  // read-only path: with early start the swap-in that writes them is still
+  // running when this grid begins, so they are not read-only for its lifetime.
   const int tid = threadIdx.x;
   const int64_t row = blockIdx.x;
-  int n = __ldg(p.miss_count + row);
+  int n = __ldcg(p.miss_count + row);
   n = n < 0 ? 0 : (n > p.top_k ? p.top_k : n);
   const uint32_t mb = (static_cast<uint32_t>(n) + gridDim.y - 1) / gridDim.y;
   const uint32_t m0 = blockIdx.y * mb;
@@ -224,8 +229,8 @@ __global__ void __launch_bounds__(kMoverThreads, kGatherBlocksPerSm)
       const uint32_t u = u0 + tid;
       const uint32_t k = p.ptr_pairs == 1 ? u : fast_div(u, p.div_ptr_pairs);
       const uint32_t pp = u - k * p.ptr_pairs;
-      const int32_t d = __ldg(dst_g + m0 + k);
-      const int64_t sr = __ldg(src_g + m0 + k);
+      const int32_t d = __ldcg(dst_g + m0 + k);
+      const int64_t sr = __ldcg(reinterpret_cast<const long long*>(src_g) + m0 + k);
       const uintptr_t pool = static_cast<uintptr_t>(__ldg(p.pool_ptrs + pp));
       const uintptr_t hot = static_cast<uintptr_t>(__ldg(p.hot_ptrs + pp));
       const unsigned char* from = nullptr;
@@ -460,7 +465,7 @@ extern "C" hs_err hs_probe_read(const void* src, int64_t bytes, unsigned long lo
 }
 
 extern "C" hs_err hs_gather_misses(const uint64_t* pool_ptrs, const uint64_t* hot_ptrs,
-                                   int32_t num_layers, int32_t has_v, int64_t pool_num_rows,
+                                   int32_t num_layers, int32_t flags, int64_t pool_num_rows,
                                    int64_t hot_num_rows, int64_t row_bytes,
                                    const int64_t* miss_src, const int32_t* miss_dst,
                                    int64_t plan_stride, const int32_t* miss_count, int32_t batch,
@@ -470,7 +475,9 @@ extern "C" hs_err hs_gather_misses(const uint64_t* pool_ptrs, const uint64_t* ho
   if (batch < 0 || top_k < 0 || num_layers < 0 || row_bytes < 1 || pool_num_rows < 0 ||
       hot_num_rows < 0)
     return fail(HS_ERR_ARG, "hs_gather_misses: negative size or row_bytes < 1");
-  if (has_v != 0 && has_v != 1) return fail(HS_ERR_ARG, "hs_gather_misses: has_v must be 0 or 1");
+  if (flags & ~(HS_GATHER_HAS_V | HS_OVERLAP_PREV))
+    return fail(HS_ERR_ARG, "hs_gather_misses: unknown flags 0x%x", flags);
+  const bool has_v = (flags & HS_GATHER_HAS_V) != 0;
   if (batch == 0 || top_k == 0 || num_layers == 0) return HS_OK;
   if (pool_ptrs == nullptr || hot_ptrs == nullptr || miss_src == nullptr ||
       miss_dst == nullptr || miss_count == nullptr)
@@ -500,6 +507,7 @@ extern "C" hs_err hs_gather_misses(const uint64_t* pool_ptrs, const uint64_t* ho
   p.div_chunks16 = FastDiv{fastdiv_magic(p.chunks16 > 0 ? p.chunks16 : 1u),
                            p.chunks16 > 0 ? p.chunks16 : 1u};
   p.div_ptr_pairs = FastDiv{fastdiv_magic(p.ptr_pairs), p.ptr_pairs};
+  p.overlap = (flags & HS_OVERLAP_PREV) != 0;
   // Enough blocks per row to cover the device even for a few rows, at most
   // one warp per (miss, layer) unit.
   constexpr int W = kMoverThreads / kWarp;
@@ -509,9 +517,16 @@ extern "C" hs_err hs_gather_misses(const uint64_t* pool_ptrs, const uint64_t* ho
   if (y > y_max) y = y_max;
   if (y < 1) y = 1;
   if (y > 65535) y = 65535;
-  gather_misses_kernel<<<dim3(static_cast<unsigned>(batch), static_cast<unsigned>(y)),
-                         kMoverThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
-  const cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(batch), static_cast<unsigned>(y), 1);
+  cfg.blockDim = dim3(kMoverThreads, 1, 1);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = p.overlap ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gather_misses_kernel, p);
   if (e != cudaSuccess)
     return fail(HS_ERR_CUDA, "hs_gather_misses launch: %s", cudaGetErrorString(e));
   return HS_OK;

@@ -112,7 +112,7 @@ def test_gather_rejects(lib):
     assert g(None, None, 0, 0, 10, 10, 16, None, None, 4, None, 2, 4, None, None) == 0  # no layers
     assert g(None, None, 3, 0, 10, 10, 16, None, None, 4, None, 2, 4, None, None) == 1  # NULLs
     assert g(8, 8, 3, 0, 10, 10, 16, 8, 8, 2, 8, 2, 4, None, None) == 1  # plan_stride < top_k
-    assert g(8, 8, 3, 2, 10, 10, 16, 8, 8, 4, 8, 2, 4, None, None) == 1  # has_v not 0/1
+    assert g(8, 8, 3, 2, 10, 10, 16, 8, 8, 4, 8, 2, 4, None, None) == 1  # unknown flag bit
     assert g(8, 8, 3, 0, 10, 10, 0, 8, 8, 4, 8, 2, 4, None, None) == 1  # row_bytes < 1
 
 

@@ -75,9 +75,12 @@ def test_gather_matches_oracle(dev, S, with_v, host, NL):
 
 
 @pytest.mark.parametrize("with_v", [False, True])
-def test_replay_equals_resolution_on_gpu(dev, with_v):
+@pytest.mark.parametrize("overlap", [False, True])
+def test_replay_equals_resolution_on_gpu(dev, with_v, overlap):
     """Layer A resolves and emits its plan; layer B (same state, other bytes)
-    replays it; layer C (a copy of B) resolves itself.  B and C must agree."""
+    replays it; layer C (a copy of B) resolves itself.  B and C must agree.
+    With overlap the replay and C's swap-in are launched with HS_OVERLAP_PREV
+    (each may start while the kernel before it runs)."""
     import synth
 
     hs = _hs()
@@ -104,7 +107,8 @@ def test_replay_equals_resolution_on_gpu(dev, with_v):
         return hs.make_swap_in_args(topk_ids=topk, seq_lens=seq, req_state=req,
                                     slot_tokens=g.tokens, slot_rows=g.rows, lru=g.lru,
                                     pool_rows=g.pool_rows, pool_k=g.pool_k, pool_v=g.pool_v,
-                                    hot_k=g.hot_k, hot_v=g.hot_v, out_rows=out, **kw)
+                                    hot_k=g.hot_k, hot_v=g.hot_v, out_rows=out,
+                                    overlap_prev=overlap and not plan, **kw)
 
     a_args, c_args = resolve(ga, out_a, True), resolve(gc, out_c, False)
     pools_b = [gb.pool_k, gb.pool_v] if with_v else [gb.pool_k]
@@ -115,7 +119,8 @@ def test_replay_equals_resolution_on_gpu(dev, with_v):
 
     def step():
         hs.swap_in_args(a_args, s)
-        hs.gather_misses(pools_b, hots_b, src, dst, miss, has_v=with_v, stream=s, ptrs=ptrs_b)
+        hs.gather_misses(pools_b, hots_b, src, dst, miss, has_v=with_v, stream=s, ptrs=ptrs_b,
+                         overlap_prev=overlap)
         hs.swap_in_args(c_args, s)
 
     ts = synth.TopkStream(9, 0, B, K, L, 0.7)
