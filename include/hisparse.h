@@ -55,7 +55,11 @@ typedef enum hs_err {
  * reads only seq_lens, req_state, num_real, slot_tokens, slot_rows and lru,
  * and writes nothing.  Set it only when no kernel still in flight in the
  * stream writes those six buffers; topk_ids and every other buffer may be
- * written by the preceding kernel. */
+ * written by the preceding kernel.  One more condition when that kernel lets
+ * its dependents start before its last writes (griddepcontrol.launch_dependents
+ * early, as hs_swap_in and hs_gather_misses do): it must not write pool_k,
+ * pool_v or the resident block table, which are read through the read-only
+ * data path (valid only for data unchanged while the reading grid exists). */
 #define HS_OVERLAP_PREV 4
 
 /*
@@ -325,7 +329,10 @@ hs_err hs_invalidate_tokens(int32_t* slot_tokens, int64_t slot_tokens_stride, in
  *              preceding kernel in the stream still runs; it reads the plan, the
  *              counts and the pointer arrays, and writes, only after that kernel
  *              has finished, so the plan may come from the swap-in right before
- *              it).  Other bits: HS_ERR_ARG.
+ *              it; the plan and counts are read through L2.  If that kernel
+ *              starts its dependents early, it must not write the pools or the
+ *              pointer arrays, read through the read-only data path).  Other
+ *              bits: HS_ERR_ARG.
  * Precondition (not checked): the miss_dst values a call copies to are distinct.
  */
 #define HS_GATHER_HAS_V 1
