@@ -379,7 +379,8 @@ def run_headline(args, dev, rank, world, dist):
     # e2e: every step uploads its top-k rows from pinned host memory, runs the
     # step's 61 swap-ins and reads back the outputs and miss counts; uploads and
     # read-backs run on their own streams, double-buffered, so step k's copies
-    # overlap steps k-1 and k+1 on the GPU.
+    # overlap steps k-1 and k+1 on the GPU (step k's read-back is enqueued after
+    # step k+1's replay).
     with torch.cuda.stream(s):  # untimed: each e2e graph's first replay
         for i in range(2):
             topk_dev[i].copy_(e2e_host[i], non_blocking=True)
@@ -398,14 +399,26 @@ def run_headline(args, dev, rank, world, dist):
     e0.record(s)
     s_in.wait_event(e0)
     s_out.wait_event(e0)
+    def read_back(i):
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[i])
+            out_host[i].copy_(out_dev[i], non_blocking=True)
+            miss_host[i].copy_(miss_dev[i], non_blocking=True)
+            out_done[i] = ev()
+            out_done[i].record(s_out)
+
+    c0s, ups = [], []
     for k_, hb in enumerate(e2e_host[2:]):
         i = k_ % 2
         with torch.cuda.stream(s_in):
             if comp_done[i] is not None:
                 s_in.wait_event(comp_done[i])  # the buffer's previous step has read it
+            u0 = ev()
+            u0.record(s_in)
             topk_dev[i].copy_(hb, non_blocking=True)
             up = ev()
             up.record(s_in)
+            ups.append((u0, up))
         with torch.cuda.stream(s):  # a graph replays on the current stream
             s.wait_event(up)
             if out_done[i] is not None:
@@ -415,13 +428,16 @@ def run_headline(args, dev, rank, world, dist):
             g_e2e[i].replay()
             comp_done[i] = ev()
             comp_done[i].record(s)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(comp_done[i])
-            out_host[i].copy_(out_dev[i], non_blocking=True)
-            miss_host[i].copy_(miss_dev[i], non_blocking=True)
-            out_done[i] = ev()
-            out_done[i].record(s_out)
-        marks.append((c0, comp_done[i], out_done[i]))
+        c0s.append(c0)
+        # The previous step's read-back is enqueued after this step's replay: a
+        # copy waiting on a step must not sit ahead of the next step's kernels
+        # where the streams share a hardware queue.
+        if k_ > 0:
+            read_back(1 - i)
+            marks.append((c0s[k_ - 1], comp_done[1 - i], out_done[1 - i]))
+    last = (len(e2e_host) - 3) % 2
+    read_back(last)
+    marks.append((c0s[-1], comp_done[last], out_done[last]))
     enqueue_ms = (time.perf_counter() - wall0) * 1e3
     for d in out_done:
         if d is not None:
@@ -435,10 +451,16 @@ def run_headline(args, dev, rank, world, dist):
     idle_us = e0.elapsed_time(marks[0][0]) * 1e3 + sum(
         marks[k - 1][1].elapsed_time(marks[k][0]) * 1e3 for k in range(1, len(marks)))
     d2h_us = [b.elapsed_time(c) * 1e3 for _, b, c in marks]
+    h2d_us = [a.elapsed_time(b) * 1e3 for a, b in ups]
+    # GPU idle before a step's compute while its upload was still running
+    wait_up_us = sum(max(0.0, marks[k - 1][1].elapsed_time(ups[k][1]) * 1e3)
+                     for k in range(1, len(marks)))
     e2e_detail = dict(compute_us_per_step_median=statistics.median(comp_us),
                       compute_us_per_step_max=max(comp_us),
                       idle_us_between_steps_total=idle_us,
                       readback_us_median=statistics.median(d2h_us), readback_us_max=max(d2h_us),
+                      upload_us_median=statistics.median(h2d_us), upload_us_max=max(h2d_us),
+                      idle_waiting_for_upload_us_total=wait_up_us,
                       host_enqueue_ms=enqueue_ms)
     e2e_misses = int(w.stats[1].item())
     smi_summary = stop_smi(smi, smi_f, smi_path)
