@@ -203,7 +203,6 @@ __global__ void __launch_bounds__(kMoverThreads, kGatherBlocksPerSm)
   constexpr int W = kMoverThreads / kWarp;
   __shared__ const unsigned char* s_src[kGatherUnits];
   __shared__ unsigned char* s_dst[kGatherUnits];
-  __shared__ int s_unaligned;
   // The next launch may start now: it reads nothing this kernel writes before
   // its own grid-dependency wait.
   grid_dep_launch_dependents();
@@ -223,8 +222,8 @@ __global__ void __launch_bounds__(kMoverThreads, kGatherBlocksPerSm)
   const int32_t* dst_g = p.miss_dst + row * p.plan_stride;
   for (uint32_t u0 = 0; u0 < units; u0 += kGatherUnits) {
     const int nu = units - u0 < kGatherUnits ? static_cast<int>(units - u0) : kGatherUnits;
-    if (tid == 0) s_unaligned = 0;
     __syncthreads();  // the previous round's copies are done with the staged units
+    bool misaligned = false;
     if (tid < nu) {
       const uint32_t u = u0 + tid;
       const uint32_t k = p.ptr_pairs == 1 ? u : fast_div(u, p.div_ptr_pairs);
@@ -241,15 +240,15 @@ __global__ void __launch_bounds__(kMoverThreads, kGatherBlocksPerSm)
         } else {
           from = reinterpret_cast<const unsigned char*>(pool) + sr * p.row_bytes;
           to = reinterpret_cast<unsigned char*>(hot) + static_cast<int64_t>(d) * p.row_bytes;
-          if (((reinterpret_cast<uintptr_t>(from) | reinterpret_cast<uintptr_t>(to)) & 15) != 0)
-            s_unaligned = 1;
+          misaligned = ((reinterpret_cast<uintptr_t>(from) | reinterpret_cast<uintptr_t>(to)) & 15) != 0;
         }
       }
       s_src[tid] = from;
       s_dst[tid] = to;
     }
-    __syncthreads();
-    if (p.chunks16 != 0 && s_unaligned == 0) {
+    // The staged units are visible to all, and every thread takes the same path.
+    const bool any_misaligned = __syncthreads_or(misaligned) != 0;
+    if (p.chunks16 != 0 && !any_misaligned) {
       const uint32_t items = static_cast<uint32_t>(nu) * p.chunks16;
       for (uint32_t w0 = tid; w0 < items; w0 += kMoverThreads * kGatherUnroll) {
         uint4 v[kGatherUnroll];
@@ -502,7 +501,8 @@ extern "C" hs_err hs_gather_misses(const uint64_t* pool_ptrs, const uint64_t* ho
   p.miss_count = miss_count;
   p.top_k = top_k;
   p.status = status;
-  p.chunks16 = row_bytes % 16 == 0 && row_bytes / 16 < (1ll << 31)
+  // The flat path counts (unit, chunk) items in 32 bits: kGatherUnits * chunks < 2^32.
+  p.chunks16 = row_bytes % 16 == 0 && row_bytes / 16 <= (1ll << 23)
                    ? static_cast<uint32_t>(row_bytes / 16) : 0u;
   p.div_chunks16 = FastDiv{fastdiv_magic(p.chunks16 > 0 ? p.chunks16 : 1u),
                            p.chunks16 > 0 ? p.chunks16 : 1u};

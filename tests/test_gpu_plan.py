@@ -36,13 +36,18 @@ def _hs():
     return hs
 
 
-@pytest.mark.parametrize("S,with_v,host,NL", [(656, False, False, 1), (656, True, True, 3),
-                                               (132, True, False, 2), (17, False, True, 3)])
-def test_gather_matches_oracle(dev, S, with_v, host, NL):
+@pytest.mark.parametrize("S,with_v,host,NL,B", [(656, False, False, 1, 6), (656, True, True, 3, 6),
+                                                 (132, True, False, 2, 6), (17, False, True, 3, 6),
+                                                 (656, True, False, 4, 160),
+                                                 (132, True, False, 4, 160)])
+def test_gather_matches_oracle(dev, S, with_v, host, NL, B):
     """NL layers (K, then V when with_v) replayed by one call; the oracle
-    replays layer by layer."""
-    rng = np.random.default_rng(S * 3 + with_v)
-    B, K, P, R = 6, 300, 5000, 2000
+    replays layer by layer.  With B=160 rows a block holds about 40 misses x 8
+    pointer pairs, more than one round of staged units (16-byte path at 656 B
+    rows, one warp per unit at 132 B)."""
+    rng = np.random.default_rng(S * 3 + with_v + B)
+    K, P = (300, 5000) if B == 6 else (120, 3000)
+    R = 2000 if B == 6 else B * K + 500
     NP = NL * (2 if with_v else 1)
     pools = [rng.integers(0, 256, (P, S), dtype=np.uint8) for _ in range(NP)]
     hots = [rng.integers(0, 256, (R, S), dtype=np.uint8) for _ in range(NP)]
@@ -52,6 +57,8 @@ def test_gather_matches_oracle(dev, S, with_v, host, NL):
     src[0, 3], dst[1, 5], dst[2, 7] = P + 2, R + 1, -1   # bad src, bad dst, no row
     src[3, 0] = -4
     count = np.array([K, 0, 17, -3, K + 50, 250], np.int32)
+    if B > 6:
+        count = np.concatenate([count, np.full(B - 6, K, np.int32)])
     st_ref = np.zeros(1, np.int32)
     refs = [h.copy() for h in hots]
     for pl, hr in zip(pools, refs):
