@@ -26,6 +26,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import threading
 import time
 
@@ -158,6 +159,10 @@ def stop_smi(p, f, path):
         p.kill()
     f.close()
     lines = [ln.strip() for ln in open(path) if ln.strip() and not ln.startswith("index")]
+    try:
+        os.remove(path)
+    except OSError:
+        pass
     return f"{len(lines)} nvidia-smi samples; last: {lines[-1] if lines else 'none'}"
 
 
@@ -361,8 +366,8 @@ def run_headline(args, dev, rank, world, dist):
     g_e2e = [w.capture_step(topk_dev[i], s, out=out_dev[i], miss=miss_dev[i]) for i in range(2)]
     torch.cuda.synchronize()
 
-    smi_path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv")
-    os.makedirs(os.path.dirname(smi_path), exist_ok=True)
+    # nvidia-smi samples of the timed region (summarised into the JSON line)
+    smi_path = os.path.join(tempfile.gettempdir(), f"hs_bench_clocks_rank{rank}_{os.getpid()}.csv")
     smi, smi_f = start_smi(dev.index, smi_path)
     sampler = NvmlSampler(dev.index)
     w.stats.zero_()
