@@ -151,8 +151,9 @@ typedef enum hs_err {
  *
  * Limits: 1 <= top_k <= hot_size <= 32767 (slots are int16).  Each row runs
  * on a cluster of up to 8 CTAs; every CTA holds the row's ids, LRU order, slot
- * tokens, slot rows and a hash of 2*top_k..4*top_k entries, plus its share of
- * the per-position state, and this must fit one CTA's shared memory
+ * tokens, slot rows and a hash of 2*top_k..8*top_k slots (the most that fits),
+ * plus its share of the per-position state, and this must fit one CTA's shared
+ * memory
  * (hs_swap_in_smem_bytes), else HS_ERR_UNSUPPORTED.  hot_num_rows <= INT32_MAX.
  * Preconditions (not checked): distinct req_state values within one call;
  * slot_rows values distinct across the slots the call can touch; pool and hot
