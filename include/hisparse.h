@@ -43,7 +43,7 @@ typedef enum hs_err {
 #define HS_ST_BAD_POOL_ROW 2  /* a miss's pool row was outside [0, pool_num_rows): -1, not a miss */
 #define HS_ST_BAD_LRU_SLOT 4  /* an LRU entry was outside [0, hot_size) or repeated a slot */
 #define HS_ST_BAD_HOT_ROW 8   /* a miss's hot row was outside [0, hot_num_rows): -1, no copy */
-#define HS_ST_TIMEOUT 16      /* a bounded wait inside a kernel gave up */
+#define HS_ST_TIMEOUT 16      /* a bounded wait inside a kernel gave up (see hs_swap_in) */
 #define HS_ST_BAD_STATE 32    /* req_state[b] >= num_states: row emitted -1 */
 #define HS_ST_BAD_INDEX 64    /* a mover index was out of range: that row was skipped */
 
@@ -100,6 +100,12 @@ typedef enum hs_err {
  *    (HS_ST_BAD_LRU_SLOT); a miss given such an entry, or a slot whose hot row
  *    is outside [0, hot_num_rows) (HS_ST_BAD_HOT_ROW), emits -1 and writes no
  *    token and no bytes but still counts as a miss.
+ *  - time-out: the kernel's waits for its own staging copies are bounded.  If
+ *    one runs out in any CTA of a row, the whole row is left alone: status[b]
+ *    is exactly HS_ST_TIMEOUT, miss_count[b] is 0, and out_rows, the plan,
+ *    the LRU row, the slot tokens, the stats and the hot buffer are not
+ *    written.  It means the GPU did not complete a copy within about a
+ *    second; treat the context as suspect.
  *
  * Layouts (all row-major with the given element strides; device memory unless
  * noted):
@@ -190,6 +196,21 @@ typedef struct hs_swap_in_args {
 } hs_swap_in_args;
 
 hs_err hs_swap_in(const hs_swap_in_args* args, hs_stream_t stream);
+
+/*
+ * hs_swap_in_timeout_selftest -- hs_swap_in with one CTA of every full-path
+ * row made to give up one of its bounded waits at once (zero polls), so that
+ * the time-out path runs without any GPU fault or hang: the copy it gave up
+ * on is still waited out before the CTA exits.  rank >= 0 picks that CTA of
+ * each row's cluster (mod the cluster size), rank < 0 the last one; which = 0
+ * gives up the wait for the row's staged state, 1 the wait for its top-k row.
+ * Every full-path row must then report exactly HS_ST_TIMEOUT with miss_count
+ * 0 and no other write (see hs_swap_in); padding and short-sequence rows do
+ * not wait and run as usual.  Defined by this library (the pages bound no
+ * waits).  Errors: those of hs_swap_in, and HS_ERR_ARG for which not 0 or 1.
+ */
+hs_err hs_swap_in_timeout_selftest(const hs_swap_in_args* args, int32_t rank, int32_t which,
+                                   hs_stream_t stream);
 
 /* Shared memory (bytes) per CTA that a swap-in row needs for (top_k, hot_size)
  * when split over the largest cluster (8 CTAs); 0 if the pair is outside the
@@ -378,7 +399,7 @@ const char* hs_last_error(void);
  */
 hs_err hs_wait_selftest(int32_t max_polls, int32_t* status, hs_stream_t stream);
 
-#define HS_ABI_VERSION 6
+#define HS_ABI_VERSION 7
 int32_t hs_abi_version(void);
 
 #ifdef __cplusplus

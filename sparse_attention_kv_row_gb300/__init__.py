@@ -24,7 +24,7 @@ from ._capi import (HisparseError, SwapInArgs, ST_BAD_HOT_ROW, ST_BAD_INDEX,  # 
                     ST_BAD_LRU_SLOT, ST_BAD_POOL_ROW, ST_BAD_STATE, ST_DUP_ID, ST_TIMEOUT)
 
 __all__ = ["swap_in", "swap_in_args", "make_swap_in_args", "gather_misses", "fp8_store_kv",
-           "invalidate_tokens", "wait_selftest",
+           "invalidate_tokens", "wait_selftest", "swap_in_timeout_selftest",
            "store_kv", "transfer_kv",
            "transfer_kv_layers", "probe_read", "swap_in_smem_bytes", "library_path",
            "HisparseError", "SwapInArgs"]
@@ -204,6 +204,16 @@ def make_swap_in_args(*, topk_ids, seq_lens, req_state, slot_tokens, slot_rows, 
 def swap_in_args(args: SwapInArgs, stream=None) -> None:
     """Launch hs_swap_in with a prepared argument block."""
     _capi.check(_lib().hs_swap_in(C.byref(args), C.c_void_p(_stream(stream))), "hs_swap_in")
+
+
+def swap_in_timeout_selftest(args: SwapInArgs, *, rank=-1, which=0, stream=None) -> None:
+    """hs_swap_in with one CTA of every full-path row giving up a bounded wait at
+    once (``rank`` of the row's cluster, the last when negative; ``which`` 0 =
+    the staged-state wait, 1 = the top-k-row wait): those rows must report
+    exactly HS_ST_TIMEOUT and write nothing else."""
+    _capi.check(_lib().hs_swap_in_timeout_selftest(C.byref(args), int(rank), int(which),
+                                                   C.c_void_p(_stream(stream))),
+                "hs_swap_in_timeout_selftest")
 
 
 def swap_in(*, stream=None, **tensors) -> None:

@@ -69,8 +69,9 @@ constexpr uint32_t kMaxPolls = 1u << 22;  // bounded mbarrier waits
 // which then makes the staged bytes visible to all of them.  (Threads polling
 // a barrier that is not armed yet would take shared-memory bandwidth from the
 // thread about to arm it.)  False in every thread when the wait ran out.
-__device__ __forceinline__ bool block_wait(uint64_t* bar, uint32_t parity) {
-  return __syncthreads_and(threadIdx.x == 0 ? mbar_wait(bar, parity, kMaxPolls) : 1) != 0;
+__device__ __forceinline__ bool block_wait(uint64_t* bar, uint32_t parity,
+                                           uint32_t polls = kMaxPolls) {
+  return __syncthreads_and(threadIdx.x == 0 ? mbar_wait(bar, parity, polls) : 1) != 0;
 }
 
 // Per-entry classification, stored as one byte per top-k entry.
@@ -179,9 +180,15 @@ struct SwapInParams {
   int32_t entry_bits;       // bits of a top-k entry index in the packed hash
   int64_t max_seq_len;      // 0, or a bound on every row's sequence length
   int32_t copy_width;       // 16, 4 or 1 bytes per copy chunk
+  int32_t fail_rank;        // self-test: this cluster rank's wait gives up at once (-1: none)
+  int32_t fail_wait;        // self-test: 0 = the state-row wait, 1 = the top-k-row wait
 };
 
-enum { kMiscFlags = 0, kMiscRepeat = 1, kMiscSlotRepeat = 2, kMiscHits = 3, kMiscMisses = 4 };
+enum {
+  kMiscFlags = 0, kMiscRepeat = 1, kMiscSlotRepeat = 2, kMiscHits = 3, kMiscMisses = 4,
+  kMiscTimeout = 5,    // this CTA's bounded wait ran out
+  kMiscRowTimeout = 6  // some CTA of the row's cluster ran out
+};
 
 __device__ __forceinline__ uint32_t hash_of(int32_t key, int bits) {
   return (static_cast<uint32_t>(key) * 2654435761u) >> (32 - bits);
@@ -287,6 +294,35 @@ struct ReqHash {
   __device__ __forceinline__ int32_t find(int32_t key) const { return find_from(key, first(key)); }
 };
 
+constexpr uint32_t kDrainPolls = 1u << 26;  // waiting out copies still in flight after a time-out
+
+// The exit of a CTA whose bounded wait ran out (block-uniform; the CTA has
+// arrived at the row's first cluster barrier).  It completes both cluster
+// barriers so that its peers' waits complete, reports the time-out (with no
+// other write: its peers see the time-out too and leave the row alone), and
+// waits, with a much larger bound, for its own bulk copies still in flight
+// before its shared memory is released.  If even that bound runs out the CTA
+// returns with the copy outstanding; HS_ST_TIMEOUT then says the context is
+// suspect.
+__device__ __noinline__ void timeout_tail(const SwapInParams& p, int b, int j, int C,
+                                          uint64_t* bar, bool ids_issued) {
+  cluster_wait();
+  if (C > 1) cluster_arrive();
+  if (threadIdx.x == 0) {
+    if (p.status) {
+      if (j == 0)
+        p.status[b] = HS_ST_TIMEOUT;
+      else
+        atomicOr(p.status + b, HS_ST_TIMEOUT);
+    }
+    if (j == 0 && p.miss_count) p.miss_count[b] = 0;
+    mbar_wait(bar + 1, 0, kDrainPolls);
+    if (ids_issued) mbar_wait(bar, 0, kDrainPolls);
+  }
+  __syncthreads();
+  if (C > 1) cluster_wait();
+}
+
 template <int G>
 struct Chunk;
 template <>
@@ -367,7 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   // writes nothing to global memory; the top-k row is read after the wait.
   // Rows are staged by bulk copies (their 16-byte-aligned bodies) completed
   // on two mbarriers, one per row kind, each used for one phase; the
-  // unaligned head and tail bytes go through registers.
+  // unaligned head and tail bytes go through registers.  Copies are issued
+  // only on the full path, so the padding and short-sequence exits leave
+  // nothing in flight.
   grid_dep_launch_dependents();
   const bool overlap = (p.flags & HS_OVERLAP_PREV) != 0;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.o_bar);
@@ -388,7 +426,6 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       stage_body(ids, ids_g, sp_ids, bar);
     }
   };
-  if (!overlap) stage_ids();
 
   int32_t* out_g = p.out_rows + static_cast<int64_t>(b) * p.out_stride;
   const bool pad_nr = p.num_real != nullptr && b >= __ldg(p.num_real);
@@ -402,7 +439,6 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const bool too_long = p.max_seq_len > 0 && Lb > p.max_seq_len;  // outside the caller's bound
   if (pad_nr || r < 0 || r >= p.num_states || too_long) {  // padding / bad state row
     grid_dep_wait();
-    if (!overlap && tid == 0) mbar_wait(bar, 0, kMaxPolls);  // no copy left in flight
     for (int i = e0 + tid; i < e1; i += kThreads) {
       out_g[i] = -1;
       if (p.miss_mask) p.miss_mask[b * p.mask_stride + i] = 0;
@@ -417,19 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const int32_t* rows_g = p.slot_rows + r * p.slot_rows_stride;
   if (Lb <= H) {  // fast path: the whole sequence sits in the hot buffer in order
     grid_dep_wait();
-    if (overlap) stage_ids();
-    __syncthreads();  // the barriers' initialisation is visible
-    stage_finish(ids, pend_ids);
-    if (!block_wait(bar, 0)) {
-      if (tid == 0) {
-        if (p.status) atomicOr(p.status + b, HS_ST_TIMEOUT);
-        mbar_wait(bar, 0, kMaxPolls);
-      }
-      return;
-    }
+    // Each CTA reads only its own entries' ids, straight from global memory
+    // through L2 (the preceding kernel may have written them).
     const int64_t count = Lb < K ? Lb : K;
     for (int i = e0 + tid; i < e1; i += kThreads) {
-      const int32_t t = ids[i];
+      const int32_t t = __ldcg(ids_g + i);
       int32_t o = -1;
       if (i < count && t >= 0 && t < Lb) {
         o = __ldg(rows_g + t);
@@ -470,6 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     stage_body(tok, tokens_g, sp_tok, bar + 1);
     stage_body(rows, rows_g, sp_rows, bar + 1);
   }
+  // Without early start the top-k row is final already: its copy goes out
+  // with the state's.
+  bool ids_issued = !overlap;
+  if (!overlap) stage_ids();
   const StagePending pend_lru = stage_edges(lru_g, 2LL * H, sp_lru, tid);
   const StagePending pend_tok = stage_edges(tokens_g, 4LL * H, sp_tok, tid);
   const StagePending pend_rows = stage_edges(rows_g, 4LL * (H + 1), sp_rows, tid);
@@ -505,19 +537,17 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   stage_finish(lru, pend_lru);
   stage_finish(tok, pend_tok);
   stage_finish(rows, pend_rows);
-  const bool staged = block_wait(bar + 1, 0);
-  // Every CTA of the row has staged the state once all have arrived here; the
-  // matching wait comes right before the first write to that state.
-  cluster_arrive();
-  if (!staged) {  // a bounded wait ran out: report it and leave the row alone
-    if (tid == 0) {
-      if (p.status) atomicOr(p.status + b, HS_ST_TIMEOUT);
-      mbar_wait(bar + 1, 0, kMaxPolls);
-      if (!overlap) mbar_wait(bar, 0, kMaxPolls);
-    }
+  // A wait that runs out in any CTA of the row leaves the whole row alone:
+  // each CTA records its outcome in misc[kMiscTimeout] before the cluster
+  // barrier, and after it every CTA reads all of them (below, before the
+  // row's first write).
+  const uint32_t polls_state = (p.fail_rank == j && p.fail_wait == 0) ? 0u : kMaxPolls;
+  if (!block_wait(bar + 1, 0, polls_state)) {
+    if (tid == 0) misc[kMiscTimeout] = 1;
+    cluster_arrive();
+    timeout_tail(p, b, j, C, bar, ids_issued);
     return;
   }
-
   // ---- P1 (state half): check the LRU row is a permutation of the slots.
   int32_t my_flags = 0;
   int sl[IT];  // the slot at each of my LRU positions
@@ -575,13 +605,20 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
 
   // ---- P1 (request half): the top-k row, written by the preceding kernel.
   grid_dep_wait();
-  if (overlap) stage_ids();
+  if (overlap) {
+    stage_ids();
+    ids_issued = true;
+  }
   stage_finish(ids, pend_ids);
-  if (!block_wait(bar, 0)) {
-    if (tid == 0) {
-      if (p.status) atomicOr(p.status + b, HS_ST_TIMEOUT);
-      mbar_wait(bar, 0, kMaxPolls);
-    }
+  const uint32_t polls_ids = (p.fail_rank == j && p.fail_wait == 1) ? 0u : kMaxPolls;
+  const bool ids_ok = block_wait(bar, 0, polls_ids);
+  if (tid == 0 && !ids_ok) misc[kMiscTimeout] = 1;
+  // Every CTA of the row has staged the state (and recorded whether its waits
+  // ran out) once all have arrived here; the matching wait comes right before
+  // the first write to that state.
+  cluster_arrive();
+  if (!ids_ok) {
+    timeout_tail(p, b, j, C, bar, ids_issued);
     return;
   }
   // Block tables: each valid id's entries are loaded with LDGSTS into prs
@@ -821,6 +858,27 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const int my_first_miss = e0 < K ? cnte[e0 >> 5] : M;
   // The first state write of the row follows: wait until every CTA has staged.
   cluster_wait();
+  if (C > 1) {
+    // The row goes ahead only if no CTA's wait ran out.  Each CTA reads its
+    // peers' outcomes from their shared memory (written before their arrive),
+    // then arrives at a second cluster barrier, waited on at exit, so that no
+    // CTA leaves while a peer may still read its shared memory.
+    if (warp == 0) {
+      const int t = lane < C ? peer_ld(peer_addr(&misc[kMiscTimeout], lane)) : 0;
+      const unsigned any = __ballot_sync(kFullMask, t != 0);
+      if (lane == 0) misc[kMiscRowTimeout] = any != 0u;
+    }
+    __syncthreads();
+    cluster_arrive();
+    if (misc[kMiscRowTimeout]) {  // another CTA's wait ran out: leave the row alone
+      if (j == 0 && tid == 0) {
+        if (p.status) p.status[b] = HS_ST_TIMEOUT;
+        if (p.miss_count) p.miss_count[b] = 0;
+      }
+      cluster_wait();
+      return;
+    }
+  }
   // Only my own entries: their chunks are whole and 32-aligned, so a warp's
   // ballot covers one chunk.
   int64_t my_pr = 0;
@@ -907,6 +965,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     copy_rows<1>(p, p.pool_k, p.hot_k, my_m, jsrc, jdst);
     if (p.pool_v != nullptr) copy_rows<1>(p, p.pool_v, p.hot_v, my_m, jsrc, jdst);
   }
+  if (C > 1) cluster_wait();  // no peer still reads this CTA's shared memory
 }
 
 using KernelFn = void (*)(const SwapInParams);
@@ -964,9 +1023,13 @@ extern "C" int64_t hs_swap_in_smem_bytes(int32_t top_k, int32_t hot_size) {
   return hs::make_layout(top_k, hot_size, hs::kMaxCluster, hs::hash_bits_for(top_k, 2)).total;
 }
 
-extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
-  using namespace hs;
-  clear_error();
+namespace hs {
+namespace {
+
+// hs_swap_in, with the self-test's forced time-out: fail_rank -1 = none, -2 =
+// the last CTA of each row's cluster, else that rank (mod the cluster size).
+hs_err swap_in_launch(const hs_swap_in_args* a, hs_stream_t stream, int fail_rank,
+                      int fail_wait) {
   if (a == nullptr) return fail(HS_ERR_ARG, "hs_swap_in: args is NULL");
   if (a->batch < 0 || a->top_k < 0)
     return fail(HS_ERR_ARG, "hs_swap_in: batch (%d) and top_k (%d) must be >= 0", a->batch,
@@ -1130,6 +1193,8 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   p.entry_bits = eb;
   p.max_seq_len = a->max_seq_len;
   p.copy_width = G;
+  p.fail_rank = fail_rank == -1 ? -1 : (fail_rank < 0 ? C - 1 : fail_rank % C);
+  p.fail_wait = fail_wait;
 
   int items = 1;
   while (items * kThreads < a->hot_size) items *= 2;
@@ -1159,4 +1224,20 @@ extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
   const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p);
   if (e != cudaSuccess) return fail(HS_ERR_CUDA, "hs_swap_in launch: %s", cudaGetErrorString(e));
   return HS_OK;
+}
+
+}  // namespace
+}  // namespace hs
+
+extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
+  hs::clear_error();
+  return hs::swap_in_launch(a, stream, -1, 0);
+}
+
+extern "C" hs_err hs_swap_in_timeout_selftest(const hs_swap_in_args* a, int32_t rank,
+                                              int32_t which, hs_stream_t stream) {
+  hs::clear_error();
+  if (which != 0 && which != 1)
+    return hs::fail(HS_ERR_ARG, "hs_swap_in_timeout_selftest: which must be 0 or 1");
+  return hs::swap_in_launch(a, stream, rank < 0 ? -2 : rank, which);
 }

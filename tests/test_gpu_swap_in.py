@@ -326,3 +326,63 @@ def test_bounded_wait_runs_out_and_context_stays_usable(dev):
         ids = cases.random_ids(rng, ref, prev=prev)
         prev = ids
         step_both(g, ref, ids, f"after the timeout, step {step}")
+
+
+@pytest.mark.parametrize("which,rank,overlap", [(0, 0, False), (0, -1, False), (1, -1, False),
+                                                (1, 3, True), (0, 2, True)])
+def test_forced_timeout_leaves_rows_alone(dev, which, rank, overlap):
+    """One CTA of every full-path row gives up a bounded wait at once (the
+    self-test entry point; the copy it gave up on is still waited out, so
+    nothing faults or hangs).  The whole row is then left alone, whichever CTA
+    of the cluster gave up: status is exactly HS_ST_TIMEOUT, miss_count 0, and
+    the outputs, plan, LRU order, slot tokens, statistics and hot buffer are
+    unchanged.  A padding row and a short-sequence row do not wait and come
+    out as the oracle says.  A normal call afterwards matches the oracle."""
+    import oracle
+    import sparse_attention_kv_row_gb300 as hs
+    import synth
+
+    rng = np.random.default_rng(600 + which * 10 + rank)
+    B, K, H, L = 5, 300, 1000, 9000      # 5 rows: clusters of 8 CTAs
+    ref = cases.random_case(rng, B=B, K=K, H=H, S=656, R=B + 1, seq_len=L)
+    ref.seq_lens[1] = H - 5              # the short-sequence path
+    ref.req_state[3] = -1                # padding
+    g = GpuCase(ref.copy(), dev)
+    ts = synth.TopkStream(5, 0, B, K, L, 0.6)
+    step_both(g, ref, ts.next(), "warm")           # some resident tokens first
+    ids = ts.next()
+    before = (g.tokens.clone(), g.lru.clone(), g.hot_k.clone())
+    topk = torch.from_numpy(ids).to(dev)
+    out = torch.full((B, K), 4242, dtype=torch.int32, device=dev)
+    miss = torch.full((B,), 777, dtype=torch.int32, device=dev)
+    status = torch.full((B,), 999, dtype=torch.int32, device=dev)
+    stats = torch.zeros(2, dtype=torch.int64, device=dev)
+    plan_src = torch.full((B, K), 5, dtype=torch.int64, device=dev)
+    plan_dst = torch.full((B, K), 6, dtype=torch.int32, device=dev)
+    mask = torch.full((B, K), 7, dtype=torch.int32, device=dev)
+    args = hs.make_swap_in_args(
+        topk_ids=topk, seq_lens=torch.from_numpy(ref.seq_lens).to(dev),
+        req_state=torch.from_numpy(ref.req_state).to(dev), slot_tokens=g.tokens,
+        slot_rows=g.rows, lru=g.lru, pool_rows=g.pool_rows, pool_k=g.pool_k, hot_k=g.hot_k,
+        out_rows=out, miss_count=miss, status=status, stats=stats, miss_src=plan_src,
+        miss_dst=plan_dst, miss_mask=mask, max_seq_len=L, overlap_prev=overlap)
+    hs.swap_in_timeout_selftest(args, rank=rank, which=which)
+    torch.cuda.synchronize()
+    assert torch.equal(g.tokens, before[0]) and torch.equal(g.lru, before[1])
+    assert torch.equal(g.hot_k, before[2])
+    assert int(stats.abs().sum()) == 0
+    full = [0, 2, 4]
+    st, ms, o = status.cpu().numpy(), miss.cpu().numpy(), out.cpu().numpy()
+    for b in full:
+        assert st[b] == oracle.ST_TIMEOUT and ms[b] == 0, (b, st, ms)
+        assert np.all(o[b] == 4242)
+        assert np.all(plan_src[b].cpu().numpy() == 5) and np.all(mask[b].cpu().numpy() == 7)
+    # the rows that do not wait: as the oracle has them (their state is untouched)
+    probe = ref.copy()
+    probe.topk = ids
+    r_out, r_miss, r_status, _ = cases.run_oracle(probe)
+    for b in (1, 3):
+        np.testing.assert_array_equal(o[b], r_out[b])
+        assert ms[b] == r_miss[b] and st[b] == r_status[b]
+    # the context is usable and the state intact: a normal call matches the oracle
+    step_both(g, ref, ids, "after the forced time-out", plan=True)
