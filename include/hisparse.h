@@ -155,12 +155,14 @@ typedef enum hs_err {
  * (all 0 for padding rows and short sequences).  miss_src and miss_dst go
  * together and need miss_count.
  *
- * Limits: 1 <= top_k <= hot_size <= 32767 (slots are int16).  Each row runs
- * on a cluster of up to 8 CTAs; every CTA holds the row's ids, LRU order, slot
- * tokens, slot rows and a hash of 2*top_k..8*top_k slots (the most that fits),
- * plus its share of the per-position state, and this must fit one CTA's shared
- * memory
- * (hs_swap_in_smem_bytes), else HS_ERR_UNSUPPORTED.  hot_num_rows <= INT32_MAX.
+ * Limits: 1 <= top_k <= hot_size <= 32767 (slots are int16).  Up to
+ * hot_size 8192 each row runs on a cluster of up to 8 CTAs; every CTA holds the
+ * row's ids, LRU order, slot tokens, slot rows and a hash of 2*top_k..8*top_k
+ * slots (the most that fits), plus its share of the per-position state.  Above
+ * 8192 each row runs on one CTA (the hs_swap_in_layers kernel), which keeps
+ * the slot tokens and rows in global memory when they do not fit.  Either way
+ * the row's state must fit one CTA's shared memory (hs_swap_in_smem_bytes),
+ * else HS_ERR_UNSUPPORTED.  hot_num_rows <= INT32_MAX.
  * Preconditions (not checked): distinct req_state values within one call;
  * slot_rows values distinct across the slots the call can touch; pool and hot
  * buffers do not overlap; no other work writes these buffers concurrently.
@@ -212,9 +214,52 @@ hs_err hs_swap_in(const hs_swap_in_args* args, hs_stream_t stream);
 hs_err hs_swap_in_timeout_selftest(const hs_swap_in_args* args, int32_t rank, int32_t which,
                                    hs_stream_t stream);
 
-/* Shared memory (bytes) per CTA that a swap-in row needs for (top_k, hot_size)
- * when split over the largest cluster (8 CTAs); 0 if the pair is outside the
- * limits above. */
+/*
+ * hs_swap_in_layers -- hs_swap_in for several layers at once, when the caller
+ * has every layer's top-k rows: layers[l] is layer l's complete argument
+ * block, and the result for each layer is exactly what hs_swap_in(&layers[l])
+ * would give, layer by layer.  All batch rows of all layers are resolved by
+ * one grid (one CTA per row and layer), so a decode step's layers share the
+ * GPU instead of running one small launch after another.  This is a variant
+ * of the pages' per-layer call (SGLang jit_kernel/csrc/hisparse.cuh,
+ * load_cache_to_device_buffer, runs once per layer); its rules, status bits
+ * and time-out behaviour are those of hs_swap_in.
+ *
+ *  layers      host array of num_layers argument blocks (read during the call
+ *              only).  Every block must agree with layers[0] in batch, top_k,
+ *              hot_size, flags, row_bytes, max_seq_len, every stride, every
+ *              row count (num_states, pool_rows_cols, pool_num_rows,
+ *              hot_num_rows), the block-table geometry, and in which optional
+ *              pointers are NULL; only the pointers themselves may differ.
+ *              Otherwise HS_ERR_ARG.
+ *  num_layers  >= 0 (0 launches nothing); any number (launched 64 layers at a
+ *              time, in order)
+ * Preconditions (not checked): no two layers write the same buffer (state
+ * rows, hot buffers, outputs, plans, status words; a shared stats counter is
+ * fine, it is added to atomically).  Read-only buffers (pools, slot_rows,
+ * pool_rows, tables, top-k rows, request metadata) may be shared.
+ * Limits: those of hs_swap_in; per CTA the row's state must fit shared memory
+ * (top_k up to a few thousand with any hot_size <= 32767), else
+ * HS_ERR_UNSUPPORTED.
+ */
+hs_err hs_swap_in_layers(const hs_swap_in_args* layers, int32_t num_layers,
+                         hs_stream_t stream);
+
+/*
+ * hs_swap_in_layers_timeout_selftest -- hs_swap_in_layers with every
+ * full-path row made to give up one bounded wait at once (which = 0: the
+ * staged state; 1: the top-k row), as hs_swap_in_timeout_selftest does for
+ * the per-layer call: those rows report exactly HS_ST_TIMEOUT with
+ * miss_count 0 and write nothing else.  Defined by this library.
+ */
+hs_err hs_swap_in_layers_timeout_selftest(const hs_swap_in_args* layers, int32_t num_layers,
+                                          int32_t which, hs_stream_t stream);
+
+/* Shared memory (bytes) per CTA that a swap-in row needs for (top_k, hot_size):
+ * split over the largest cluster (8 CTAs) up to hot_size 8192, the one-CTA
+ * kernel's least above it; 0 if the pair is outside [1, 32767] or
+ * top_k > hot_size.  The call returns HS_ERR_UNSUPPORTED when this exceeds the
+ * device's per-CTA shared memory. */
 int64_t hs_swap_in_smem_bytes(int32_t top_k, int32_t hot_size);
 
 /*
@@ -399,7 +444,7 @@ const char* hs_last_error(void);
  */
 hs_err hs_wait_selftest(int32_t max_polls, int32_t* status, hs_stream_t stream);
 
-#define HS_ABI_VERSION 7
+#define HS_ABI_VERSION 8
 int32_t hs_abi_version(void);
 
 #ifdef __cplusplus

@@ -25,6 +25,7 @@ from ._capi import (HisparseError, SwapInArgs, ST_BAD_HOT_ROW, ST_BAD_INDEX,  # 
 
 __all__ = ["swap_in", "swap_in_args", "make_swap_in_args", "gather_misses", "fp8_store_kv",
            "invalidate_tokens", "wait_selftest", "swap_in_timeout_selftest",
+           "swap_in_layers", "swap_in_layers_timeout_selftest", "layer_args_array",
            "store_kv", "transfer_kv",
            "transfer_kv_layers", "probe_read", "swap_in_smem_bytes", "library_path",
            "HisparseError", "SwapInArgs"]
@@ -214,6 +215,32 @@ def swap_in_timeout_selftest(args: SwapInArgs, *, rank=-1, which=0, stream=None)
     _capi.check(_lib().hs_swap_in_timeout_selftest(C.byref(args), int(rank), int(which),
                                                    C.c_void_p(_stream(stream))),
                 "hs_swap_in_timeout_selftest")
+
+
+def layer_args_array(layers):
+    """A ctypes array of hs_swap_in_args from a list of ``make_swap_in_args``
+    results (one per layer); keeps the layers' tensors alive with it."""
+    arr = (SwapInArgs * len(layers))(*layers)
+    arr.keep = list(layers)
+    return arr
+
+
+def swap_in_layers(layers, stream=None) -> None:
+    """hs_swap_in_layers: every layer's swap-in in one launch.  ``layers`` is a
+    list of ``make_swap_in_args`` results (same geometry, other pointers) or an
+    array from ``layer_args_array`` (cheaper to reuse)."""
+    arr = layers if isinstance(layers, C.Array) else layer_args_array(layers)
+    _capi.check(_lib().hs_swap_in_layers(arr, len(arr), C.c_void_p(_stream(stream))),
+                "hs_swap_in_layers")
+
+
+def swap_in_layers_timeout_selftest(layers, *, which=0, stream=None) -> None:
+    """hs_swap_in_layers with every full-path row giving up one bounded wait at
+    once (``which`` 0 = the staged state, 1 = the top-k row)."""
+    arr = layers if isinstance(layers, C.Array) else layer_args_array(layers)
+    _capi.check(_lib().hs_swap_in_layers_timeout_selftest(arr, len(arr), int(which),
+                                                          C.c_void_p(_stream(stream))),
+                "hs_swap_in_layers_timeout_selftest")
 
 
 def swap_in(*, stream=None, **tensors) -> None:

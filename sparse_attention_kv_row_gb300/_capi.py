@@ -24,12 +24,13 @@ SEQ_LENS_I64 = 1
 REQ_STATE_I64 = 2
 OVERLAP_PREV = 4
 DT_F32, DT_F16, DT_BF16 = 0, 1, 2
-ABI_VERSION = 7
+ABI_VERSION = 8
 
 # Every symbol include/hisparse.h declares.
 EXPORTS = ("hs_swap_in", "hs_swap_in_smem_bytes", "hs_store_kv", "hs_transfer_kv",
            "hs_gather_misses", "hs_fp8_store_kv", "hs_invalidate_tokens", "hs_probe_read", "hs_err_string", "hs_status_string", "hs_last_error",
-           "hs_abi_version", "hs_wait_selftest", "hs_swap_in_timeout_selftest")
+           "hs_abi_version", "hs_wait_selftest", "hs_swap_in_timeout_selftest",
+           "hs_swap_in_layers", "hs_swap_in_layers_timeout_selftest")
 
 
 class SwapInArgs(C.Structure):
@@ -89,6 +90,10 @@ def load() -> C.CDLL:
         lib.hs_swap_in.restype = C.c_int
         lib.hs_swap_in_timeout_selftest.argtypes = [C.POINTER(SwapInArgs), i32, i32, vp]
         lib.hs_swap_in_timeout_selftest.restype = C.c_int
+        lib.hs_swap_in_layers.argtypes = [C.POINTER(SwapInArgs), i32, vp]
+        lib.hs_swap_in_layers.restype = C.c_int
+        lib.hs_swap_in_layers_timeout_selftest.argtypes = [C.POINTER(SwapInArgs), i32, i32, vp]
+        lib.hs_swap_in_layers_timeout_selftest.restype = C.c_int
         lib.hs_swap_in_smem_bytes.argtypes = [i32, i32]
         lib.hs_swap_in_smem_bytes.restype = i64
         lib.hs_store_kv.argtypes = [vp, vp, i64, i64, vp, vp, i64, i64, vp, i64, i64, vp, vp]

@@ -36,10 +36,13 @@ hs_err current_device(DeviceInfo* out) {
   if (dev < 0 || dev >= kMaxDevices) return fail(HS_ERR_UNSUPPORTED, "device index %d", dev);
   std::lock_guard<std::mutex> lock(g_dev_mu);
   if (!g_dev_ok[dev]) {
-    DeviceInfo d{dev, 0, 0};
+    DeviceInfo d{dev, 0, 0, 0};
     e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess)
       e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&d.max_smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                 dev);
     if (e != cudaSuccess)
       return fail(HS_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
     g_dev[dev] = d;

@@ -18,6 +18,7 @@ struct DeviceInfo {
   int device;
   int sm_count;
   int max_smem_optin;
+  int max_smem_per_sm;
 };
 // Properties of the current device (cached per device).
 hs_err current_device(DeviceInfo* out);

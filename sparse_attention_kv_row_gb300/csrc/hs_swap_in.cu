@@ -53,6 +53,7 @@
 
 #include "hs_device.cuh"
 #include "hs_host.h"
+#include "hs_swap_in_common.cuh"
 
 namespace hs {
 namespace {
@@ -61,25 +62,6 @@ constexpr int kThreads = 1024;
 constexpr int kMaxItems = 8;  // LRU positions per thread: hot_size <= 8192
 constexpr int kCopyUnroll = 4;
 constexpr int kMaxCluster = 8;
-constexpr int32_t kUnclaimed = INT_MAX;
-constexpr uint32_t kMaxPolls = 1u << 22;  // bounded mbarrier waits
-
-// Waits until the phase of `bar` with the given parity has completed: thread
-// 0 polls (a bounded wait) while the other threads wait at the block barrier,
-// which then makes the staged bytes visible to all of them.  (Threads polling
-// a barrier that is not armed yet would take shared-memory bandwidth from the
-// thread about to arm it.)  False in every thread when the wait ran out.
-__device__ __forceinline__ bool block_wait(uint64_t* bar, uint32_t parity,
-                                           uint32_t polls = kMaxPolls) {
-  return __syncthreads_and(threadIdx.x == 0 ? mbar_wait(bar, parity, polls) : 1) != 0;
-}
-
-// Per-entry classification, stored as one byte per top-k entry.
-enum : int8_t {
-  kInvalid = 0, kRepeat = 1, kNewest = 2, kHit = 3, kBadPool = 4, kMiss = 5,
-  kResident = 6,  // served from a resident block (block tables)
-  kUnmapped = 7   // no source row through the source block table: treated as invalid
-};
 
 constexpr int kBloomBits = 17;  // request filter: 2^17 bits = 16 KB
 
@@ -93,13 +75,6 @@ __host__ __device__ inline int take(int* o, int bytes) {
   const int r = *o;
   *o += (bytes + 15) & ~15;
   return r;
-}
-
-// Hash-table size exponent: the smallest power of two >= mult * K.
-__host__ __device__ inline int hash_bits_for(int K, int mult) {
-  int bits = 2;  // the wide form keeps at least two pairs
-  while ((1 << bits) < mult * K) ++bits;
-  return bits;
 }
 
 // Shared-memory layout of one CTA.  Slices are whole 32-element chunks so a
@@ -190,111 +165,7 @@ enum {
   kMiscRowTimeout = 6  // some CTA of the row's cluster ran out
 };
 
-__device__ __forceinline__ uint32_t hash_of(int32_t key, int bits) {
-  return (static_cast<uint32_t>(key) * 2654435761u) >> (32 - bits);
-}
-
-// Bit of `key` in the request filter (a second multiplicative hash).
-__device__ __forceinline__ uint32_t bloom_bit(int32_t key) {
-  return (static_cast<uint32_t>(key) * 0x85EBCA6Bu) >> (32 - kBloomBits);
-}
-
-// The request hash: valid ids -> their canonical (smallest) top-k entry, by
-// open addressing with linear probing in one shared-memory region of
-// 4 * 2^bits bytes.  Packed form, used when the caller bounds every sequence
-// so that each valid id is below 2^(32 - eb) - 1: 2^bits words
-// `id << eb | entry`.  Wide form otherwise: 2^(bits - 1) pairs {id, entry}.
-// Empty slots are all ones in both forms, so one fill clears either.
-template <bool packed>
-struct ReqHash {
-  uint32_t* w;
-  int bits, eb;
-
-  static constexpr uint32_t kEmpty = 0xFFFFFFFFu;
-  __device__ __forceinline__ int nbits() const { return packed ? bits : bits - 1; }
-  __device__ __forceinline__ uint32_t mask() const { return (1u << nbits()) - 1u; }
-  __device__ __forceinline__ uint32_t first(int32_t key) const { return hash_of(key, nbits()); }
-  __device__ __forceinline__ int2* pairs() const { return reinterpret_cast<int2*>(w); }
-
-  // Inserts (key, i); true when the key was already present.
-  __device__ __forceinline__ bool insert(int32_t key, int32_t i) const {
-    const uint32_t m = mask();
-    uint32_t h = first(key);
-    if (packed) {
-      const uint32_t v = (static_cast<uint32_t>(key) << eb) | i;
-      for (uint32_t n = 0; n <= m; ++n) {
-        const uint32_t old = atomicCAS(&w[h], kEmpty, v);
-        if (old == kEmpty) return false;
-        if ((old >> eb) == static_cast<uint32_t>(key)) return true;
-        h = (h + 1u) & m;
-      }
-      return false;
-    }
-    for (uint32_t n = 0; n <= m; ++n) {
-      const int32_t old = atomicCAS(&pairs()[h].x, -1, key);
-      if (old == -1) {
-        pairs()[h].y = i;
-        return false;
-      }
-      if (old == key) return true;
-      h = (h + 1u) & m;
-    }
-    return false;
-  }
-  // Packed form: inserts (key, i) from slot h on; true when the key was already present.
-  __device__ __forceinline__ bool insert_from(int32_t key, int32_t i, uint32_t h) const {
-    const uint32_t m = mask();
-    const uint32_t v = (static_cast<uint32_t>(key) << eb) | i;
-    for (uint32_t n = 0; n < m; ++n) {
-      const uint32_t old = atomicCAS(&w[h], kEmpty, v);
-      if (old == kEmpty) return false;
-      if ((old >> eb) == static_cast<uint32_t>(key)) return true;
-      h = (h + 1u) & m;
-    }
-    return false;
-  }
-  // Lowers key's entry to i if i is smaller (the key is present).
-  __device__ __forceinline__ void make_min(int32_t key, int32_t i) const {
-    const uint32_t m = mask();
-    uint32_t h = first(key);
-    for (uint32_t n = 0; n <= m; ++n) {
-      if (packed) {
-        if ((w[h] >> eb) == static_cast<uint32_t>(key)) {
-          atomicMin(&w[h], (static_cast<uint32_t>(key) << eb) | i);
-          return;
-        }
-      } else if (pairs()[h].x == key) {
-        atomicMin(&pairs()[h].y, i);
-        return;
-      }
-      h = (h + 1u) & m;
-    }
-  }
-  // Entry of `key` looked up from slot h on; -1 when absent.
-  __device__ __forceinline__ int32_t find_from(int32_t key, uint32_t h) const {
-    const uint32_t m = mask();
-    if (packed) {
-      const uint32_t emask = (1u << eb) - 1u;
-      for (uint32_t n = 0; n <= m; ++n) {
-        const uint32_t v = w[h];
-        if (v == kEmpty) return -1;
-        if ((v >> eb) == static_cast<uint32_t>(key)) return static_cast<int32_t>(v & emask);
-        h = (h + 1u) & m;
-      }
-      return -1;
-    }
-    for (uint32_t n = 0; n <= m; ++n) {
-      const int2 kv = pairs()[h];
-      if (kv.x == key) return kv.y;
-      if (kv.x == -1) return -1;
-      h = (h + 1u) & m;
-    }
-    return -1;
-  }
-  __device__ __forceinline__ int32_t find(int32_t key) const { return find_from(key, first(key)); }
-};
-
-constexpr uint32_t kDrainPolls = 1u << 26;  // waiting out copies still in flight after a time-out
+__device__ __forceinline__ uint32_t bloom_bit(int32_t key) { return filter_bit(key, kBloomBits); }
 
 // The exit of a CTA whose bounded wait ran out (block-uniform; the CTA has
 // arrived at the row's first cluster barrier).  It completes both cluster
@@ -307,7 +178,7 @@ constexpr uint32_t kDrainPolls = 1u << 26;  // waiting out copies still in fligh
 __device__ __noinline__ void timeout_tail(const SwapInParams& p, int b, int j, int C,
                                           uint64_t* bar, bool ids_issued) {
   cluster_wait();
-  if (C > 1) cluster_arrive();
+  if (C > 1) cluster_arrive_relaxed();
   if (threadIdx.x == 0) {
     if (p.status) {
       if (j == 0)
@@ -322,27 +193,6 @@ __device__ __noinline__ void timeout_tail(const SwapInParams& p, int b, int j, i
   __syncthreads();
   if (C > 1) cluster_wait();
 }
-
-template <int G>
-struct Chunk;
-template <>
-struct Chunk<16> {
-  using T = uint4;
-  static __device__ __forceinline__ T ld(const unsigned char* p) { return ld_stream_v4(p); }
-  static __device__ __forceinline__ void st(unsigned char* p, T v) { st_l2_v4(p, v); }
-};
-template <>
-struct Chunk<4> {
-  using T = uint32_t;
-  static __device__ __forceinline__ T ld(const unsigned char* p) { return ld_stream_u32(p); }
-  static __device__ __forceinline__ void st(unsigned char* p, T v) { st_l2_u32(p, v); }
-};
-template <>
-struct Chunk<1> {
-  using T = uint32_t;
-  static __device__ __forceinline__ T ld(const unsigned char* p) { return ld_stream_u8(p); }
-  static __device__ __forceinline__ void st(unsigned char* p, T v) { st_l2_u8(p, v); }
-};
 
 // P6: copy this CTA's misses, work item = (miss, chunk).
 template <int G>
@@ -543,8 +393,11 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   // row's first write).
   const uint32_t polls_state = (p.fail_rank == j && p.fail_wait == 0) ? 0u : kMaxPolls;
   if (!block_wait(bar + 1, 0, polls_state)) {
-    if (tid == 0) misc[kMiscTimeout] = 1;
-    cluster_arrive();
+    if (tid == 0) {
+      misc[kMiscTimeout] = 1;
+      fence_acq_rel_cluster();
+    }
+    cluster_arrive_relaxed();
     timeout_tail(p, b, j, C, bar, ids_issued);
     return;
   }
@@ -612,11 +465,15 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   stage_finish(ids, pend_ids);
   const uint32_t polls_ids = (p.fail_rank == j && p.fail_wait == 1) ? 0u : kMaxPolls;
   const bool ids_ok = block_wait(bar, 0, polls_ids);
-  if (tid == 0 && !ids_ok) misc[kMiscTimeout] = 1;
   // Every CTA of the row has staged the state (and recorded whether its waits
-  // ran out) once all have arrived here; the matching wait comes right before
-  // the first write to that state.
-  cluster_arrive();
+  // ran out) once all have arrived here; the matching wait comes before the
+  // walk, well before the row's first write.  Thread 0, which saw the copies
+  // complete and wrote the outcome, releases; the others arrive relaxed.
+  if (tid == 0) {
+    if (!ids_ok) misc[kMiscTimeout] = 1;
+    fence_acq_rel_cluster();
+  }
+  cluster_arrive_relaxed();
   if (!ids_ok) {
     timeout_tail(p, b, j, C, bar, ids_issued);
     return;
@@ -714,6 +571,13 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     __syncthreads();
   }
 
+  // Every CTA of the row has staged its state and recorded whether a wait ran
+  // out.  Warp 0 reads the peers' outcomes from their shared memory now; the
+  // loads complete during the walk.
+  cluster_wait();
+  int peer_timeout = 0;
+  if (C > 1 && warp == 0 && lane < C) peer_timeout = peer_ld(peer_addr(&misc[kMiscTimeout], lane));
+
   // ---- P2: walk the LRU order; the lowest position holding a wanted token claims it.
   {
     uint32_t bw[IT];
@@ -748,7 +612,24 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     for (int k = 0; k < IT; ++k)
       if (f[k] >= 0) atomicMin(&claim[f[k]], k * kThreads + tid);
   }
+  if (C > 1 && warp == 0) {
+    const unsigned any = __ballot_sync(kFullMask, peer_timeout != 0);
+    if (lane == 0 && any) misc[kMiscRowTimeout] = 1;
+  }
   __syncthreads();
+  if (C > 1) {
+    // This CTA no longer reads its peers' shared memory: the second cluster
+    // barrier, waited on at exit, keeps every CTA alive until all have read.
+    cluster_arrive_relaxed();
+    if (misc[kMiscRowTimeout]) {  // a wait ran out in another CTA: leave the row alone
+      if (j == 0 && tid == 0) {
+        if (p.status) p.status[b] = HS_ST_TIMEOUT;
+        if (p.miss_count) p.miss_count[b] = 0;
+      }
+      cluster_wait();
+      return;
+    }
+  }
   // Pool rows of the miss candidates (wanted, not newest, not claimed), loaded
   // with LDGSTS now so the load overlaps P3.
   const bool id_repeat = misc[kMiscRepeat] != 0;
@@ -856,29 +737,6 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const int M = misc[kMiscMisses];
   const int E = H - NH;
   const int my_first_miss = e0 < K ? cnte[e0 >> 5] : M;
-  // The first state write of the row follows: wait until every CTA has staged.
-  cluster_wait();
-  if (C > 1) {
-    // The row goes ahead only if no CTA's wait ran out.  Each CTA reads its
-    // peers' outcomes from their shared memory (written before their arrive),
-    // then arrives at a second cluster barrier, waited on at exit, so that no
-    // CTA leaves while a peer may still read its shared memory.
-    if (warp == 0) {
-      const int t = lane < C ? peer_ld(peer_addr(&misc[kMiscTimeout], lane)) : 0;
-      const unsigned any = __ballot_sync(kFullMask, t != 0);
-      if (lane == 0) misc[kMiscRowTimeout] = any != 0u;
-    }
-    __syncthreads();
-    cluster_arrive();
-    if (misc[kMiscRowTimeout]) {  // another CTA's wait ran out: leave the row alone
-      if (j == 0 && tid == 0) {
-        if (p.status) p.status[b] = HS_ST_TIMEOUT;
-        if (p.miss_count) p.miss_count[b] = 0;
-      }
-      cluster_wait();
-      return;
-    }
-  }
   // Only my own entries: their chunks are whole and 32-aligned, so a warp's
   // ballot covers one chunk.
   int64_t my_pr = 0;
@@ -980,31 +838,6 @@ KernelFn pick_items(int items) {
   }
 }
 
-// Raises the dynamic shared-memory limit of a kernel once per device to the
-// largest size requested so far.
-hs_err ensure_smem(KernelFn fn, int device, int bytes) {
-  struct Entry {
-    KernelFn fn;
-    int device;
-    int bytes;
-  };
-  static std::mutex mu;
-  static Entry table[128];
-  static int n = 0;
-  std::lock_guard<std::mutex> lock(mu);
-  int slot = -1;
-  for (int i = 0; i < n; ++i)
-    if (table[i].fn == fn && table[i].device == device) slot = i;
-  if (slot >= 0 && table[slot].bytes >= bytes) return HS_OK;
-  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e != cudaSuccess) return fail(HS_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-  if (slot >= 0)
-    table[slot].bytes = bytes;
-  else if (n < 128)
-    table[n++] = Entry{fn, device, bytes};
-  return HS_OK;
-}
-
 // Cluster size for a batch: the largest power of two <= 8 with batch * C <=
 // SMs (at least 1), raised while the per-CTA state does not fit shared memory.
 int pick_cluster(int batch, int K, int H, int bits, const DeviceInfo& dev) {
@@ -1018,8 +851,9 @@ int pick_cluster(int batch, int K, int H, int bits, const DeviceInfo& dev) {
 }  // namespace hs
 
 extern "C" int64_t hs_swap_in_smem_bytes(int32_t top_k, int32_t hot_size) {
-  if (top_k < 1 || hot_size < 1 || hot_size > hs::kMaxItems * hs::kThreads || top_k > hot_size)
-    return 0;
+  if (top_k < 1 || hot_size < 1 || hot_size > 32767 || top_k > hot_size) return 0;
+  if (hot_size > hs::kMaxItems * hs::kThreads)  // one CTA per row
+    return hs::swap_in_rows_min_smem(top_k, hot_size, false);
   return hs::make_layout(top_k, hot_size, hs::kMaxCluster, hs::hash_bits_for(top_k, 2)).total;
 }
 
@@ -1030,66 +864,17 @@ namespace {
 // the last CTA of each row's cluster, else that rank (mod the cluster size).
 hs_err swap_in_launch(const hs_swap_in_args* a, hs_stream_t stream, int fail_rank,
                       int fail_wait) {
-  if (a == nullptr) return fail(HS_ERR_ARG, "hs_swap_in: args is NULL");
-  if (a->batch < 0 || a->top_k < 0)
-    return fail(HS_ERR_ARG, "hs_swap_in: batch (%d) and top_k (%d) must be >= 0", a->batch,
-                a->top_k);
-  if (a->hot_size < 1 || a->hot_size > 32767)
-    return fail(HS_ERR_UNSUPPORTED, "hs_swap_in: hot_size %d outside [1, 32767]", a->hot_size);
-  if (a->hot_size > kMaxItems * kThreads)
-    return fail(HS_ERR_UNSUPPORTED, "hs_swap_in: this build handles hot_size <= %d",
-                kMaxItems * kThreads);
-  if (a->top_k > a->hot_size)
-    return fail(HS_ERR_UNSUPPORTED, "hs_swap_in: top_k %d > hot_size %d", a->top_k,
-                a->hot_size);
-  if (a->row_bytes < 1) return fail(HS_ERR_ARG, "hs_swap_in: row_bytes must be >= 1");
-  if (a->flags & ~(HS_SEQ_LENS_I64 | HS_REQ_STATE_I64 | HS_OVERLAP_PREV))
-    return fail(HS_ERR_ARG, "hs_swap_in: unknown flags 0x%x", a->flags);
-  if (a->batch == 0 || a->top_k == 0) return HS_OK;
-
-  const struct {
-    const void* p;
-    const char* name;
-  } required[] = {{a->topk_ids, "topk_ids"},   {a->seq_lens, "seq_lens"},
-                  {a->req_state, "req_state"}, {a->slot_tokens, "slot_tokens"},
-                  {a->slot_rows, "slot_rows"}, {a->lru, "lru"},
-                  {a->pool_k, "pool_k"},       {a->hot_k, "hot_k"},
-                  {a->out_rows, "out_rows"}};
-  for (const auto& q : required)
-    if (q.p == nullptr) return fail(HS_ERR_ARG, "hs_swap_in: %s is NULL", q.name);
-  if ((a->pool_v == nullptr) != (a->hot_v == nullptr))
-    return fail(HS_ERR_ARG, "hs_swap_in: pool_v and hot_v must both be set or both be NULL");
-  const int64_t H = a->hot_size, K = a->top_k;
-  if (a->topk_stride < K || a->out_stride < K)
-    return fail(HS_ERR_ARG, "hs_swap_in: topk_stride/out_stride must be >= top_k");
-  if (a->slot_tokens_stride < H + 1 || a->slot_rows_stride < H + 1)
-    return fail(HS_ERR_ARG, "hs_swap_in: slot strides must be >= hot_size + 1");
-  if (a->lru_stride < H) return fail(HS_ERR_ARG, "hs_swap_in: lru_stride must be >= hot_size");
-  if ((a->miss_src == nullptr) != (a->miss_dst == nullptr))
-    return fail(HS_ERR_ARG, "hs_swap_in: miss_src and miss_dst must both be set or both be NULL");
-  if (a->miss_src != nullptr && (a->miss_count == nullptr || a->plan_stride < K))
-    return fail(HS_ERR_ARG, "hs_swap_in: the miss plan needs miss_count and plan_stride >= top_k");
-  if (a->miss_mask != nullptr && a->mask_stride < K)
-    return fail(HS_ERR_ARG, "hs_swap_in: mask_stride must be >= top_k");
-  if (a->pool_rows == nullptr && a->src_bt == nullptr)
-    return fail(HS_ERR_ARG, "hs_swap_in: pool_rows or src_bt is required");
-  if (a->src_bt == nullptr &&
-      (a->pool_rows_cols < 0 || a->pool_rows_stride < a->pool_rows_cols))
-    return fail(HS_ERR_ARG, "hs_swap_in: need 0 <= pool_rows_cols <= pool_rows_stride");
-  if (a->src_bt != nullptr &&
-      (a->src_block_size < 1 || a->src_bt_blocks < 0 || a->src_bt_stride < a->src_bt_blocks))
-    return fail(HS_ERR_ARG, "hs_swap_in: src_bt needs block size >= 1 and stride >= blocks");
-  if (a->res_bt != nullptr &&
-      (a->res_block_size < 1 || a->res_bt_blocks < 0 || a->res_bt_stride < a->res_bt_blocks))
-    return fail(HS_ERR_ARG, "hs_swap_in: res_bt needs block size >= 1 and stride >= blocks");
-  if (a->max_seq_len < 0) return fail(HS_ERR_ARG, "hs_swap_in: max_seq_len must be >= 0");
-  if (a->num_states < 1 || a->pool_num_rows < 0 || a->hot_num_rows < 0)
-    return fail(HS_ERR_ARG, "hs_swap_in: num_states >= 1, pool/hot row counts >= 0");
-  if (a->hot_num_rows > INT32_MAX)
-    return fail(HS_ERR_UNSUPPORTED, "hs_swap_in: hot_num_rows must fit int32");
+  bool empty = false;
+  hs_err err = check_swap_in_args(a, "hs_swap_in", 32767, &empty);
+  if (err != HS_OK || empty) return err;
+  if (a->hot_size > kMaxItems * kThreads)  // the one-CTA-per-row kernel takes larger rows
+    return swap_in_rows_launch(a, 1, stream, "hs_swap_in", fail_rank == -1 ? -1 : fail_wait);
+  SwapInDerived dv;
+  err = derive_swap_in(a, "hs_swap_in", &dv);
+  if (err != HS_OK) return err;
 
   DeviceInfo dev;
-  hs_err err = current_device(&dev);
+  err = current_device(&dev);
   if (err != HS_OK) return err;
   // A request hash of >= 8 slots per id in its packed form (load <= 1/8)
   // keeps probe chains short; smaller where shared memory is tight.
@@ -1109,28 +894,6 @@ hs_err swap_in_launch(const hs_swap_in_args* a, hs_stream_t stream, int fail_ran
                 a->top_k, a->hot_size, L.total, C, dev.max_smem_optin);
   if (static_cast<int64_t>(a->batch) * C > INT32_MAX)
     return fail(HS_ERR_UNSUPPORTED, "hs_swap_in: batch too large");
-
-  const MemKind pk = classify(a->pool_k);
-  const MemKind pv = a->pool_v ? classify(a->pool_v) : MemKind::kDevice;
-  for (MemKind k : {pk, pv})
-    if (k == MemKind::kUnregistered || k == MemKind::kUnknown)
-      return fail(HS_ERR_ARG,
-                  "hs_swap_in: pool memory must be device, managed or pinned host memory");
-  const MemKind hk = classify(a->hot_k);
-  const MemKind hv = a->hot_v ? classify(a->hot_v) : MemKind::kDevice;
-  for (MemKind k : {hk, hv})
-    if (k != MemKind::kDevice && k != MemKind::kManaged)
-      return fail(HS_ERR_ARG, "hs_swap_in: hot buffers must be device memory");
-
-  const uintptr_t align = reinterpret_cast<uintptr_t>(a->pool_k) |
-                          reinterpret_cast<uintptr_t>(a->hot_k) |
-                          reinterpret_cast<uintptr_t>(a->pool_v) |
-                          reinterpret_cast<uintptr_t>(a->hot_v) |
-                          static_cast<uintptr_t>(a->row_bytes);
-  const int G = (align & 15) == 0 ? 16 : ((align & 3) == 0 ? 4 : 1);
-  const uint64_t cpr = static_cast<uint64_t>(a->row_bytes) / G;
-  if (cpr * static_cast<uint64_t>(K) >= (1ull << 32))
-    return fail(HS_ERR_UNSUPPORTED, "hs_swap_in: top_k * row chunks must be < 2^32");
 
   SwapInParams p;
   p.top_k = a->top_k;
@@ -1178,33 +941,23 @@ hs_err swap_in_launch(const hs_swap_in_args* a, hs_stream_t stream, int fail_ran
   p.res_bt_blocks = a->res_bt_blocks;
   p.res_bs = a->res_block_size;
   p.res_null = a->res_null_block;
-  {
-    const uint32_t sbs = a->src_bt != nullptr ? static_cast<uint32_t>(a->src_block_size) : 1u;
-    const uint32_t rbs = a->res_bt != nullptr ? static_cast<uint32_t>(a->res_block_size) : 1u;
-    p.div_src_bs = FastDiv{fastdiv_magic(sbs), sbs};
-    p.div_res_bs = FastDiv{fastdiv_magic(rbs), rbs};
-  }
+  p.div_src_bs = dv.div_src_bs;
+  p.div_res_bs = dv.div_res_bs;
   p.mask_stride = a->mask_stride;
-  p.chunks_per_row = static_cast<uint32_t>(cpr);
-  p.div_chunks = FastDiv{fastdiv_magic(static_cast<uint32_t>(cpr)), static_cast<uint32_t>(cpr)};
+  p.chunks_per_row = dv.chunks_per_row;
+  p.div_chunks = FastDiv{fastdiv_magic(dv.chunks_per_row), dv.chunks_per_row};
   p.lay = L;
-  int eb = 1;  // bits of an entry index (K <= 2^eb)
-  while ((1 << eb) < a->top_k) ++eb;
-  p.entry_bits = eb;
+  p.entry_bits = dv.entry_bits;
   p.max_seq_len = a->max_seq_len;
-  p.copy_width = G;
+  p.copy_width = dv.copy_width;
   p.fail_rank = fail_rank == -1 ? -1 : (fail_rank < 0 ? C - 1 : fail_rank % C);
   p.fail_wait = fail_wait;
 
   int items = 1;
   while (items * kThreads < a->hot_size) items *= 2;
-  const bool tables = a->src_bt != nullptr || a->res_bt != nullptr;
-  // The packed hash needs every valid id (< max_seq_len) below 2^(32 - eb) - 1.
-  const bool packed = a->max_seq_len > 0 &&
-                      static_cast<uint64_t>(a->max_seq_len) - 1 < (1ull << (32 - p.entry_bits)) - 1;
-  KernelFn fn = tables ? (packed ? pick_items<true, true>(items) : pick_items<true, false>(items))
-                       : (packed ? pick_items<false, true>(items) : pick_items<false, false>(items));
-  err = ensure_smem(fn, dev.device, L.total);
+  KernelFn fn = dv.tables ? (dv.packed ? pick_items<true, true>(items) : pick_items<true, false>(items))
+                          : (dv.packed ? pick_items<false, true>(items) : pick_items<false, false>(items));
+  err = ensure_smem(reinterpret_cast<const void*>(fn), dev.device, L.total);
   if (err != HS_OK) return err;
 
   cudaLaunchConfig_t cfg = {};
@@ -1227,6 +980,131 @@ hs_err swap_in_launch(const hs_swap_in_args* a, hs_stream_t stream, int fail_ran
 }
 
 }  // namespace
+}  // namespace hs
+
+namespace hs {
+
+hs_err check_swap_in_args(const hs_swap_in_args* a, const char* who, int max_hot_size,
+                          bool* empty) {
+  *empty = false;
+  if (a == nullptr) return fail(HS_ERR_ARG, "%s: args is NULL", who);
+  if (a->batch < 0 || a->top_k < 0)
+    return fail(HS_ERR_ARG, "%s: batch (%d) and top_k (%d) must be >= 0", who, a->batch,
+                a->top_k);
+  if (a->hot_size < 1 || a->hot_size > max_hot_size)
+    return fail(HS_ERR_UNSUPPORTED, "%s: hot_size %d outside [1, %d]", who, a->hot_size,
+                max_hot_size);
+  if (a->top_k > a->hot_size)
+    return fail(HS_ERR_UNSUPPORTED, "%s: top_k %d > hot_size %d", who, a->top_k, a->hot_size);
+  if (a->row_bytes < 1) return fail(HS_ERR_ARG, "%s: row_bytes must be >= 1", who);
+  if (a->flags & ~(HS_SEQ_LENS_I64 | HS_REQ_STATE_I64 | HS_OVERLAP_PREV))
+    return fail(HS_ERR_ARG, "%s: unknown flags 0x%x", who, a->flags);
+  if (a->batch == 0 || a->top_k == 0) {
+    *empty = true;
+    return HS_OK;
+  }
+  const struct {
+    const void* p;
+    const char* name;
+  } required[] = {{a->topk_ids, "topk_ids"},   {a->seq_lens, "seq_lens"},
+                  {a->req_state, "req_state"}, {a->slot_tokens, "slot_tokens"},
+                  {a->slot_rows, "slot_rows"}, {a->lru, "lru"},
+                  {a->pool_k, "pool_k"},       {a->hot_k, "hot_k"},
+                  {a->out_rows, "out_rows"}};
+  for (const auto& q : required)
+    if (q.p == nullptr) return fail(HS_ERR_ARG, "%s: %s is NULL", who, q.name);
+  if ((a->pool_v == nullptr) != (a->hot_v == nullptr))
+    return fail(HS_ERR_ARG, "%s: pool_v and hot_v must both be set or both be NULL", who);
+  const int64_t H = a->hot_size, K = a->top_k;
+  if (a->topk_stride < K || a->out_stride < K)
+    return fail(HS_ERR_ARG, "%s: topk_stride/out_stride must be >= top_k", who);
+  if (a->slot_tokens_stride < H + 1 || a->slot_rows_stride < H + 1)
+    return fail(HS_ERR_ARG, "%s: slot strides must be >= hot_size + 1", who);
+  if (a->lru_stride < H) return fail(HS_ERR_ARG, "%s: lru_stride must be >= hot_size", who);
+  if ((a->miss_src == nullptr) != (a->miss_dst == nullptr))
+    return fail(HS_ERR_ARG, "%s: miss_src and miss_dst must both be set or both be NULL", who);
+  if (a->miss_src != nullptr && (a->miss_count == nullptr || a->plan_stride < K))
+    return fail(HS_ERR_ARG, "%s: the miss plan needs miss_count and plan_stride >= top_k", who);
+  if (a->miss_mask != nullptr && a->mask_stride < K)
+    return fail(HS_ERR_ARG, "%s: mask_stride must be >= top_k", who);
+  if (a->pool_rows == nullptr && a->src_bt == nullptr)
+    return fail(HS_ERR_ARG, "%s: pool_rows or src_bt is required", who);
+  if (a->src_bt == nullptr &&
+      (a->pool_rows_cols < 0 || a->pool_rows_stride < a->pool_rows_cols))
+    return fail(HS_ERR_ARG, "%s: need 0 <= pool_rows_cols <= pool_rows_stride", who);
+  if (a->src_bt != nullptr &&
+      (a->src_block_size < 1 || a->src_bt_blocks < 0 || a->src_bt_stride < a->src_bt_blocks))
+    return fail(HS_ERR_ARG, "%s: src_bt needs block size >= 1 and stride >= blocks", who);
+  if (a->res_bt != nullptr &&
+      (a->res_block_size < 1 || a->res_bt_blocks < 0 || a->res_bt_stride < a->res_bt_blocks))
+    return fail(HS_ERR_ARG, "%s: res_bt needs block size >= 1 and stride >= blocks", who);
+  if (a->max_seq_len < 0) return fail(HS_ERR_ARG, "%s: max_seq_len must be >= 0", who);
+  if (a->num_states < 1 || a->pool_num_rows < 0 || a->hot_num_rows < 0)
+    return fail(HS_ERR_ARG, "%s: num_states >= 1, pool/hot row counts >= 0", who);
+  if (a->hot_num_rows > INT32_MAX)
+    return fail(HS_ERR_UNSUPPORTED, "%s: hot_num_rows must fit int32", who);
+  return HS_OK;
+}
+
+hs_err derive_swap_in(const hs_swap_in_args* a, const char* who, SwapInDerived* d) {
+  const MemKind pk = classify(a->pool_k);
+  const MemKind pv = a->pool_v ? classify(a->pool_v) : MemKind::kDevice;
+  for (MemKind k : {pk, pv})
+    if (k == MemKind::kUnregistered || k == MemKind::kUnknown)
+      return fail(HS_ERR_ARG, "%s: pool memory must be device, managed or pinned host memory",
+                  who);
+  const MemKind hk = classify(a->hot_k);
+  const MemKind hv = a->hot_v ? classify(a->hot_v) : MemKind::kDevice;
+  for (MemKind k : {hk, hv})
+    if (k != MemKind::kDevice && k != MemKind::kManaged)
+      return fail(HS_ERR_ARG, "%s: hot buffers must be device memory", who);
+  const uintptr_t align = reinterpret_cast<uintptr_t>(a->pool_k) |
+                          reinterpret_cast<uintptr_t>(a->hot_k) |
+                          reinterpret_cast<uintptr_t>(a->pool_v) |
+                          reinterpret_cast<uintptr_t>(a->hot_v) |
+                          static_cast<uintptr_t>(a->row_bytes);
+  d->copy_width = (align & 15) == 0 ? 16 : ((align & 3) == 0 ? 4 : 1);
+  const uint64_t cpr = static_cast<uint64_t>(a->row_bytes) / d->copy_width;
+  if (cpr * static_cast<uint64_t>(a->top_k) >= (1ull << 32))
+    return fail(HS_ERR_UNSUPPORTED, "%s: top_k * row chunks must be < 2^32", who);
+  d->chunks_per_row = static_cast<uint32_t>(cpr);
+  int eb = 1;  // bits of an entry index (K <= 2^eb)
+  while ((1 << eb) < a->top_k) ++eb;
+  d->entry_bits = eb;
+  // The packed hash needs every valid id (< max_seq_len) below 2^(32 - eb) - 1.
+  d->packed = a->max_seq_len > 0 &&
+              static_cast<uint64_t>(a->max_seq_len) - 1 < (1ull << (32 - eb)) - 1;
+  d->tables = a->src_bt != nullptr || a->res_bt != nullptr;
+  const uint32_t sbs = a->src_bt != nullptr ? static_cast<uint32_t>(a->src_block_size) : 1u;
+  const uint32_t rbs = a->res_bt != nullptr ? static_cast<uint32_t>(a->res_block_size) : 1u;
+  d->div_src_bs = FastDiv{fastdiv_magic(sbs), sbs};
+  d->div_res_bs = FastDiv{fastdiv_magic(rbs), rbs};
+  return HS_OK;
+}
+
+hs_err ensure_smem(const void* fn, int device, int bytes) {
+  struct Entry {
+    const void* fn;
+    int device;
+    int bytes;
+  };
+  static std::mutex mu;
+  static Entry table[256];
+  static int n = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  int slot = -1;
+  for (int i = 0; i < n; ++i)
+    if (table[i].fn == fn && table[i].device == device) slot = i;
+  if (slot >= 0 && table[slot].bytes >= bytes) return HS_OK;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return fail(HS_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+  if (slot >= 0)
+    table[slot].bytes = bytes;
+  else if (n < 256)
+    table[n++] = Entry{fn, device, bytes};
+  return HS_OK;
+}
+
 }  // namespace hs
 
 extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
