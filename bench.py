@@ -627,6 +627,24 @@ def time_launches(fn, reps, stream, flush):
     return statistics.mean(a.elapsed_time(b) / 1e3 for a, b in ts)
 
 
+def time_replayed(call, R, stream, reps=8):
+    """Seconds per call of `call(i)`, i < R, captured back to back in one CUDA
+    graph and replayed `reps` times after one untimed replay."""
+    with torch.cuda.stream(stream):
+        for i in range(R):  # eager once: one-time set-up outside the capture
+            call(i)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        for i in range(R):
+            call(i)
+    torch.cuda.synchronize()
+    t = timed_graphs([gr] + [gr] * reps, stream)  # the first replay warms the graph
+    t1 = timed_graphs([gr], stream)
+    del gr
+    return (t - t1) / (R * reps) if t > t1 else t / (R * (reps + 1))
+
+
 def run_store_kv(dev, hbm_peak, flush, stream):
     import sparse_attention_kv_row_gb300 as hs
 
@@ -645,12 +663,25 @@ def run_store_kv(dev, hbm_peak, flush, stream):
             hs.store_kv(k, v, kd, vd, loc, stream=stream)
     t = time_launches(lambda: hs.store_kv(k, v, kd, vd, loc, stream=stream), 30, stream, flush)
     alg = 2 * 2 * n * S + 8 * n
-    del kd, vd
+    # Back to back: a graph of R calls, each with its own sources and token
+    # slots, so what one call reads or writes is not in L2 for the next.
+    R = 16
+    ks = [torch.randn((n, heads, hd), generator=g, device=dev).to(torch.bfloat16) for _ in range(R)]
+    vs = [torch.randn((n, heads, hd), generator=g, device=dev).to(torch.bfloat16) for _ in range(R)]
+    locs = [torch.randperm(rows, generator=g, device=dev)[:n] for _ in range(R)]
+    rep = time_replayed(lambda i: hs.store_kv(ks[i], vs[i], kd, vd, locs[i], stream=stream), R,
+                        stream)
+    del kd, vd, ks, vs
     torch.cuda.empty_cache()
     return dict(workload=c["name"], us_per_call=t * 1e6, alg_bytes=alg, gbs=alg / t / 1e9,
                 roofline=dict(bound="hbm", achieved=alg / t / 1e9, peak=hbm_peak,
                               frac=alg / t / 1e9 / hbm_peak), launches_timed=30,
-                l2="flushed before every launch (256 MiB written, then read)")
+                l2="flushed before every launch (256 MiB written, then read)",
+                replayed=dict(us_per_call=rep * 1e6, gbs=alg / rep / 1e9,
+                              frac=alg / rep / 1e9 / hbm_peak, calls_per_graph=R,
+                              how=f"a CUDA graph of {R} back-to-back calls, each with its own "
+                                  "K/V sources and 4096 distinct destination rows (268 MB of "
+                                  "sources, > L2), replayed 8 times"))
 
 
 def run_fp8_store(dev, hbm_peak, flush, stream):
@@ -676,14 +707,26 @@ def run_fp8_store(dev, hbm_peak, flush, stream):
             fn()
     t = time_launches(fn, 30, stream, flush)
     alg = 2 * n * heads * hd * (2 + 1) + 8 * n
-    del kc, vc
+    R = 16
+    kk = [torch.randn((n, heads, hd), generator=g, device=dev).to(torch.bfloat16) for _ in range(R)]
+    vv = [torch.randn((n, heads, hd), generator=g, device=dev).to(torch.bfloat16) for _ in range(R)]
+    locs = [torch.randperm(slots, generator=g, device=dev)[:n] for _ in range(R)]
+    rep = time_replayed(lambda i: hs.fp8_store_kv(kk[i], vv[i], kc, vc, locs[i], k_scale=ks,
+                                                  v_scale=vs, page_size=ps, stream=stream),
+                        R, stream)
+    del kc, vc, kk, vv
     torch.cuda.empty_cache()
     return dict(workload="fp8 KV write: 4096 tokens x [8 x 128] bf16 K and V -> e4m3 paged "
                          "caches (2^20 slots, pages of 16), scales given",
                 us_per_call=t * 1e6, alg_bytes=alg, gbs=alg / t / 1e9,
                 roofline=dict(bound="hbm", achieved=alg / t / 1e9, peak=hbm_peak,
                               frac=alg / t / 1e9 / hbm_peak), launches_timed=30,
-                l2="flushed before every launch (256 MiB written, then read)")
+                l2="flushed before every launch (256 MiB written, then read)",
+                replayed=dict(us_per_call=rep * 1e6, gbs=alg / rep / 1e9,
+                              frac=alg / rep / 1e9 / hbm_peak, calls_per_graph=R,
+                              how=f"a CUDA graph of {R} back-to-back calls, each with its own "
+                                  "K/V sources and 4096 distinct destination slots, replayed "
+                                  "8 times"))
 
 
 def run_host_link_peak(dev, stream, pinned):
@@ -760,6 +803,48 @@ def run_swapin_cfg(cfg, dev, stream, steps, hbm_peak, link_peak, flush=None, sha
     return res
 
 
+def run_layers_op(dev, stream, hbm_peak, layers, steps=20):
+    """The layers variant on its own (for profiling): `layers` DeepSeek-V3.2
+    layers, each with its own state and hot buffer, sharing one 2.75 GB HBM
+    pool, resolved by one hs_swap_in_layers launch per step (graphs, back to
+    back, after the warm-up to the steady state)."""
+    import dataclasses
+
+    cfg = dataclasses.replace(synth.DSV32, layers=layers,
+                              name=synth.DSV32.name + f" [{layers} layers, one shared pool]")
+    B, K, H, S = cfg.batch, cfg.top_k, cfg.hot_size, cfg.row_bytes
+    w = SwapInWorkload(cfg, dev, layers, 0, n_pools=1)
+    w.overlap = False
+    hs = w.hs
+
+    def capture(topk):
+        arr = hs.layer_args_array([w.args(l, topk[l]) for l in range(layers)])
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            hs.swap_in_layers(arr, stream)
+        return gr, arr
+
+    with torch.cuda.stream(stream):
+        for _ in range(cfg.warm_steps):
+            hs.swap_in_layers([w.args(l, t) for l, t in enumerate(w.next_topk())], stream)
+    torch.cuda.synchronize()
+    caps = [capture(w.next_topk().clone()) for _ in range(steps + 2)]
+    graphs = [c[0] for c in caps]
+    timed_graphs(graphs[:2], stream)
+    w.stats.zero_()
+    torch.cuda.synchronize()
+    t = timed_graphs(graphs[2:], stream)
+    hits, misses = (int(x) for x in w.stats.cpu())
+    alg = swapin_alg_bytes(B, K, H, S, layers * steps, misses)
+    del graphs, caps
+    w.free()
+    torch.cuda.empty_cache()
+    return dict(workload=cfg.name, us_per_launch=t / steps * 1e6, rows_per_s=misses / t,
+                alg_bytes_per_launch=alg / steps,
+                roofline=dict(bound="hbm", achieved=alg / t / 1e9, peak=hbm_peak,
+                              frac=alg / t / 1e9 / hbm_peak, unit="GB/s"))
+
+
 def dsv32_block_tables(w, bs=64, recent=4096):
     """Block tables for the DeepSeek-V3.2 layer: token blocks of 64 map to the pool
     blocks that pool_rows uses, shifted by one so that no live block is the null
@@ -777,7 +862,9 @@ def dsv32_block_tables(w, bs=64, recent=4096):
                 res_block_size=bs, res_null_block=-1)
 
 
-def run_transfer(dev, stream, link_peak, hot_rows_target):
+def run_transfer(dev, stream, link_peak, hot_rows_target, host=True, hbm_peak=None):
+    """The all-layer transfer: 61 layers x 78,592 pairs of 656 B rows, from
+    per-layer pools in pinned host memory (host link) or in HBM (HBM to HBM)."""
     import sparse_attention_kv_row_gb300 as hs
 
     c = synth.TRANSFER
@@ -790,9 +877,13 @@ def run_transfer(dev, stream, link_peak, hot_rows_target):
     stage = torch.empty((src_rows, S), dtype=torch.uint8, device=dev)
     src = []
     for l in range(NL):
-        t = torch.empty((src_rows, S), dtype=torch.uint8, pin_memory=True)
-        synth.fill_rows_torch(stage, synth.stream_key(c["seed"], l))
-        t.copy_(stage)
+        if host:
+            t = torch.empty((src_rows, S), dtype=torch.uint8, pin_memory=True)
+            synth.fill_rows_torch(stage, synth.stream_key(c["seed"], l))
+            t.copy_(stage)
+        else:
+            t = torch.empty((src_rows, S), dtype=torch.uint8, device=dev)
+            synth.fill_rows_torch(t, synth.stream_key(c["seed"], l))
         src.append(t)
     del stage
     dst_rows = hot_rows_target
@@ -815,12 +906,29 @@ def run_transfer(dev, stream, link_peak, hot_rows_target):
     for _ in range(32):
         l, i = int(rng.integers(NL)), int(rng.integers(n))
         ok &= bool(torch.equal(dst[l][di[i]].cpu(), src[l][si[i]]))
-    res = dict(workload=c["name"] + f" (src pools {src_rows} rows/layer pinned; dst 61 HBM "
+    where = "pinned" if host else "HBM"
+    res = dict(workload=c["name"] + f" (src pools {src_rows} rows/layer {where}; dst 61 HBM "
                                     f"buffers of {dst_rows} rows; indices seeded distinct)",
                ms_per_call=t * 1e3, rows_per_s=n * NL / t, alg_bytes=alg, gbs=alg / t / 1e9,
-               sampled_check_ok=ok,
-               roofline=dict(bound="host_link", achieved=link_bytes / t / 1e9, peak=link_peak,
-                             frac=link_bytes / t / 1e9 / link_peak, unit="GB/s"))
+               sampled_check_ok=ok)
+    if host:
+        res["roofline"] = dict(bound="host_link", achieved=link_bytes / t / 1e9, peak=link_peak,
+                               frac=link_bytes / t / 1e9 / link_peak, unit="GB/s")
+    else:
+        res["roofline"] = dict(bound="hbm", achieved=alg / t / 1e9, peak=hbm_peak,
+                               frac=alg / t / 1e9 / hbm_peak, unit="GB/s")
+        # the per-layer form: one launch per layer (61 launches in a graph, back to back)
+        one = [(hs.layer_pointer_array([src[l]], dev), hs.layer_pointer_array([dst[l]], dev))
+               for l in range(NL)]
+        torch.cuda.synchronize()
+        rep = time_replayed(lambda l: hs.transfer_kv_layers([src[l]], [dst[l]], src_idx, dst_idx,
+                                                            stream=stream, ptrs=one[l]),
+                            NL, stream, reps=2)
+        alg1 = 2 * n * S + 16 * n
+        res["per_layer"] = dict(us_per_call=rep * 1e6, gbs=alg1 / rep / 1e9,
+                                frac=alg1 / rep / 1e9 / hbm_peak,
+                                how="hs_transfer_kv with num_layers=1, one launch per layer, "
+                                    "61 launches captured back to back in a CUDA graph")
     del src, dst
     torch.cuda.empty_cache()
     return res
@@ -1012,7 +1120,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: fewer layers than the workload's 61")
     ap.add_argument("--op", choices=["store_kv", "fp8_store_kv", "dsv32_layer_swap_in",
-                                     "tables_swap_in", "indexer_swap_in", "stress_swap_in"],
+                                     "tables_swap_in", "indexer_swap_in", "stress_swap_in",
+                                     "layers_swap_in"],
                     default=None,
                     help="profiling only: run this one secondary line and print it")
     args = ap.parse_args()
@@ -1063,7 +1172,9 @@ def main():
     if args.op is not None:  # one secondary line on its own (for ncu)
         s_ = torch.cuda.Stream(dev)
         flush_ = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-        if args.op in ("store_kv", "fp8_store_kv"):
+        if args.op == "layers_swap_in":
+            out_ = run_layers_op(dev, s_, hbm_peak, args.layers or 8)
+        elif args.op in ("store_kv", "fp8_store_kv"):
             fn_ = run_store_kv if args.op == "store_kv" else run_fp8_store
             out_ = fn_(dev, hbm_peak, flush_, s_)
         elif args.op in ("indexer_swap_in", "stress_swap_in"):
@@ -1094,6 +1205,11 @@ def main():
         ops["fp8_store_kv"] = run_fp8_store(dev, hbm_peak, flush, s)
         ops["tiny_swap_in"] = run_swapin_cfg(synth.TINY, dev, s, 8, hbm_peak, None, flush=flush,
                                              shared_pool=True)
+        tiny_rep = run_swapin_cfg(synth.TINY, dev, s, 64, hbm_peak, None, shared_pool=True)
+        ops["tiny_swap_in"]["replayed"] = dict(
+            us_per_call=tiny_rep["us_per_call"], launches_timed=64,
+            how="64 decode steps, one graph each, replayed back to back (no L2 flush: the "
+                "workload's 21 KB stays in L2 by nature)")
         probe_buf = torch.empty(2 * GiB, dtype=torch.uint8, pin_memory=True)
         link = run_host_link_peak(dev, s, probe_buf)
         del probe_buf
@@ -1113,6 +1229,9 @@ def main():
         ops["tables_swap_in"] = tb
         ops["transfer_all_layer"] = run_transfer(dev, s, link["peak_gbs"],
                                                  synth.STRESS.batch * (synth.STRESS.hot_size + 1))
+        ops["transfer_all_layer_hbm"] = run_transfer(
+            dev, s, link["peak_gbs"], synth.STRESS.batch * (synth.STRESS.hot_size + 1),
+            host=False, hbm_peak=hbm_peak)
 
     if rank != 0:
         if dist:

@@ -123,18 +123,31 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
       "r"(bytes)
       : "memory");
 }
-// Polls for the completion of phase `parity`, at most `max_polls` times;
-// returns false if the phase did not complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_polls) {
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Each poll lets the thread sleep until the phase completes, for at most this
+// long: a waiting thread issues a handful of instructions, not one poll every
+// few cycles that takes issue slots from the warps still working.
+constexpr uint32_t kPollSleepNs = 100000;
+// Waits for the completion of phase `parity`: at most `max_polls` polls and at
+// most `limit_ns` nanoseconds; false if the phase did not complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t max_polls,
+                                          uint64_t limit_ns = 1000000000ull) {
+  const uint64_t t0 = max_polls != 0 ? global_ns() : 0ull;
   for (uint32_t n = 0; n < max_polls; ++n) {
     uint32_t done;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(kPollSleepNs)
         : "memory");
     if (done) return true;
+    if (global_ns() - t0 > limit_ns) return false;
   }
   return false;
 }
@@ -327,6 +340,34 @@ __device__ __forceinline__ void cluster_sync() {
 }
 
 // ------------------------------------------------------------------ block scan
+// Exclusive prefix sum of v over the block's threads in thread order; `wsum`
+// is shared scratch of >= 33 ints.  Returns the prefix and, in *total, the
+// block sum.  Every thread of the block must call it.
+__device__ __forceinline__ int block_exclusive_sum(int v, int* wsum, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  int x = v;
+#pragma unroll
+  for (int d = 1; d < kWarp; d <<= 1) {
+    const int y = __shfl_up_sync(kFullMask, x, d);
+    if (lane >= d) x += y;
+  }
+  if (lane == kWarp - 1) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    const int t = lane < nwarps ? wsum[lane] : 0;
+    int tot;
+    const int ex = warp_exclusive_scan(t, lane, &tot);
+    if (lane < nwarps) wsum[lane] = ex;
+    if (lane == 0) wsum[32] = tot;
+  }
+  __syncthreads();
+  const int r = wsum[warp] + x - v;
+  *total = wsum[32];
+  __syncthreads();  // wsum may be reused right away
+  return r;
+}
+
 // Exclusive prefix of `flag` over the threads of the block in thread order;
 // `wsum` is shared scratch of >= 33 ints.  Returns the prefix and, in *total,
 // the block total.  Every thread of the block must call it.

@@ -187,8 +187,8 @@ __device__ __noinline__ void timeout_tail(const SwapInParams& p, int b, int j, i
         atomicOr(p.status + b, HS_ST_TIMEOUT);
     }
     if (j == 0 && p.miss_count) p.miss_count[b] = 0;
-    mbar_wait(bar + 1, 0, kDrainPolls);
-    if (ids_issued) mbar_wait(bar, 0, kDrainPolls);
+    mbar_wait(bar + 1, 0, kDrainPolls, kDrainNs);
+    if (ids_issued) mbar_wait(bar, 0, kDrainPolls, kDrainNs);
   }
   __syncthreads();
   if (C > 1) cluster_wait();

@@ -13,8 +13,9 @@
 namespace hs {
 
 constexpr int32_t kUnclaimed = INT_MAX;
-constexpr uint32_t kMaxPolls = 1u << 22;    // bounded mbarrier waits
+constexpr uint32_t kMaxPolls = 1u << 22;    // bounded mbarrier waits (and at most 1 s each)
 constexpr uint32_t kDrainPolls = 1u << 26;  // waiting out copies still in flight after a time-out
+constexpr uint64_t kDrainNs = 16000000000ull;  // ... for at most 16 s
 
 // Waits until the phase of `bar` with the given parity has completed: thread
 // 0 polls (a bounded wait) while the other threads wait at the block barrier,

@@ -26,11 +26,11 @@
 //      hits     claimed entries set their position's bit in a hit bitmap;
 //               candidates fetch their pool rows with LDGSTS;
 //   P3 ranks    popc of the bitmap words and one warp scan give each position
-//               its hits-before count; evictables are listed in LRU order
-//               (the first K: a row never has more misses);
+//               its hits-before count;
 //   P4 misses   ballot/popc over entries in top-k order gives each miss its
-//               rank m; miss m takes evictable m, emits its hot row and
-//               records the slot's new token;
+//               rank m; miss m takes the m-th non-hit position in LRU order
+//               (found by a binary search over the word prefixes), emits its
+//               hot row and records the slot's new token;
 //   P5 LRU      the new order [stale evictables][misses][hits] is built in
 //               shared memory and stored coalesced;
 //   P6 copy     (miss, chunk) items over all threads, loads before stores.
@@ -54,13 +54,20 @@ constexpr int kRowMaxLayers = 64;   // layers per launch (kernel-parameter space
 
 // Shared-memory layout of one CTA, computed on the host.  Regions whose
 // contents are dead by a later phase are reused: the hash region holds the
-// misses' pool rows for the copy (it is >= 8K bytes), the token region the
-// candidates' pool rows (without block tables) and then the new LRU order.
+// misses' source and destination byte offsets for the copy (it is >= 16K
+// bytes), the token region the candidates' pool rows (without block tables)
+// and then the new LRU order.
+// The request map: valid id -> its canonical (smallest) top-k entry.
+enum : int { kMapWide = 0, kMapPacked = 1, kMapDirect = 2 };
+
 struct RowLayout {
   int hash_bits;
+  int map;                    // kMapWide / kMapPacked / kMapDirect
+  int direct_words;           // bitmap words of the direct map (max_seq_len / 32, rounded up)
+  int o_dpre, o_dent;         // direct map: word prefixes (uint16), dense rank -> entry (int32)
   int stage_tok, stage_rows;  // slot tokens / slot rows staged (else read from global memory)
-  int o_hash, o_filter, o_ids, o_lru, o_tok, o_prs, o_rows, o_claim, o_evl, o_code;
-  int o_sbits, o_dup, o_hit, o_cntp, o_cnte, o_misc, o_bar;
+  int o_hash, o_filter, o_ids, o_lru, o_tok, o_prs, o_rows, o_claim, o_code;
+  int o_sbits, o_dup, o_hit, o_cntp, o_cnte, o_misc, o_wsum, o_bar;
   int total;
 };
 
@@ -70,16 +77,30 @@ inline int take_(int* o, int64_t bytes) {
   return r;
 }
 
-RowLayout make_row_layout(int K, int H, int bits, bool stage_tok, bool stage_rows,
-                          bool tables) {
+// map: kMapDirect takes max_len (the caller's sequence bound) and ignores
+// bits; the hash forms take bits.
+RowLayout make_row_layout(int K, int H, int map, int bits, int64_t max_len, bool stage_tok,
+                          bool stage_rows, bool tables) {
   RowLayout L{};
+  L.map = map;
   L.hash_bits = bits;
   L.stage_tok = stage_tok;
   L.stage_rows = stage_rows;
   const int64_t k = K, h = H, nw = (H + 31) / 32;
   int o = 0;
-  L.o_hash = take_(&o, std::max<int64_t>(int64_t{4} << bits, 8 * k));
-  L.o_filter = take_(&o, 4 << (kRowFilterBits - 5));
+  if (map == kMapDirect) {  // bitmap | word prefixes | rank -> entry, then the copy offsets
+    const int64_t dw = (max_len + 31) / 32;
+    L.direct_words = static_cast<int>(dw);
+    const int64_t pre = (4 * dw + 15) & ~int64_t{15};
+    const int64_t ent = pre + ((2 * dw + 15) & ~int64_t{15});
+    L.o_hash = take_(&o, std::max<int64_t>(ent + 4 * k, 16 * k));
+    L.o_dpre = L.o_hash + static_cast<int>(pre);
+    L.o_dent = L.o_hash + static_cast<int>(ent);
+    L.o_filter = take_(&o, 0);
+  } else {
+    L.o_hash = take_(&o, std::max<int64_t>(int64_t{4} << bits, 16 * k));
+    L.o_filter = take_(&o, 4 << (kRowFilterBits - 5));
+  }
   L.o_ids = take_(&o, 4 * k + 16);
   L.o_lru = take_(&o, 2 * h + 16);
   int64_t tok_bytes = 2 * h + 16;  // the new LRU order
@@ -89,7 +110,6 @@ RowLayout make_row_layout(int K, int H, int bits, bool stage_tok, bool stage_row
   L.o_prs = tables ? take_(&o, 8 * k) : L.o_tok;
   L.o_rows = stage_rows ? take_(&o, 4 * (h + 1) + 16) : 0;
   L.o_claim = take_(&o, 4 * k);
-  L.o_evl = take_(&o, 4 * k);
   L.o_code = take_(&o, k);
   L.o_sbits = take_(&o, 4 * nw);
   L.o_dup = take_(&o, 4 * nw);
@@ -97,6 +117,7 @@ RowLayout make_row_layout(int K, int H, int bits, bool stage_tok, bool stage_row
   L.o_cntp = take_(&o, 4 * nw);
   L.o_cnte = take_(&o, 4 * ((k + 31) / 32));
   L.o_misc = take_(&o, 64);
+  L.o_wsum = take_(&o, 4 * 33);
   L.o_bar = take_(&o, 16);
   L.total = o;
   return L;
@@ -162,19 +183,43 @@ __device__ __noinline__ void rows_timeout_exit(int32_t* status, int32_t* miss_co
   if (threadIdx.x == 0) {
     if (status) status[b] = HS_ST_TIMEOUT;
     if (miss_count) miss_count[b] = 0;
-    mbar_wait(bar + 1, 0, kDrainPolls);
-    if (ids_issued) mbar_wait(bar, 0, kDrainPolls);
+    mbar_wait(bar + 1, 0, kDrainPolls, kDrainNs);
+    if (ids_issued) mbar_wait(bar, 0, kDrainPolls, kDrainNs);
   }
   __syncthreads();
 }
 
-// P6: copy misses [0, n): pool row src[m] -> hot row dst[m] (skipped when < 0).
+// The direct request map, used when the caller bounds the sequence length:
+// one bit per token id of the row marks the requested ids; a word's prefix
+// (set bits in the words before it) plus the popc of its lower bits is the
+// id's dense rank among the requested ids; ent[rank] is the id's canonical
+// (smallest) top-k entry.  A lookup is three shared loads and no probe loop.
+struct DirectMap {
+  uint32_t* bm;
+  uint16_t* pre;
+  int32_t* ent;
+  // The rank of a requested id (its bit is set).
+  __device__ __forceinline__ int rank(int32_t t, uint32_t w) const {
+    return pre[t >> 5] + __popc(w & ((1u << (t & 31)) - 1u));
+  }
+  // Entry of a valid id, -1 when it is not requested.
+  __device__ __forceinline__ int32_t find(int32_t t) const {
+    const uint32_t w = bm[t >> 5];
+    if (!((w >> (t & 31)) & 1u)) return -1;
+    return ent[rank(t, w)];
+  }
+};
+
+// P6: copy misses [0, n): the row at byte offset src[m] of the pool goes to
+// byte offset dst[m] of the hot buffer (skipped when dst[m] < 0).  Work items
+// are (miss, chunk) over all threads, kRowCopyUnroll loads before the stores.
 template <int G>
 __device__ __forceinline__ void copy_misses(const RowCommon& p, const unsigned char* pool,
                                             unsigned char* hot, int n, const int64_t* src,
-                                            const int32_t* dst) {
+                                            const int64_t* dst) {
   using Ch = Chunk<G>;
   const uint32_t cpr = p.chunks_per_row;
+  const FastDiv dv = p.div_chunks;
   const uint32_t total = static_cast<uint32_t>(n) * cpr;
   for (uint32_t w0 = threadIdx.x; w0 < total; w0 += kRowThreads * kRowCopyUnroll) {
     typename Ch::T v[kRowCopyUnroll];
@@ -184,13 +229,12 @@ __device__ __forceinline__ void copy_misses(const RowCommon& p, const unsigned c
       const uint32_t w = w0 + u * kRowThreads;
       to[u] = nullptr;
       if (w < total) {
-        const uint32_t m = cpr == 1 ? w : fast_div(w, p.div_chunks);
-        const uint32_t c = w - m * cpr;
-        const int32_t d = dst[m];
+        const uint32_t m = cpr == 1 ? w : fast_div(w, dv);
+        const uint32_t off = (w - m * cpr) * G;
+        const int64_t d = dst[m];
         if (d >= 0) {
-          const int64_t off = static_cast<int64_t>(c) * G;
-          v[u] = Ch::ld(pool + src[m] * p.row_bytes + off);
-          to[u] = hot + static_cast<int64_t>(d) * p.row_bytes + off;
+          v[u] = Ch::ld(pool + src[m] + off);
+          to[u] = hot + d + off;
         }
       }
     }
@@ -200,7 +244,7 @@ __device__ __forceinline__ void copy_misses(const RowCommon& p, const unsigned c
   }
 }
 
-template <int NL, bool kTables, bool kPacked>
+template <int NL, bool kTables, int kMap>
 __global__ void __launch_bounds__(kRowThreads, 2)
     swap_in_rows_kernel(const __grid_constant__ RowParams<NL> P) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -318,7 +362,6 @@ __global__ void __launch_bounds__(kRowThreads, 2)
   uint32_t* filter = reinterpret_cast<uint32_t*>(smem + L.o_filter);
   int64_t* prs = reinterpret_cast<int64_t*>(smem + L.o_prs);
   int32_t* claim = reinterpret_cast<int32_t*>(smem + L.o_claim);
-  int32_t* evl = reinterpret_cast<int32_t*>(smem + L.o_evl);
   int8_t* code = reinterpret_cast<int8_t*>(smem + L.o_code);
   uint32_t* sbits = reinterpret_cast<uint32_t*>(smem + L.o_sbits);
   uint32_t* dup = reinterpret_cast<uint32_t*>(smem + L.o_dup);
@@ -326,15 +369,29 @@ __global__ void __launch_bounds__(kRowThreads, 2)
   int32_t* cntp = reinterpret_cast<int32_t*>(smem + L.o_cntp);
   int32_t* cnte = reinterpret_cast<int32_t*>(smem + L.o_cnte);
   int32_t* misc = reinterpret_cast<int32_t*>(smem + L.o_misc);
+  int32_t* wsum = reinterpret_cast<int32_t*>(smem + L.o_wsum);
+  const DirectMap dm{tab, reinterpret_cast<uint16_t*>(smem + L.o_dpre),
+                     reinterpret_cast<int32_t*>(smem + L.o_dent)};
+  const int nwq = static_cast<int>((Lb + 31) >> 5);  // direct map: bitmap words of this row
   const int nw = (H + 31) / 32;
   {  // whole 16-byte words: every region is padded to 16 bytes
-    int4* t4 = reinterpret_cast<int4*>(tab);
-    for (int i = tid; i < (1 << L.hash_bits) / 4; i += kRowThreads) t4[i] = make_int4(-1, -1, -1, -1);
     int4* c4 = reinterpret_cast<int4*>(claim);
     for (int i = tid; i < (K + 3) / 4; i += kRowThreads)
       c4[i] = make_int4(kUnclaimed, kUnclaimed, kUnclaimed, kUnclaimed);
-    int4* f4 = reinterpret_cast<int4*>(filter);
-    for (int i = tid; i < (1 << (kRowFilterBits - 7)); i += kRowThreads) f4[i] = make_int4(0, 0, 0, 0);
+    if constexpr (kMap == kMapDirect) {
+      int4* b4 = reinterpret_cast<int4*>(dm.bm);
+      for (int i = tid; i < (nwq + 3) / 4; i += kRowThreads) b4[i] = make_int4(0, 0, 0, 0);
+      int4* e4 = reinterpret_cast<int4*>(dm.ent);
+      for (int i = tid; i < (K + 3) / 4; i += kRowThreads)
+        e4[i] = make_int4(kUnclaimed, kUnclaimed, kUnclaimed, kUnclaimed);
+    } else {
+      int4* t4 = reinterpret_cast<int4*>(tab);
+      for (int i = tid; i < (1 << L.hash_bits) / 4; i += kRowThreads)
+        t4[i] = make_int4(-1, -1, -1, -1);
+      int4* f4 = reinterpret_cast<int4*>(filter);
+      for (int i = tid; i < (1 << (kRowFilterBits - 7)); i += kRowThreads)
+        f4[i] = make_int4(0, 0, 0, 0);
+    }
     for (int i = tid; i < nw; i += kRowThreads) {
       sbits[i] = 0u;
       dup[i] = 0u;
@@ -385,6 +442,7 @@ __global__ void __launch_bounds__(kRowThreads, 2)
     }
     __syncthreads();
     for (int i = tid; i < nw; i += kRowThreads) hit[i] = 0u;
+    my_flags |= HS_ST_BAD_LRU_SLOT;  // a repeated slot's later positions are corrupt entries
     __syncthreads();
   }
 
@@ -423,8 +481,42 @@ __global__ void __launch_bounds__(kRowThreads, 2)
     }
     cp_async_commit();
   }
+  constexpr bool kPacked = kMap == kMapPacked;
   const ReqHash<kPacked> hsh{tab, L.hash_bits, p.entry_bits};
-  {
+  if constexpr (kMap == kMapDirect) {
+    // Mark the requested ids (a bit already set is a repeated id), then the
+    // words' prefixes (each thread a run of words), then rank -> entry.
+    bool rep = false;
+    for (int i = tid; i < K; i += kRowThreads) {
+      const int32_t t = ids[i];
+      if (static_cast<uint32_t>(t) >= lim) continue;
+      const uint32_t bit = 1u << (t & 31);
+      rep |= (atomicOr(&dm.bm[t >> 5], bit) & bit) != 0u;
+    }
+    if (rep) misc[kRmRepeat] = 1;
+    __syncthreads();
+    const int per = (nwq + kRowThreads - 1) / kRowThreads;
+    const int w0 = tid * per, w1 = min(nwq, w0 + per);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) cnt += __popc(dm.bm[w]);
+    int total;
+    int run = block_exclusive_sum(cnt, wsum, &total);
+    for (int w = w0; w < w1; ++w) {
+      dm.pre[w] = static_cast<uint16_t>(run);
+      run += __popc(dm.bm[w]);
+    }
+    __syncthreads();
+    const bool any_rep = misc[kRmRepeat] != 0;
+    for (int i = tid; i < K; i += kRowThreads) {
+      const int32_t t = ids[i];
+      if (static_cast<uint32_t>(t) >= lim) continue;
+      const int d = dm.rank(t, dm.bm[t >> 5]);
+      if (any_rep)
+        atomicMin(&dm.ent[d], i);
+      else
+        dm.ent[d] = i;
+    }
+  } else {
     bool rep = false;
     for (int g0 = 0; g0 < K; g0 += 4 * kRowThreads) {
       int32_t tv[4];
@@ -493,13 +585,20 @@ __global__ void __launch_bounds__(kRowThreads, 2)
   }
   __syncthreads();
   const bool id_repeat = misc[kRmRepeat] != 0;
-  if (id_repeat) {  // rare: each repeated id's smallest entry becomes canonical
+  if (kMap != kMapDirect && id_repeat) {  // rare: each repeated id's smallest entry becomes canonical
     for (int i = tid; i < K; i += kRowThreads) {
       const int32_t t = ids[i];
       if (static_cast<uint32_t>(t) < lim) hsh.make_min(t, i);
     }
     __syncthreads();
   }
+  // The canonical entry of a valid id, -1 when it is not requested.
+  auto map_find = [&](int32_t t) -> int32_t {
+    if constexpr (kMap == kMapDirect)
+      return dm.find(t);
+    else
+      return hsh.find(t);
+  };
 
   // ---- P2: walk the LRU order; the lowest position holding a wanted token claims it.
   for (int x0 = 0; x0 < H; x0 += 4 * kRowThreads) {
@@ -513,11 +612,19 @@ __global__ void __launch_bounds__(kRowThreads, 2)
       tk[u] = ok[u] ? tokp[s] : -1;
       ok[u] = ok[u] && static_cast<uint32_t>(tk[u]) < lim && tk[u] != newest;
     }
+    int f[4];
+    if constexpr (kMap == kMapDirect) {  // exact: no filter, no probe chains
+      uint32_t bw[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) bw[u] = ok[u] ? dm.bm[tk[u] >> 5] : 0u;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        f[u] = ((bw[u] >> (tk[u] & 31)) & 1u) ? dm.ent[dm.rank(tk[u], bw[u])] : -1;
+    } else {
     uint32_t fw[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u)
       fw[u] = ok[u] ? filter[filter_bit(tk[u], kRowFilterBits) >> 5] : 0u;
-    int f[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       ok[u] = ok[u] && ((fw[u] >> (filter_bit(tk[u], kRowFilterBits) & 31)) & 1u);
@@ -541,6 +648,7 @@ __global__ void __launch_bounds__(kRowThreads, 2)
       for (int u = 0; u < 4; ++u)
         if (ok[u]) f[u] = hsh.find(tk[u]);
     }
+    }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       if (kTables && f[u] >= 0 && code[f[u]] != 0) f[u] = -1;  // resident or unmapped: not wanted
@@ -560,7 +668,7 @@ __global__ void __launch_bounds__(kRowThreads, 2)
     const int8_t pre = (kTables && valid) ? code[i] : 0;
     if (pre == kResident) continue;
     const bool cand = valid && t != newest && pre == 0 && c == kUnclaimed &&
-                      (!id_repeat || hsh.find(t) == i);
+                      (!id_repeat || map_find(t) == i);
     if (q.src_bt != nullptr) {
       if (!cand) prs[i] = -1;
     } else if (cand && t < p.pool_rows_cols) {
@@ -572,25 +680,27 @@ __global__ void __launch_bounds__(kRowThreads, 2)
   cp_async_commit();
   __syncthreads();
 
-  // ---- P3: hits before each bitmap word (one warp scan), then the
-  // evictables in LRU order; only the first K can be taken by a miss.
+  // ---- P3: hits before each bitmap word (one warp scan).
   for (int w = tid; w < nw; w += kRowThreads) cntp[w] = __popc(hit[w]);
   __syncthreads();
   if (warp == 0) {
     const int nh = warp_scan_array(cntp, nw, lane);
     if (lane == 0) misc[kRmHits] = nh;
   }
-  __syncthreads();
-  for (int x = tid; x < H; x += kRowThreads) {
-    const uint32_t hw = hit[x >> 5];
-    const uint32_t bit = 1u << (x & 31);
-    if (hw & bit) continue;
-    const int e = x - (cntp[x >> 5] + __popc(hw & (bit - 1u)));
-    const int s = lru[x];
-    const bool corrupt = !(s >= 0 && s < H) || (slot_repeat && bit_of(dup, x));
-    if (corrupt) my_flags |= HS_ST_BAD_LRU_SLOT;
-    if (e < K) evl[e] = (corrupt ? 0x10000 : 0) | (s & 0xFFFF);
-  }
+  // The m-th evictable in LRU order is the m-th position that is not a hit:
+  // the last word with at most m non-hits before it (binary search on the
+  // prefixes), then the right bit of that word.  Only the misses look theirs up.
+  auto evictable = [&](int m) -> int {
+    int lo = 0, hi = nw - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (32 * mid - cntp[mid] <= m) lo = mid;
+      else hi = mid - 1;
+    }
+    uint32_t free_bits = ~hit[lo];
+    if (lo == nw - 1 && (H & 31)) free_bits &= (1u << (H & 31)) - 1u;
+    return 32 * lo + static_cast<int>(__fns(free_bits, 0, m - (32 * lo - cntp[lo]) + 1));
+  };
 
   // ---- P4: entries in top-k order.
   cp_async_wait_all();
@@ -603,7 +713,7 @@ __global__ void __launch_bounds__(kRowThreads, 2)
       int8_t c;
       if (static_cast<uint32_t>(t) >= lim) {
         c = kInvalid;
-      } else if (id_repeat && hsh.find(t) != i) {
+      } else if (id_repeat && map_find(t) != i) {
         c = kRepeat;
         my_flags |= HS_ST_DUP_ID;
       } else if (kTables && code[i] == kResident) {
@@ -638,9 +748,10 @@ __global__ void __launch_bounds__(kRowThreads, 2)
   const int NH = misc[kRmHits];
   const int M = misc[kRmMisses];
   const int E = H - NH;
-  // The hash is dead: it now holds each miss's pool row; evl[m] becomes miss
-  // m's hot row (or -1).
+  // The hash is dead: it now holds each miss's source and destination byte
+  // offsets (the destination -1 when the miss got no hot row).
   int64_t* jsrc = reinterpret_cast<int64_t*>(smem + L.o_hash);
+  int64_t* jdst = jsrc + K;
   for (int base = 0; base < K; base += kRowThreads) {
     const int i = base + tid;
     const bool mine = i < K;
@@ -649,10 +760,10 @@ __global__ void __launch_bounds__(kRowThreads, 2)
     if (mine && mask_g) mask_g[i] = c == kMiss;
     if (c == kMiss) {
       const int mm = cnte[i >> 5] + __popc(m & lanes_before);  // the row's mm-th miss
-      const int32_t e = evl[mm];                               // takes the mm-th evictable
+      const int x = evictable(mm);                             // takes the mm-th evictable
+      const int s = lru[x];
       int32_t d = -1;
-      if (!(e >> 16)) {
-        const int s = static_cast<int16_t>(e & 0xFFFF);
+      if (s >= 0 && s < H && !(slot_repeat && bit_of(dup, x))) {  // not a corrupt entry
         const int32_t hr = rowp[s];
         if (hr >= 0 && hr < p.hot_num_rows) {
           d = hr;
@@ -663,8 +774,8 @@ __global__ void __launch_bounds__(kRowThreads, 2)
       }
       const int64_t pr = prs[i];
       out_g[i] = d;
-      jsrc[mm] = pr;
-      evl[mm] = d;
+      jsrc[mm] = pr * p.row_bytes;
+      jdst[mm] = d >= 0 ? static_cast<int64_t>(d) * p.row_bytes : -1;
       if (q.miss_src) {
         q.miss_src[b * p.plan_stride + mm] = pr;
         q.miss_dst[b * p.plan_stride + mm] = d;
@@ -716,24 +827,29 @@ __global__ void __launch_bounds__(kRowThreads, 2)
 
   // ---- P6: copy the misses' rows.
   if (p.copy_width == 16) {
-    copy_misses<16>(p, q.pool_k, q.hot_k, M, jsrc, evl);
-    if (q.pool_v != nullptr) copy_misses<16>(p, q.pool_v, q.hot_v, M, jsrc, evl);
+    copy_misses<16>(p, q.pool_k, q.hot_k, M, jsrc, jdst);
+    if (q.pool_v != nullptr) copy_misses<16>(p, q.pool_v, q.hot_v, M, jsrc, jdst);
   } else if (p.copy_width == 4) {
-    copy_misses<4>(p, q.pool_k, q.hot_k, M, jsrc, evl);
-    if (q.pool_v != nullptr) copy_misses<4>(p, q.pool_v, q.hot_v, M, jsrc, evl);
+    copy_misses<4>(p, q.pool_k, q.hot_k, M, jsrc, jdst);
+    if (q.pool_v != nullptr) copy_misses<4>(p, q.pool_v, q.hot_v, M, jsrc, jdst);
   } else {
-    copy_misses<1>(p, q.pool_k, q.hot_k, M, jsrc, evl);
-    if (q.pool_v != nullptr) copy_misses<1>(p, q.pool_v, q.hot_v, M, jsrc, evl);
+    copy_misses<1>(p, q.pool_k, q.hot_k, M, jsrc, jdst);
+    if (q.pool_v != nullptr) copy_misses<1>(p, q.pool_v, q.hot_v, M, jsrc, jdst);
   }
 }
 
 template <int NL>
 using RowKernelFn = void (*)(const RowParams<NL>);
 
+template <int NL, bool kTables>
+RowKernelFn<NL> pick_rows_map(int map) {
+  if (map == kMapDirect) return swap_in_rows_kernel<NL, kTables, kMapDirect>;
+  if (map == kMapPacked) return swap_in_rows_kernel<NL, kTables, kMapPacked>;
+  return swap_in_rows_kernel<NL, kTables, kMapWide>;
+}
 template <int NL>
-RowKernelFn<NL> pick_rows_kernel(bool tables, bool packed) {
-  if (tables) return packed ? swap_in_rows_kernel<NL, true, true> : swap_in_rows_kernel<NL, true, false>;
-  return packed ? swap_in_rows_kernel<NL, false, true> : swap_in_rows_kernel<NL, false, false>;
+RowKernelFn<NL> pick_rows_kernel(bool tables, int map) {
+  return tables ? pick_rows_map<NL, true>(map) : pick_rows_map<NL, false>(map);
 }
 
 // Layer geometry that must agree across the layers of one launch.
@@ -790,12 +906,12 @@ RowLayerPtrs layer_ptrs(const hs_swap_in_args& a) {
 
 template <int NL>
 hs_err launch_rows(const RowCommon& c, const hs_swap_in_args* layers, int n, bool tables,
-                   bool packed, int device, hs_stream_t stream, const char* who) {
+                   int device, hs_stream_t stream, const char* who) {
   RowParams<NL> prm;
   prm.c = c;
   for (int l = 0; l < n; ++l) prm.ly[l] = layer_ptrs(layers[l]);
   for (int l = n; l < NL; ++l) prm.ly[l] = prm.ly[0];
-  const RowKernelFn<NL> fn = pick_rows_kernel<NL>(tables, packed);
+  const RowKernelFn<NL> fn = pick_rows_kernel<NL>(tables, c.lay.map);
   hs_err err = ensure_smem(reinterpret_cast<const void*>(fn), device, c.lay.total);
   if (err != HS_OK) return err;
   cudaLaunchConfig_t cfg = {};
@@ -815,21 +931,34 @@ hs_err launch_rows(const RowCommon& c, const hs_swap_in_args* layers, int n, boo
 
 // Shared-memory plan: two CTAs per SM when it fits (slot tokens and rows
 // staged, a request hash of four then two slots per id), else one.
-hs_err pick_row_layout(int K, int H, bool tables, const DeviceInfo& dev, const char* who,
-                       RowLayout* out) {
+// The request map is direct when the caller bounds the sequence length
+// (max_len > 0) and it fits, else the packed hash when `packed`, else the wide.
+hs_err pick_row_layout(int K, int H, bool tables, bool packed, int64_t max_len,
+                       const DeviceInfo& dev, const char* who, RowLayout* out) {
   const int two = dev.max_smem_per_sm / 2 - 1024;
   const int budgets[2] = {two < dev.max_smem_optin ? two : dev.max_smem_optin,
                           dev.max_smem_optin};
   const bool stage[3][2] = {{true, true}, {true, false}, {false, false}};
+  const int hash_map = packed ? kMapPacked : kMapWide;
   for (int budget : budgets)
-    for (const auto& st : stage)
-      for (int mult = 4; mult >= 2; mult /= 2) {
-        const RowLayout L = make_row_layout(K, H, hash_bits_for(K, mult), st[0], st[1], tables);
+    for (const auto& st : stage) {
+      if (max_len > 0 && max_len <= (int64_t{1} << 24)) {
+        const RowLayout L =
+            make_row_layout(K, H, kMapDirect, 0, max_len, st[0], st[1], tables);
         if (L.total <= budget) {
           *out = L;
           return HS_OK;
         }
       }
+      for (int mult = 4; mult >= 2; mult /= 2) {
+        const RowLayout L =
+            make_row_layout(K, H, hash_map, hash_bits_for(K, mult), 0, st[0], st[1], tables);
+        if (L.total <= budget) {
+          *out = L;
+          return HS_OK;
+        }
+      }
+    }
   return fail(HS_ERR_UNSUPPORTED,
               "%s: top_k %d / hot_size %d need more shared memory per CTA than the device's %d B",
               who, K, H, dev.max_smem_optin);
@@ -838,7 +967,7 @@ hs_err pick_row_layout(int K, int H, bool tables, const DeviceInfo& dev, const c
 }  // namespace
 
 int64_t swap_in_rows_min_smem(int K, int H, bool tables) {
-  return make_row_layout(K, H, hash_bits_for(K, 2), false, false, tables).total;
+  return make_row_layout(K, H, kMapPacked, hash_bits_for(K, 2), 0, false, false, tables).total;
 }
 
 hs_err swap_in_rows_launch(const hs_swap_in_args* layers, int num_layers, hs_stream_t stream,
@@ -862,7 +991,8 @@ hs_err swap_in_rows_launch(const hs_swap_in_args* layers, int num_layers, hs_str
   hs_err err = current_device(&dev);
   if (err != HS_OK) return err;
   RowLayout lay;
-  err = pick_row_layout(a.top_k, a.hot_size, dv.tables, dev, who, &lay);
+  err = pick_row_layout(a.top_k, a.hot_size, dv.tables, dv.packed, a.max_seq_len, dev, who,
+                        &lay);
   if (err != HS_OK) return err;
   if (static_cast<int64_t>(a.batch) * kRowMaxLayers > INT32_MAX)
     return fail(HS_ERR_UNSUPPORTED, "%s: batch too large", who);
@@ -907,9 +1037,9 @@ hs_err swap_in_rows_launch(const hs_swap_in_args* layers, int num_layers, hs_str
     return fail(HS_ERR_UNSUPPORTED, "%s: top_k * row chunks must be < 2^32", who);
   for (int l0 = 0; l0 < num_layers; l0 += kRowMaxLayers) {
     const int n = num_layers - l0 < kRowMaxLayers ? num_layers - l0 : kRowMaxLayers;
-    err = n == 1 ? launch_rows<1>(c, layers + l0, n, dv.tables, dv.packed, dev.device, stream, who)
-                 : launch_rows<kRowMaxLayers>(c, layers + l0, n, dv.tables, dv.packed,
-                                              dev.device, stream, who);
+    err = n == 1 ? launch_rows<1>(c, layers + l0, n, dv.tables, dev.device, stream, who)
+                 : launch_rows<kRowMaxLayers>(c, layers + l0, n, dv.tables, dev.device, stream,
+                                              who);
     if (err != HS_OK) return err;
   }
   return HS_OK;
