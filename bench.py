@@ -221,6 +221,7 @@ class SwapInWorkload:
 
         self.hs = hs
         self.overlap = True
+        self.use_layers = False  # profiling: steps through hs_swap_in_layers (the one-CTA kernel)
         self.tables = {}  # optional block tables passed to every call
         self.cfg, self.dev, self.layers = cfg, dev, layers
         B, H, S, L = cfg.batch, cfg.hot_size, cfg.row_bytes, cfg.seq_len
@@ -292,6 +293,12 @@ class SwapInWorkload:
         g = torch.cuda.CUDAGraph()
         argv = [self.args(l, topk[l], None if out is None else out[l],
                           None if miss is None else miss[l]) for l in range(self.layers)]
+        if self.use_layers:
+            arr = self.hs.layer_args_array(argv)
+            with torch.cuda.graph(g, stream=stream):
+                self.hs.swap_in_layers(arr, stream)
+            g.keep = arr
+            return g
         with torch.cuda.graph(g, stream=stream):
             for a in argv:
                 self.hs.swap_in_args(a, stream)
@@ -751,11 +758,13 @@ def run_host_link_peak(dev, stream, pinned):
 
 
 def run_swapin_cfg(cfg, dev, stream, steps, hbm_peak, link_peak, flush=None, shared_pool=False,
-                   tables=None):
+                   tables=None, use_layers=False):
     """A single-layer swap-in workload timed as graphs of one launch per step;
-    ``tables(w)`` may return block tables passed to every call."""
+    ``tables(w)`` may return block tables passed to every call; ``use_layers``
+    (profiling) steps it through hs_swap_in_layers instead."""
     B, K, H, S = cfg.batch, cfg.top_k, cfg.hot_size, cfg.row_bytes
     w = SwapInWorkload(cfg, dev, 1, 0, pool_host=cfg.pool_in_host, shared_pool=shared_pool)
+    w.use_layers = use_layers
     if tables is not None:
         w.tables = tables(w)
     with torch.cuda.stream(stream):
@@ -905,7 +914,7 @@ def run_transfer(dev, stream, link_peak, hot_rows_target, host=True, hbm_peak=No
     si, di = src_idx.cpu().numpy(), dst_idx.cpu().numpy()
     for _ in range(32):
         l, i = int(rng.integers(NL)), int(rng.integers(n))
-        ok &= bool(torch.equal(dst[l][di[i]].cpu(), src[l][si[i]]))
+        ok &= bool(torch.equal(dst[l][di[i]].cpu(), src[l][si[i]].cpu()))
     where = "pinned" if host else "HBM"
     res = dict(workload=c["name"] + f" (src pools {src_rows} rows/layer {where}; dst 61 HBM "
                                     f"buffers of {dst_rows} rows; indices seeded distinct)",
@@ -1121,9 +1130,11 @@ def main():
                     help="profiling only: fewer layers than the workload's 61")
     ap.add_argument("--op", choices=["store_kv", "fp8_store_kv", "dsv32_layer_swap_in",
                                      "tables_swap_in", "indexer_swap_in", "stress_swap_in",
-                                     "layers_swap_in"],
+                                     "layers_swap_in", "transfer_hbm"],
                     default=None,
                     help="profiling only: run this one secondary line and print it")
+    ap.add_argument("--rows-kernel", action="store_true",
+                    help="profiling only: run --op's swap-in through hs_swap_in_layers")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -1174,6 +1185,9 @@ def main():
         flush_ = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         if args.op == "layers_swap_in":
             out_ = run_layers_op(dev, s_, hbm_peak, args.layers or 8)
+        elif args.op == "transfer_hbm":
+            out_ = run_transfer(dev, s_, None, synth.STRESS.batch * (synth.STRESS.hot_size + 1),
+                                host=False, hbm_peak=hbm_peak)
         elif args.op in ("store_kv", "fp8_store_kv"):
             fn_ = run_store_kv if args.op == "store_kv" else run_fp8_store
             out_ = fn_(dev, hbm_peak, flush_, s_)
@@ -1183,7 +1197,7 @@ def main():
             del probe_
             cfg_ = synth.INDEXER if args.op == "indexer_swap_in" else synth.STRESS
             out_ = run_swapin_cfg(cfg_, dev, s_, 20 if cfg_ is synth.INDEXER else 10, hbm_peak,
-                                  link_["peak_gbs"])
+                                  link_["peak_gbs"], use_layers=args.rows_kernel)
         else:
             out_ = run_swapin_cfg(synth.DSV32, dev, s_, 30, hbm_peak, None, flush=flush_,
                                   tables=dsv32_block_tables if args.op == "tables_swap_in"

@@ -282,6 +282,13 @@ hs_err hs_store_kv(const void* k_src, const void* v_src, int64_t src_k_stride,
                    int64_t dst_rows, const int64_t* loc, int64_t n_tokens, int64_t row_bytes,
                    int32_t* status, hs_stream_t stream);
 
+/* hs_transfer_kv's has_v word: bit 0 says the V pointers follow the K
+ * pointers; HS_XFER_DEVICE_SOURCES asserts that every source pointer is
+ * device memory, which lets the library move 16-byte-aligned rows with bulk
+ * (TMA) copies. */
+#define HS_XFER_HAS_V 1
+#define HS_XFER_DEVICE_SOURCES 2
+
 /*
  * hs_transfer_kv -- indexed row gather/scatter over layers: for every pair n
  * and every pointer pair p in [0, num_layers * (1 + has_v)),
@@ -299,9 +306,13 @@ hs_err hs_store_kv(const void* k_src, const void* v_src, int64_t src_k_stride,
  *  src_stride/dst_stride  row pitch in bytes (>= row_bytes); src_rows/dst_rows
  *                      bound the indices
  *  status              device int32 [1] or NULL: HS_ST_BAD_INDEX when a pair is
- *                      out of range (the pair is skipped for every layer)
+ *                      out of range (the pair is skipped for every layer);
+ *                      HS_ST_TIMEOUT if a bulk copy's bounded wait gave up
+ *  has_v               HS_XFER_HAS_V | HS_XFER_DEVICE_SOURCES (other bits:
+ *                      HS_ERR_ARG)
  * Precondition (not checked): dst_idx values are distinct; sources and
- * destinations do not overlap.
+ * destinations do not overlap; with HS_XFER_DEVICE_SOURCES every source is
+ * device memory.
  */
 hs_err hs_transfer_kv(const uint64_t* src_ptrs, const uint64_t* dst_ptrs, int32_t num_layers,
                       int32_t has_v, const int64_t* src_idx, const int64_t* dst_idx, int64_t n,

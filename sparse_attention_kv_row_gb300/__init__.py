@@ -384,14 +384,17 @@ def store_kv(k_src, v_src, k_dst, v_dst, loc, status=None, stream=None) -> None:
 
 
 def transfer_kv(src_ptrs, dst_ptrs, src_idx, dst_idx, *, num_layers, has_v, src_stride,
-                dst_stride, src_rows, dst_rows, row_bytes, status=None, stream=None) -> None:
-    """Raw hs_transfer_kv: device uint64 pointer arrays and int64 index arrays."""
+                dst_stride, src_rows, dst_rows, row_bytes, status=None, stream=None,
+                device_sources=False) -> None:
+    """Raw hs_transfer_kv: device uint64 pointer arrays and int64 index arrays;
+    ``device_sources`` asserts every source is device memory (bulk copies)."""
     _need(src_idx, torch.int64, "src_idx", 1)
     _need(dst_idx, torch.int64, "dst_idx", 1)
     if src_idx.numel() != dst_idx.numel():
         raise ValueError("src_idx and dst_idx differ in length")
     _capi.check(_lib().hs_transfer_kv(
-        _ptr(src_ptrs), _ptr(dst_ptrs), num_layers, int(bool(has_v)), _ptr(src_idx),
+        _ptr(src_ptrs), _ptr(dst_ptrs), num_layers,
+        int(bool(has_v)) | (_capi.XFER_DEVICE_SOURCES if device_sources else 0), _ptr(src_idx),
         _ptr(dst_idx), src_idx.numel(), src_stride, dst_stride, src_rows, dst_rows, row_bytes,
         _ptr(status), C.c_void_p(_stream(stream))), "hs_transfer_kv")
 
@@ -421,7 +424,7 @@ def transfer_kv_layers(src_layers, dst_layers, src_idx, dst_idx, *, has_v=False,
     transfer_kv(ptrs[0], ptrs[1], src_idx, dst_idx, num_layers=nl, has_v=has_v, src_stride=sp,
                 dst_stride=dp, src_rows=min(t.shape[0] for t in src_layers),
                 dst_rows=min(t.shape[0] for t in dst_layers), row_bytes=rb, status=status,
-                stream=stream)
+                stream=stream, device_sources=all(t.is_cuda for t in src_layers))
 
 
 def probe_read(src, sink, stream=None) -> None:

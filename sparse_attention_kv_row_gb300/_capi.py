@@ -24,6 +24,7 @@ SEQ_LENS_I64 = 1
 REQ_STATE_I64 = 2
 OVERLAP_PREV = 4
 DT_F32, DT_F16, DT_BF16 = 0, 1, 2
+XFER_HAS_V, XFER_DEVICE_SOURCES = 1, 2
 ABI_VERSION = 8
 
 # Every symbol include/hisparse.h declares.

@@ -14,16 +14,22 @@
 //             for each index pair, the same row of every layer's cache.
 //
 // Work is flattened into (row) units -- (token, K|V) for store_kv and
-// (pair, layer) for transfer, pair-major like the pages -- and spread one
-// warp per unit over a persistent grid sized to the SM count.  A warp moves
-// its row in 16-byte chunks when source, destination and size allow it, else
-// in 4-byte words, else bytes, with up to four chunks per lane in flight.
+// (pair, layer) for transfer, pair-major like the pages.  The register mover
+// spreads one warp per unit over a persistent grid sized to the SM count; a
+// warp moves its row in 16-byte chunks when source, destination and size
+// allow it, else in 4-byte words, else bytes, with up to four chunks per lane
+// in flight.  A transfer whose sources the caller declares device memory, with
+// 16-byte row pitches and sizes, uses the bulk (TMA) mover instead: one
+// thread per row in flight, global -> shared -> global (measured 61 % of HBM
+// against 55 % for the register mover on the 61-layer transfer; the register
+// mover stays for store_kv, where it was the faster of the two).
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 #include "hs_device.cuh"
 #include "hs_host.h"
+#include "hs_swap_in_common.cuh"
 
 namespace hs {
 namespace {
@@ -114,6 +120,60 @@ struct StoreKvParams {
   int32_t* status;
 };
 
+// ------------------------------------------------------------------ bulk (TMA) mover
+// For rows whose addresses and size are multiples of 16 bytes.  Thread t of a
+// CTA owns slot t (row_bytes of shared memory) and mbarrier t and moves units
+// u = blockIdx.x * blockDim.x + t, += gridDim.x * blockDim.x, one at a time:
+// one bulk load global -> slot completed on the mbarrier (a bounded wait),
+// then one bulk store slot -> global, which has read the slot before the
+// slot's next load.  A thread issues a few instructions per row, and an SM
+// holds ~190 KB of rows in flight.
+constexpr int kBulkSmemTarget = 96 * 1024;  // shared memory per CTA, about
+constexpr uint32_t kMoverPolls = 1u << 22;
+
+__host__ __device__ inline int bulk_slots_offset(int threads) { return (threads * 8 + 15) & ~15; }
+
+template <class Unit>
+__device__ __forceinline__ void bulk_move(const Unit& unit, uint64_t units, uint32_t bytes,
+                                          int32_t* status) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int t = threadIdx.x;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem) + t;
+  unsigned char* slot = smem + bulk_slots_offset(blockDim.x) + static_cast<uint32_t>(t) * bytes;
+  mbar_init(bar, 1);
+  fence_mbar_init();
+  uint32_t parity = 0;
+  bool stored = false;
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * blockDim.x + t; u < units; u += stride) {
+    const unsigned char* src;
+    unsigned char* dst;
+    if (!unit(u, &src, &dst)) continue;
+    const uintptr_t al = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst);
+    if ((al & 15) != 0) {  // a layer base off 16 bytes: this row by words or bytes
+      if ((al & 3) == 0) {
+        for (uint32_t o = 0; o < bytes; o += 4) st_stream_u32(dst + o, ld_stream_u32(src + o));
+      } else {
+        for (uint32_t o = 0; o < bytes; ++o) st_stream_u8(dst + o, ld_stream_u8(src + o));
+      }
+      continue;
+    }
+    if (stored) bulk_wait_read_all();
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load(slot, src, bytes, bar);
+    if (!mbar_wait(bar, parity, kMoverPolls)) {
+      if (status) atomicOr(status, HS_ST_TIMEOUT);
+      mbar_wait(bar, parity, kMoverPolls, 16000000000ull);  // wait out the load in flight
+      break;
+    }
+    parity ^= 1u;
+    bulk_store(dst, slot, bytes);
+    bulk_commit();
+    stored = true;
+  }
+  if (stored) bulk_wait_read_all();  // every slot is read before shared memory is released
+}
+
 __global__ void __launch_bounds__(kMoverThreads) store_kv_kernel(const StoreKvParams p) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (kMoverThreads / kWarp);
@@ -168,6 +228,30 @@ __global__ void __launch_bounds__(kMoverThreads) transfer_kernel(const TransferP
         reinterpret_cast<unsigned char*>(__ldg(p.dst_ptrs + layer)) + d * p.dst_stride;
     warp_copy_row(dst, src, p.row_bytes, lane);
   }
+}
+
+struct TransferUnit {
+  const TransferParams* p;
+  __device__ __forceinline__ bool operator()(uint64_t u32, const unsigned char** src,
+                                             unsigned char** dst) const {
+    const uint32_t u = static_cast<uint32_t>(u32);
+    const uint32_t pair = p->ptr_pairs == 1 ? u : fast_div(u, p->div_ptr_pairs);
+    const uint32_t layer = u - pair * p->ptr_pairs;
+    const int64_t n = p->pair_begin + pair;
+    const int64_t s = __ldg(p->src_idx + n);
+    const int64_t d = __ldg(p->dst_idx + n);
+    if (s < 0 || s >= p->src_rows || d < 0 || d >= p->dst_rows) {
+      if (layer == 0 && p->status) atomicOr(p->status, HS_ST_BAD_INDEX);
+      return false;
+    }
+    *src = reinterpret_cast<const unsigned char*>(__ldg(p->src_ptrs + layer)) + s * p->src_stride;
+    *dst = reinterpret_cast<unsigned char*>(__ldg(p->dst_ptrs + layer)) + d * p->dst_stride;
+    return true;
+  }
+};
+
+__global__ void transfer_bulk_kernel(const TransferParams p) {
+  bulk_move(TransferUnit{&p}, p.units, static_cast<uint32_t>(p.row_bytes), p.status);
 }
 
 struct GatherParams {
@@ -348,6 +432,35 @@ __global__ void __launch_bounds__(512) probe_read_kernel(const uint4* src, int64
   if ((threadIdx.x & 31) == 0 && acc != 0) atomicXor(sink, static_cast<unsigned long long>(acc));
 }
 
+// Threads (= slots) per CTA of a bulk mover for rows of `bytes`, and its
+// shared memory; 0 threads when rows that large do not suit it.
+int bulk_threads(int64_t bytes) {
+  if (bytes < 16 || bytes > 16384 || bytes % 16 != 0) return 0;
+  int t = static_cast<int>(kBulkSmemTarget / (bytes + 8));
+  t = t < 32 ? 32 : (t > 512 ? 512 : t);
+  return t & ~31;
+}
+
+template <class Params>
+hs_err launch_bulk(void (*kernel)(Params), const Params& p, int64_t units, int64_t bytes,
+                   const DeviceInfo& dev, hs_stream_t stream, const char* who) {
+  const int threads = bulk_threads(bytes);
+  const int smem = bulk_slots_offset(threads) + threads * static_cast<int>(bytes);
+  hs_err err = ensure_smem(reinterpret_cast<const void*>(kernel), dev.device, smem);
+  if (err != HS_OK) return err;
+  int per_sm = 0;
+  cudaError_t e =
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+  if (e != cudaSuccess) return fail(HS_ERR_CUDA, "%s: occupancy query: %s", who, cudaGetErrorString(e));
+  int64_t grid = static_cast<int64_t>(dev.sm_count) * (per_sm > 0 ? per_sm : 1);
+  const int64_t need = (units + threads - 1) / threads;
+  if (grid > need) grid = need;
+  kernel<<<static_cast<unsigned>(grid), threads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(HS_ERR_CUDA, "%s launch: %s", who, cudaGetErrorString(e));
+  return HS_OK;
+}
+
 int mover_grid(const DeviceInfo& dev, int64_t units) {
   const int64_t warps_per_block = kMoverThreads / kWarp;
   int64_t blocks = (units + warps_per_block - 1) / warps_per_block;
@@ -407,7 +520,10 @@ extern "C" hs_err hs_transfer_kv(const uint64_t* src_ptrs, const uint64_t* dst_p
   clear_error();
   if (n < 0 || num_layers < 0 || row_bytes < 1 || src_rows < 0 || dst_rows < 0)
     return fail(HS_ERR_ARG, "hs_transfer_kv: negative size or row_bytes < 1");
-  if (has_v != 0 && has_v != 1) return fail(HS_ERR_ARG, "hs_transfer_kv: has_v must be 0 or 1");
+  if (has_v & ~(HS_XFER_HAS_V | HS_XFER_DEVICE_SOURCES))
+    return fail(HS_ERR_ARG, "hs_transfer_kv: unknown flags 0x%x", has_v);
+  const bool device_src = (has_v & HS_XFER_DEVICE_SOURCES) != 0;
+  has_v &= HS_XFER_HAS_V;
   if (n == 0 || num_layers == 0) return HS_OK;
   if (src_ptrs == nullptr || dst_ptrs == nullptr || src_idx == nullptr || dst_idx == nullptr)
     return fail(HS_ERR_ARG, "hs_transfer_kv: pointer arrays and index arrays are required");
@@ -436,6 +552,14 @@ extern "C" hs_err hs_transfer_kv(const uint64_t* src_ptrs, const uint64_t* dst_p
     p.dst_rows = dst_rows;
     p.row_bytes = row_bytes;
     p.status = status;
+    // The layers' base pointers are on the device: the bulk mover copies a row
+    // whose address is off 16 bytes by words instead.
+    if (device_src && ((src_stride | dst_stride) & 15) == 0 && bulk_threads(row_bytes) > 0) {
+      err = launch_bulk(transfer_bulk_kernel, p, p.units, row_bytes, dev, stream,
+                        "hs_transfer_kv");
+      if (err != HS_OK) return err;
+      continue;
+    }
     transfer_kernel<<<mover_grid(dev, p.units), kMoverThreads, 0,
                       reinterpret_cast<cudaStream_t>(stream)>>>(p);
     const cudaError_t e = cudaGetLastError();

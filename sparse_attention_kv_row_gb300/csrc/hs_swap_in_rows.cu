@@ -48,7 +48,7 @@ namespace hs {
 namespace {
 
 constexpr int kRowThreads = 512;
-constexpr int kRowCopyUnroll = 4;
+constexpr int kRowCopyUnroll = 6;
 constexpr int kRowFilterBits = 15;  // request filter: 2^15 bits = 4 KB
 constexpr int kRowMaxLayers = 64;   // layers per launch (kernel-parameter space)
 

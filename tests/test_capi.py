@@ -120,7 +120,7 @@ def test_movers_reject(lib):
     assert lib.hs_store_kv(None, None, 16, 16, None, None, 16, 10, None, 5, 16, None, None) == 1
     assert lib.hs_store_kv(1, None, 8, 0, 1, None, 16, 10, 1, 5, 16, None, None) == 1  # stride
     assert lib.hs_store_kv(1, 1, 16, 16, 1, None, 16, 10, 1, 5, 16, None, None) == 1  # v pair
-    assert lib.hs_transfer_kv(1, 1, 3, 2, 1, 1, 5, 16, 16, 1, 1, 16, None, None) == 1  # has_v
+    assert lib.hs_transfer_kv(1, 1, 3, 4, 1, 1, 5, 16, 16, 1, 1, 16, None, None) == 1  # flags
     assert lib.hs_transfer_kv(1, 1, 3, 0, 1, 1, 5, 8, 16, 1, 1, 16, None, None) == 1  # stride
     assert lib.hs_probe_read(8, 32, 16, None) == 1  # misaligned source
     assert lib.hs_wait_selftest(-1, 8, None) == 1   # negative poll budget

@@ -97,6 +97,37 @@ def test_transfer_parity(dev, L, S, has_v, host):
     assert st.item() == r_st[0] == oracle.ST_BAD_INDEX
 
 
+@pytest.mark.parametrize("offset", [0, 4, 1])
+def test_transfer_bulk_path_with_layer_bases_off_16_bytes(dev, offset):
+    """Device sources with 16-byte row pitches take the bulk (TMA) path; a layer
+    whose base address is off 16 bytes (views 4 or 1 bytes into a buffer) is
+    copied row by row in words or bytes instead.  Same results as the oracle."""
+    rng = np.random.default_rng(40 + offset)
+    L, S, n, src_rows, dst_rows = 3, 656, 2000, 5000, 2500
+    src = [rng.integers(0, 256, (src_rows, S), dtype=np.uint8) for _ in range(L)]
+    dst = [rng.integers(0, 256, (dst_rows, S), dtype=np.uint8) for _ in range(L)]
+    src_idx = rng.integers(0, src_rows, n).astype(np.int64)
+    dst_idx = rng.choice(dst_rows, size=n, replace=False).astype(np.int64)
+    g_src = []
+    for l, x in enumerate(src):
+        off = offset if l == 1 else 0   # only the middle layer is off 16 bytes
+        buf = torch.zeros(src_rows * S + 16, dtype=torch.uint8, device=dev)
+        view = buf[off: off + src_rows * S].view(src_rows, S)
+        view.copy_(torch.from_numpy(x))
+        g_src.append(view)
+    g_dst = [torch.from_numpy(x.copy()).to(dev) for x in dst]
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    _hs().transfer_kv_layers(g_src, g_dst, torch.from_numpy(src_idx).to(dev),
+                             torch.from_numpy(dst_idx).to(dev), status=st)
+    r_st = np.zeros(1, np.int32)
+    oracle.transfer_kv(src_layers=src, dst_layers=dst, src_idx=src_idx, dst_idx=dst_idx,
+                       status=r_st)
+    torch.cuda.synchronize()
+    for l in range(L):
+        np.testing.assert_array_equal(g_dst[l].cpu().numpy(), dst[l], err_msg=f"layer {l}")
+    assert st.item() == r_st[0] == 0
+
+
 def test_empty_calls_launch_nothing(dev):
     hs = _hs()
     z = torch.zeros((0, 16), dtype=torch.uint8, device=dev)
