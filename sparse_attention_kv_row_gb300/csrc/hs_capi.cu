@@ -2,8 +2,11 @@
 // and the small informational entry points of the C ABI.
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "hs_host.h"
@@ -50,6 +53,23 @@ hs_err current_device(DeviceInfo* out) {
   }
   *out = g_dev[dev];
   return HS_OK;
+}
+
+namespace {
+bool nvtx_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("HS_NVTX");
+    return v != nullptr && v[0] != '\0' && !(v[0] == '0' && v[1] == '\0');
+  }();
+  return on;
+}
+}  // namespace
+
+CallRange::CallRange(const char* name) : on_(nvtx_enabled()) {
+  if (on_) nvtxRangePushA(name);
+}
+CallRange::~CallRange() {
+  if (on_) nvtxRangePop();
 }
 
 MemKind classify(const void* p) {

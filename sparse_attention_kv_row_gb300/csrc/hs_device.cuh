@@ -83,12 +83,6 @@ __device__ __forceinline__ void cp_async_commit_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-// Copy `nbytes` from global `src` to shared `dst`, where dst and src agree
-// modulo 16 (the shared array is placed at the source's alignment).  The
-// 16-byte-aligned body goes through LDGSTS (no register staging, many copies
-// in flight).  Each of the < 16 head bytes and < 16 tail bytes is loaded by one
-// thread into a register and stored by stage_finish() only after the caller's
-// LDGSTS wait, so no thread stalls on it in between.
 // ------------------------------------------------------------------ bulk copies
 // One-dimensional bulk copies global -> shared through the tensor memory
 // accelerator, completed on an mbarrier by transaction bytes.
@@ -196,30 +190,9 @@ struct StagePending {
   int32_t off;  // byte offset in dst, or -1
   uint32_t val;
 };
-__device__ __forceinline__ StagePending stage_bytes(void* dst, const void* src, int64_t nbytes,
-                                                    int tid, int nthreads) {
-  const uintptr_t s = reinterpret_cast<uintptr_t>(src);
-  int64_t head = static_cast<int64_t>((16u - (s & 15u)) & 15u);
-  if (head > nbytes) head = nbytes;
-  const int64_t body = ((nbytes - head) / 16) * 16;
-  const int64_t tail = nbytes - head - body;
-  const unsigned char* sc = static_cast<const unsigned char*>(src);
-  char* dc = static_cast<char*>(dst);
-  StagePending pend{-1, 0};
-  if (tid < head) {
-    pend.off = tid;
-    pend.val = sc[tid];
-  } else if (tid >= 32 && tid < 32 + tail) {
-    pend.off = static_cast<int32_t>(head + body + (tid - 32));
-    pend.val = sc[pend.off];
-  }
-  // Offsets fit 32 bits: staged rows are at most a few hundred KB.
-  const uint32_t end = static_cast<uint32_t>(head + body);
-  for (uint32_t o = static_cast<uint32_t>(head) + static_cast<uint32_t>(tid) * 16u; o < end;
-       o += static_cast<uint32_t>(nthreads) * 16u)
-    cp_async_16(dc + o, sc + o);
-  return pend;
-}
+// A byte of a staged row's unaligned head or tail, loaded by one thread into a
+// register and stored by stage_finish() after the row's wait, so that no
+// thread stalls on the load in between.
 __device__ __forceinline__ void stage_finish(void* dst, StagePending pend) {
   if (pend.off >= 0) static_cast<unsigned char*>(dst)[pend.off] = static_cast<unsigned char>(pend.val);
 }
@@ -227,7 +200,7 @@ __device__ __forceinline__ void stage_finish(void* dst, StagePending pend) {
 // Staging by one bulk copy: the 16-byte-aligned body of [src, src + nbytes)
 // goes to dst (dst must be congruent to src modulo 16) through the tensor
 // memory accelerator; the unaligned head and tail bytes are loaded by threads
-// into a StagePending exactly as stage_bytes does.
+// into a StagePending.
 struct StageSplit {
   uint32_t head, body;
 };
@@ -383,29 +356,6 @@ __device__ __forceinline__ int block_exclusive_sum(int v, int* wsum, int* total)
   }
   __syncthreads();
   const int r = wsum[warp] + x - v;
-  *total = wsum[32];
-  __syncthreads();  // wsum may be reused right away
-  return r;
-}
-
-// Exclusive prefix of `flag` over the threads of the block in thread order;
-// `wsum` is shared scratch of >= 33 ints.  Returns the prefix and, in *total,
-// the block total.  Every thread of the block must call it.
-__device__ __forceinline__ int block_exclusive_count(bool flag, int* wsum, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarps = (blockDim.x + 31) >> 5;
-  const unsigned m = __ballot_sync(kFullMask, flag);
-  if (lane == 0) wsum[warp] = __popc(m);
-  __syncthreads();
-  if (warp == 0) {
-    const int v = lane < nwarps ? wsum[lane] : 0;
-    int t;
-    const int ex = warp_exclusive_scan(v, lane, &t);
-    if (lane < nwarps) wsum[lane] = ex;
-    if (lane == 0) wsum[32] = t;
-  }
-  __syncthreads();
-  const int r = wsum[warp] + __popc(m & ((1u << lane) - 1u));
   *total = wsum[32];
   __syncthreads();  // wsum may be reused right away
   return r;

@@ -243,6 +243,7 @@ extern "C" hs_err hs_fp8_store_kv(const void* k, const void* v, int32_t in_dtype
                                   int64_t n_tokens, int32_t num_kv_heads, int32_t head_dim,
                                   const float* k_scale, const float* v_scale, int32_t* status,
                                   hs_stream_t stream) {
+  hs::CallRange range("hs_fp8_store_kv");
   using namespace hs;
   clear_error();
   if (in_dtype != HS_DT_F32 && in_dtype != HS_DT_F16 && in_dtype != HS_DT_BF16)

@@ -26,6 +26,20 @@ hs_err current_device(DeviceInfo* out);
 enum class MemKind { kDevice, kHost, kManaged, kUnregistered, kUnknown };
 MemKind classify(const void* p);
 
+// A named NVTX range around one C-ABI call when the environment variable
+// HS_NVTX is set to anything but "0" (read once per process); otherwise it
+// does nothing.  For timelines taken with a profiler.
+class CallRange {
+ public:
+  explicit CallRange(const char* name);
+  ~CallRange();
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+
+ private:
+  bool on_;
+};
+
 // Lemire-Kaser-Kurz divider constant for 1 <= d < 2^32 (d == 1 gives magic 0
 // and the device side short-circuits it).
 inline uint64_t fastdiv_magic(uint32_t d) { return d <= 1 ? 0ull : (~0ull) / d + 1ull; }

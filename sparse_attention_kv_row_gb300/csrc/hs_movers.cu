@@ -476,6 +476,7 @@ extern "C" hs_err hs_store_kv(const void* k_src, const void* v_src, int64_t src_
                               int64_t src_v_stride, void* k_dst, void* v_dst, int64_t dst_stride,
                               int64_t dst_rows, const int64_t* loc, int64_t n_tokens,
                               int64_t row_bytes, int32_t* status, hs_stream_t stream) {
+  hs::CallRange range("hs_store_kv");
   using namespace hs;
   clear_error();
   if (n_tokens < 0 || row_bytes < 1 || dst_rows < 0)
@@ -516,6 +517,7 @@ extern "C" hs_err hs_transfer_kv(const uint64_t* src_ptrs, const uint64_t* dst_p
                                  const int64_t* dst_idx, int64_t n, int64_t src_stride,
                                  int64_t dst_stride, int64_t src_rows, int64_t dst_rows,
                                  int64_t row_bytes, int32_t* status, hs_stream_t stream) {
+  hs::CallRange range("hs_transfer_kv");
   using namespace hs;
   clear_error();
   if (n < 0 || num_layers < 0 || row_bytes < 1 || src_rows < 0 || dst_rows < 0)
@@ -593,6 +595,7 @@ extern "C" hs_err hs_gather_misses(const uint64_t* pool_ptrs, const uint64_t* ho
                                    const int64_t* miss_src, const int32_t* miss_dst,
                                    int64_t plan_stride, const int32_t* miss_count, int32_t batch,
                                    int32_t top_k, int32_t* status, hs_stream_t stream) {
+  hs::CallRange range("hs_gather_misses");
   using namespace hs;
   clear_error();
   if (batch < 0 || top_k < 0 || num_layers < 0 || row_bytes < 1 || pool_num_rows < 0 ||
@@ -660,6 +663,7 @@ extern "C" hs_err hs_invalidate_tokens(int32_t* slot_tokens, int64_t slot_tokens
                                        int32_t hot_size, int64_t num_states,
                                        const int64_t* state_rows, const int32_t* tokens,
                                        int64_t n_tokens, int32_t* status, hs_stream_t stream) {
+  hs::CallRange range("hs_invalidate_tokens");
   using namespace hs;
   clear_error();
   if (n_tokens < 0 || hot_size < 0 || num_states < 0)

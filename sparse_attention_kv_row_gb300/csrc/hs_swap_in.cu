@@ -1108,6 +1108,7 @@ hs_err ensure_smem(const void* fn, int device, int bytes) {
 }  // namespace hs
 
 extern "C" hs_err hs_swap_in(const hs_swap_in_args* a, hs_stream_t stream) {
+  hs::CallRange range("hs_swap_in");
   hs::clear_error();
   return hs::swap_in_launch(a, stream, -1, 0);
 }

@@ -159,6 +159,30 @@ struct Chunk<1> {
   static __device__ __forceinline__ void st(unsigned char* p, T v) { st_l2_u8(p, v); }
 };
 
+// The request map: valid id -> its canonical (smallest) top-k entry.
+enum : int { kMapWide = 0, kMapPacked = 1, kMapDirect = 2 };
+
+// The direct request map, used when the caller bounds the sequence length:
+// one bit per token id of the row marks the requested ids; a word's prefix
+// (set bits in the words before it) plus the popc of its lower bits is the
+// id's dense rank among the requested ids; ent[rank] is the id's canonical
+// (smallest) top-k entry.  A lookup is three shared loads and no probe loop.
+struct DirectMap {
+  uint32_t* bm;
+  uint16_t* pre;
+  int32_t* ent;
+  // The rank of a requested id (its bit is set).
+  __device__ __forceinline__ int rank(int32_t t, uint32_t w) const {
+    return pre[t >> 5] + __popc(w & ((1u << (t & 31)) - 1u));
+  }
+  // Entry of a valid id, -1 when it is not requested.
+  __device__ __forceinline__ int32_t find(int32_t t) const {
+    const uint32_t w = bm[t >> 5];
+    if (!((w >> (t & 31)) & 1u)) return -1;
+    return ent[rank(t, w)];
+  }
+};
+
 // ------------------------------------------------------------------ host side
 // What the host derives once from a checked hs_swap_in_args.
 struct SwapInDerived {

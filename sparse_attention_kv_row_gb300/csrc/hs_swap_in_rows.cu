@@ -57,9 +57,6 @@ constexpr int kRowMaxLayers = 64;   // layers per launch (kernel-parameter space
 // misses' source and destination byte offsets for the copy (it is >= 16K
 // bytes), the token region the candidates' pool rows (without block tables)
 // and then the new LRU order.
-// The request map: valid id -> its canonical (smallest) top-k entry.
-enum : int { kMapWide = 0, kMapPacked = 1, kMapDirect = 2 };
-
 struct RowLayout {
   int hash_bits;
   int map;                    // kMapWide / kMapPacked / kMapDirect
@@ -188,27 +185,6 @@ __device__ __noinline__ void rows_timeout_exit(int32_t* status, int32_t* miss_co
   }
   __syncthreads();
 }
-
-// The direct request map, used when the caller bounds the sequence length:
-// one bit per token id of the row marks the requested ids; a word's prefix
-// (set bits in the words before it) plus the popc of its lower bits is the
-// id's dense rank among the requested ids; ent[rank] is the id's canonical
-// (smallest) top-k entry.  A lookup is three shared loads and no probe loop.
-struct DirectMap {
-  uint32_t* bm;
-  uint16_t* pre;
-  int32_t* ent;
-  // The rank of a requested id (its bit is set).
-  __device__ __forceinline__ int rank(int32_t t, uint32_t w) const {
-    return pre[t >> 5] + __popc(w & ((1u << (t & 31)) - 1u));
-  }
-  // Entry of a valid id, -1 when it is not requested.
-  __device__ __forceinline__ int32_t find(int32_t t) const {
-    const uint32_t w = bm[t >> 5];
-    if (!((w >> (t & 31)) & 1u)) return -1;
-    return ent[rank(t, w)];
-  }
-};
 
 // P6: copy misses [0, n): the row at byte offset src[m] of the pool goes to
 // byte offset dst[m] of the hot buffer (skipped when dst[m] < 0).  Work items
@@ -1049,6 +1025,7 @@ hs_err swap_in_rows_launch(const hs_swap_in_args* layers, int num_layers, hs_str
 
 extern "C" hs_err hs_swap_in_layers(const hs_swap_in_args* layers, int32_t num_layers,
                                     hs_stream_t stream) {
+  hs::CallRange range("hs_swap_in_layers");
   using namespace hs;
   clear_error();
   if (num_layers < 0) return fail(HS_ERR_ARG, "hs_swap_in_layers: num_layers must be >= 0");

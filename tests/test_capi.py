@@ -132,3 +132,20 @@ def test_smem_bytes(lib):
     assert lib.hs_swap_in_smem_bytes(4097, 4096) == 0
     assert lib.hs_swap_in_smem_bytes(1, 32768) == 0
     assert lib.hs_swap_in_smem_bytes(2048, 4096) < 227 * 1024
+
+
+def test_nvtx_ranges_switch_on_without_a_profiler():
+    """HS_NVTX=1 wraps each call in an NVTX range; with no profiler attached the
+    calls behave exactly as without it (here: argument errors, no GPU needed)."""
+    import subprocess
+    import sys
+
+    code = ("import ctypes, sys; sys.path.insert(0, '.'); "
+            "from sparse_attention_kv_row_gb300 import _capi; lib = _capi.load(); "
+            "assert lib.hs_swap_in(None, None) == 1; "
+            "assert lib.hs_store_kv(None, None, 16, 16, None, None, 16, 10, None, 5, 16, None, None) == 1; "
+            "assert lib.hs_swap_in_layers(None, 1, None) == 1; print('ok')")
+    env = dict(os.environ, HS_NVTX="1")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stderr

@@ -386,3 +386,40 @@ def test_forced_timeout_leaves_rows_alone(dev, which, rank, overlap):
         assert ms[b] == r_miss[b] and st[b] == r_status[b]
     # the context is usable and the state intact: a normal call matches the oracle
     step_both(g, ref, ids, "after the forced time-out", plan=True)
+
+
+@pytest.mark.parametrize("layers_api", [False, True])
+def test_packed_hash_when_the_bound_is_too_long_for_the_direct_map(dev, layers_api):
+    """A sequence bound above 2^24 rules out the layers kernel's direct request
+    map; with top_k 64 the packed hash still fits every id (the per-layer
+    kernel's hash too).  Results match the oracle all the same."""
+    import sparse_attention_kv_row_gb300 as hs
+    import synth
+
+    rng = np.random.default_rng(4242)
+    B, K, H, L = 3, 64, 300, 5000
+    ref = cases.random_case(rng, B=B, K=K, H=H, S=656, R=B + 1, seq_len=L)
+    g = GpuCase(ref.copy(), dev, seq_bound=30_000_000)
+    g.case = ref
+    ts = synth.TopkStream(21, 0, B, K, L, 0.6)
+    for step in range(4):
+        ids = ts.next() if step < 3 else cases.random_ids(rng, ref)
+        if not layers_api:
+            step_both(g, ref, ids, f"step {step}", plan=True)
+            continue
+        out = torch.full((B, K), 12345, dtype=torch.int32, device=dev)
+        miss = torch.zeros(B, dtype=torch.int32, device=dev)
+        status = torch.zeros(B, dtype=torch.int32, device=dev)
+        a = hs.make_swap_in_args(
+            topk_ids=torch.from_numpy(ids).to(dev), seq_lens=torch.from_numpy(ref.seq_lens).to(dev),
+            req_state=torch.from_numpy(ref.req_state).to(dev), slot_tokens=g.tokens,
+            slot_rows=g.rows, lru=g.lru, pool_rows=g.pool_rows, pool_k=g.pool_k, hot_k=g.hot_k,
+            out_rows=out, miss_count=miss, status=status, max_seq_len=30_000_000)
+        hs.swap_in_layers([a])
+        torch.cuda.synchronize()
+        ref.topk = ids
+        r_out, r_miss, r_status, _ = cases.run_oracle(ref)
+        np.testing.assert_array_equal(out.cpu().numpy(), r_out)
+        np.testing.assert_array_equal(miss.cpu().numpy(), r_miss)
+        np.testing.assert_array_equal(status.cpu().numpy(), r_status)
+        g.assert_matches(ref, f"layers step {step}")
