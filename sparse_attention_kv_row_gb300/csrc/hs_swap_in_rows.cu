@@ -15,14 +15,17 @@
 // to 32767 works; what a phase needs from an earlier one is in shared memory:
 //   P0 stage    the LRU row, and where they fit the slot tokens and slot rows,
 //               by TMA bulk copies on an mbarrier (thread 0 polls, bounded);
-//   P1 state    LRU entries outside [0, H) are corrupt; a slot listed twice
-//               keeps its lowest position (one warp walks the row in order,
-//               only when an atomicOr bitmap pass saw a repeat);
-//      request  valid ids into the request hash (Knuth multiplicative,
-//               linear probing, a thread's first CASes issued together) and a
-//               4 KB filter; a second pass only if an id repeats;
+//   P1 request  valid ids into the request map: direct (a bitmap over token
+//               ids, word prefixes, rank -> entry) when the caller bounds the
+//               sequence length, else the hash (Knuth multiplicative, linear
+//               probing, a thread's first CASes issued together) and a 4 KB
+//               filter; a second pass only if an id repeats;
 //   P2 walk     every position probes its slot's token; the lowest position
-//               holding a wanted token claims the entry (atomicMin);
+//               holding a wanted token claims the entry (atomicMin).  The same
+//               pass checks the LRU row: entries outside [0, H) are corrupt;
+//               a slot listed twice keeps its lowest position (only when the
+//               atomicOr bitmap saw a repeat does one warp mark the later
+//               positions, and the walk runs again without them);
 //      hits     claimed entries set their position's bit in a hit bitmap;
 //               candidates fetch their pool rows with LDGSTS;
 //   P3 ranks    popc of the bitmap words and one warp scan give each position
@@ -189,34 +192,47 @@ __device__ __noinline__ void rows_timeout_exit(int32_t* status, int32_t* miss_co
 // P6: copy misses [0, n): the row at byte offset src[m] of the pool goes to
 // byte offset dst[m] of the hot buffer (skipped when dst[m] < 0).  Work items
 // are (miss, chunk) over all threads, kRowCopyUnroll loads before the stores.
+// One round of copy items, w0 + u * kRowThreads for u < kRowCopyUnroll:
+// loads only (the caller stores them with copy_store_round).
+template <int G, int U = kRowCopyUnroll>
+__device__ __forceinline__ void copy_load_round(const RowCommon& p, const unsigned char* pool,
+                                                unsigned char* hot, uint32_t total, uint32_t w0,
+                                                const int64_t* src, const int64_t* dst,
+                                                typename Chunk<G>::T* v, unsigned char** to) {
+  const uint32_t cpr = p.chunks_per_row;
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const uint32_t w = w0 + u * kRowThreads;
+    to[u] = nullptr;
+    if (w < total) {
+      const uint32_t m = cpr == 1 ? w : fast_div(w, p.div_chunks);
+      const uint32_t off = (w - m * cpr) * G;
+      const int64_t d = dst[m];
+      if (d >= 0) {
+        v[u] = Chunk<G>::ld(pool + src[m] + off);
+        to[u] = hot + d + off;
+      }
+    }
+  }
+}
+template <int G, int U = kRowCopyUnroll>
+__device__ __forceinline__ void copy_store_round(const typename Chunk<G>::T* v,
+                                                 unsigned char* const* to) {
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+    if (to[u] != nullptr) Chunk<G>::st(to[u], v[u]);
+}
+// Items from `first` on (first is a multiple of kRowThreads).
 template <int G>
 __device__ __forceinline__ void copy_misses(const RowCommon& p, const unsigned char* pool,
                                             unsigned char* hot, int n, const int64_t* src,
-                                            const int64_t* dst) {
-  using Ch = Chunk<G>;
-  const uint32_t cpr = p.chunks_per_row;
-  const FastDiv dv = p.div_chunks;
-  const uint32_t total = static_cast<uint32_t>(n) * cpr;
-  for (uint32_t w0 = threadIdx.x; w0 < total; w0 += kRowThreads * kRowCopyUnroll) {
-    typename Ch::T v[kRowCopyUnroll];
+                                            const int64_t* dst, uint32_t first = 0) {
+  const uint32_t total = static_cast<uint32_t>(n) * p.chunks_per_row;
+  for (uint32_t w0 = first + threadIdx.x; w0 < total; w0 += kRowThreads * kRowCopyUnroll) {
+    typename Chunk<G>::T v[kRowCopyUnroll];
     unsigned char* to[kRowCopyUnroll];
-#pragma unroll
-    for (int u = 0; u < kRowCopyUnroll; ++u) {
-      const uint32_t w = w0 + u * kRowThreads;
-      to[u] = nullptr;
-      if (w < total) {
-        const uint32_t m = cpr == 1 ? w : fast_div(w, dv);
-        const uint32_t off = (w - m * cpr) * G;
-        const int64_t d = dst[m];
-        if (d >= 0) {
-          v[u] = Ch::ld(pool + src[m] + off);
-          to[u] = hot + d + off;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kRowCopyUnroll; ++u)
-      if (to[u] != nullptr) Ch::st(to[u], v[u]);
+    copy_load_round<G>(p, pool, hot, total, w0, src, dst, v, to);
+    copy_store_round<G>(v, to);
   }
 }
 
@@ -384,43 +400,7 @@ __global__ void __launch_bounds__(kRowThreads, 2)
     return;
   }
 
-  // ---- P1 (state): slots outside [0, H) are corrupt entries; a repeated
-  // slot is seen by the bitmap pass.
   int32_t my_flags = 0;
-  for (int x = tid; x < H; x += kRowThreads) {
-    const int s = lru[x];
-    if (s >= 0 && s < H) {
-      const uint32_t bit = 1u << (s & 31);
-      if (atomicOr(&sbits[s >> 5], bit) & bit) misc[kRmSlotRepeat] = 1;
-    } else {
-      my_flags |= HS_ST_BAD_LRU_SLOT;
-    }
-  }
-  __syncthreads();
-  const bool slot_repeat = misc[kRmSlotRepeat] != 0;
-  if (slot_repeat) {
-    // Rare: one warp walks the row in LRU order and marks every position whose
-    // slot appeared at a lower position (`hit` serves as the seen-set here).
-    if (warp == 0) {
-      for (int base = 0; base < H; base += 32) {
-        const int x = base + lane;
-        const int s = x < H ? lru[x] : -1;
-        const bool valid = x < H && s >= 0 && s < H;
-        const unsigned same = __match_any_sync(kFullMask, valid ? s : -1 - lane);
-        const bool first = valid && (__ffs(same) - 1) == lane;
-        const bool seen = valid && bit_of(hit, s);
-        __syncwarp();
-        if (first && !seen) atomicOr(&hit[s >> 5], 1u << (s & 31));
-        const unsigned dm = __ballot_sync(kFullMask, valid && (!first || seen));
-        if (lane == 0) dup[base >> 5] = dm;
-        __syncwarp();
-      }
-    }
-    __syncthreads();
-    for (int i = tid; i < nw; i += kRowThreads) hit[i] = 0u;
-    my_flags |= HS_ST_BAD_LRU_SLOT;  // a repeated slot's later positions are corrupt entries
-    __syncthreads();
-  }
 
   // ---- P1 (request): the top-k row, written by the preceding kernel.
   grid_dep_wait();
@@ -576,7 +556,13 @@ __global__ void __launch_bounds__(kRowThreads, 2)
       return hsh.find(t);
   };
 
-  // ---- P2: walk the LRU order; the lowest position holding a wanted token claims it.
+  // ---- P2: walk the LRU order; the lowest position holding a wanted token
+  // claims it.  The first walk also checks the LRU row: a slot outside [0, H)
+  // is a corrupt entry, and a slot already seen (atomicOr bitmap) means a slot
+  // repeats -- rare: then one warp marks every position whose slot appeared at
+  // a lower position, the claims are cleared and the walk runs again without
+  // those positions.
+  auto walk = [&](bool first_walk, bool skip_dups) {
   for (int x0 = 0; x0 < H; x0 += 4 * kRowThreads) {
     int32_t tk[4];
     bool ok[4];
@@ -584,7 +570,16 @@ __global__ void __launch_bounds__(kRowThreads, 2)
     for (int u = 0; u < 4; ++u) {
       const int x = x0 + u * kRowThreads + tid;
       const int s = x < H ? lru[x] : -1;
-      ok[u] = x < H && s >= 0 && s < H && !(slot_repeat && bit_of(dup, x));
+      const bool in_range = x < H && s >= 0 && s < H;
+      if (first_walk && x < H) {
+        if (in_range) {
+          const uint32_t bit = 1u << (s & 31);
+          if (atomicOr(&sbits[s >> 5], bit) & bit) misc[kRmSlotRepeat] = 1;
+        } else {
+          my_flags |= HS_ST_BAD_LRU_SLOT;
+        }
+      }
+      ok[u] = in_range && !(skip_dups && bit_of(dup, x));
       tk[u] = ok[u] ? tokp[s] : -1;
       ok[u] = ok[u] && static_cast<uint32_t>(tk[u]) < lim && tk[u] != newest;
     }
@@ -631,7 +626,33 @@ __global__ void __launch_bounds__(kRowThreads, 2)
       if (f[u] >= 0) atomicMin(&claim[f[u]], x0 + u * kRowThreads + tid);
     }
   }
+  };
+  walk(true, false);
   __syncthreads();
+  const bool slot_repeat = misc[kRmSlotRepeat] != 0;
+  if (slot_repeat) {  // rare: `hit` serves as the seen-set of the in-order pass
+    if (warp == 0) {
+      for (int base = 0; base < H; base += 32) {
+        const int x = base + lane;
+        const int s = x < H ? lru[x] : -1;
+        const bool valid = x < H && s >= 0 && s < H;
+        const unsigned same = __match_any_sync(kFullMask, valid ? s : -1 - lane);
+        const bool first = valid && (__ffs(same) - 1) == lane;
+        const bool seen = valid && bit_of(hit, s);
+        __syncwarp();
+        if (first && !seen) atomicOr(&hit[s >> 5], 1u << (s & 31));
+        const unsigned dmask = __ballot_sync(kFullMask, valid && (!first || seen));
+        if (lane == 0) dup[base >> 5] = dmask;
+        __syncwarp();
+      }
+    }
+    for (int i = tid; i < K; i += kRowThreads) claim[i] = kUnclaimed;
+    __syncthreads();
+    for (int i = tid; i < nw; i += kRowThreads) hit[i] = 0u;
+    my_flags |= HS_ST_BAD_LRU_SLOT;  // a repeated slot's later positions are corrupt entries
+    walk(false, true);
+    __syncthreads();
+  }
   // Claimed entries mark their position as a hit; the pool rows of the miss
   // candidates (valid, not newest, unclaimed, canonical) are fetched with
   // LDGSTS so the loads overlap P3.
