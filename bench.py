@@ -197,7 +197,11 @@ def kernel_source_hash(sources):
     return h.hexdigest()[:16]
 
 
+ROWS_SOURCES = ["sparse_attention_kv_row_gb300/csrc/hs_swap_in_rows.cu",
+                "sparse_attention_kv_row_gb300/csrc/hs_swap_in_common.cuh",
+                "sparse_attention_kv_row_gb300/csrc/hs_device.cuh"]
 SWAP_IN_SOURCES = ["sparse_attention_kv_row_gb300/csrc/hs_swap_in.cu",
+                   "sparse_attention_kv_row_gb300/csrc/hs_swap_in_common.cuh",
                    "sparse_attention_kv_row_gb300/csrc/hs_device.cuh"]
 
 
@@ -536,12 +540,19 @@ def run_layers_variant(w, args, stream):
     alg = swapin_alg_bytes(B, K, H, S, NL * n, misses)
     hbm_peak, peak_src = peaks()
     gbs = alg / t / 1e9
+    # DRAM bytes per launch from the 8-layer capture, scaled to the launch's
+    # 61 layers (traffic grows with the (row, layer) problems); None once the
+    # kernel changed since the capture.
+    tr8 = profile_traffic("layers_swap_in_dsv32.md", ROWS_SOURCES)
     return dict(us_per_decode_step=t / n * 1e6, value=misses / t, unit="rows/s", steps=n,
                 topk_entries_per_s=NL * n * B * K / t, alg_bytes_per_step=alg / n,
                 roofline=dict(bound="hbm", achieved=gbs, peak=hbm_peak, unit="GB/s",
                               frac=gbs / hbm_peak, peak_source=peak_src,
                               kernel="swap_in_rows_kernel (hs_swap_in_layers)",
-                              launches_per_step=(NL + 63) // 64),
+                              launches_per_step=(NL + 63) // 64,
+                              traffic=(tr8 * NL / 8 if tr8 is not None else None),
+                              traffic_note="ncu DRAM read+write bytes of an 8-layer launch "
+                                           "(profiles/layers_swap_in_dsv32.md) x 61/8"),
                 how="variant: the whole 61-layer step as one hs_swap_in_layers launch (one "
                     "CTA per row and layer, 1952 CTAs), when every layer's top-k rows are "
                     "known up front; one CUDA graph per step; not the per-layer headline")
@@ -871,13 +882,14 @@ def dsv32_block_tables(w, bs=64, recent=4096):
                 res_block_size=bs, res_null_block=-1)
 
 
-def run_transfer(dev, stream, link_peak, hot_rows_target, host=True, hbm_peak=None):
+def run_transfer(dev, stream, link_peak, hot_rows_target, host=True, hbm_peak=None, layers=0):
     """The all-layer transfer: 61 layers x 78,592 pairs of 656 B rows, from
-    per-layer pools in pinned host memory (host link) or in HBM (HBM to HBM)."""
+    per-layer pools in pinned host memory (host link) or in HBM (HBM to HBM);
+    `layers` (profiling only) takes fewer layers."""
     import sparse_attention_kv_row_gb300 as hs
 
     c = synth.TRANSFER
-    NL, S = c["layers"], c["row_bytes"]
+    NL, S = layers or c["layers"], c["row_bytes"]
     st = synth.STRESS
     src_rows = st.seq_len  # one request's worth of rows per layer (pinned budget)
     n = 78592
@@ -916,7 +928,9 @@ def run_transfer(dev, stream, link_peak, hot_rows_target, host=True, hbm_peak=No
         l, i = int(rng.integers(NL)), int(rng.integers(n))
         ok &= bool(torch.equal(dst[l][di[i]].cpu(), src[l][si[i]].cpu()))
     where = "pinned" if host else "HBM"
-    res = dict(workload=c["name"] + f" (src pools {src_rows} rows/layer {where}; dst 61 HBM "
+    name = (f"all-layer transfer_kv: {NL} layers x {n:,} pairs of {S} B rows, "
+            f"{'pinned host' if host else 'HBM'} -> HBM")
+    res = dict(workload=name + f" (src pools {src_rows} rows/layer {where}; dst {NL} HBM "
                                     f"buffers of {dst_rows} rows; indices seeded distinct)",
                ms_per_call=t * 1e3, rows_per_s=n * NL / t, alg_bytes=alg, gbs=alg / t / 1e9,
                sampled_check_ok=ok)
@@ -1187,7 +1201,7 @@ def main():
             out_ = run_layers_op(dev, s_, hbm_peak, args.layers or 8)
         elif args.op == "transfer_hbm":
             out_ = run_transfer(dev, s_, None, synth.STRESS.batch * (synth.STRESS.hot_size + 1),
-                                host=False, hbm_peak=hbm_peak)
+                                host=False, hbm_peak=hbm_peak, layers=args.layers)
         elif args.op in ("store_kv", "fp8_store_kv"):
             fn_ = run_store_kv if args.op == "store_kv" else run_fp8_store
             out_ = fn_(dev, hbm_peak, flush_, s_)

@@ -145,31 +145,47 @@ __device__ __forceinline__ void bulk_move(const Unit& unit, uint64_t units, uint
   uint32_t parity = 0;
   bool stored = false;
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
-  for (uint64_t u = static_cast<uint64_t>(blockIdx.x) * blockDim.x + t; u < units; u += stride) {
-    const unsigned char* src;
-    unsigned char* dst;
-    if (!unit(u, &src, &dst)) continue;
-    const uintptr_t al = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst);
-    if ((al & 15) != 0) {  // a layer base off 16 bytes: this row by words or bytes
-      if ((al & 3) == 0) {
-        for (uint32_t o = 0; o < bytes; o += 4) st_stream_u32(dst + o, ld_stream_u32(src + o));
+  uint64_t u = static_cast<uint64_t>(blockIdx.x) * blockDim.x + t;
+  const unsigned char* src = nullptr;
+  unsigned char* dst = nullptr;
+  bool ok = u < units && unit(u, &src, &dst);
+  while (u < units) {
+    bool loading = false;
+    if (ok) {
+      const uintptr_t al = reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst);
+      if ((al & 15) != 0) {  // a layer base off 16 bytes: this row by words or bytes
+        if ((al & 3) == 0) {
+          for (uint32_t o = 0; o < bytes; o += 4) st_stream_u32(dst + o, ld_stream_u32(src + o));
+        } else {
+          for (uint32_t o = 0; o < bytes; ++o) st_stream_u8(dst + o, ld_stream_u8(src + o));
+        }
       } else {
-        for (uint32_t o = 0; o < bytes; ++o) st_stream_u8(dst + o, ld_stream_u8(src + o));
+        if (stored) bulk_wait_read_all();
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_load(slot, src, bytes, bar);
+        loading = true;
       }
-      continue;
     }
-    if (stored) bulk_wait_read_all();
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_load(slot, src, bytes, bar);
-    if (!mbar_wait(bar, parity, kMoverPolls)) {
-      if (status) atomicOr(status, HS_ST_TIMEOUT);
-      mbar_wait(bar, parity, kMoverPolls, 16000000000ull);  // wait out the load in flight
-      break;
+    // The next row's indices and addresses load while this row is in flight.
+    const uint64_t nu = u + stride;
+    const unsigned char* nsrc = nullptr;
+    unsigned char* ndst = nullptr;
+    const bool nok = nu < units && unit(nu, &nsrc, &ndst);
+    if (loading) {
+      if (!mbar_wait(bar, parity, kMoverPolls)) {
+        if (status) atomicOr(status, HS_ST_TIMEOUT);
+        mbar_wait(bar, parity, kMoverPolls, 16000000000ull);  // wait out the load in flight
+        break;
+      }
+      parity ^= 1u;
+      bulk_store(dst, slot, bytes);
+      bulk_commit();
+      stored = true;
     }
-    parity ^= 1u;
-    bulk_store(dst, slot, bytes);
-    bulk_commit();
-    stored = true;
+    u = nu;
+    src = nsrc;
+    dst = ndst;
+    ok = nok;
   }
   if (stored) bulk_wait_read_all();  // every slot is read before shared memory is released
 }
