@@ -395,10 +395,6 @@ __global__ void __launch_bounds__(kRowThreads, 2)
   stage_finish(lru, pend_lru);
   stage_finish(tok_s, pend_tok);
   stage_finish(rows_s, pend_rows);
-  if (!block_wait(bar + 1, 0, p.fail_wait == 0 ? 0u : kMaxPolls)) {
-    rows_timeout_exit(q.status, q.miss_count, b, bar, ids_issued);
-    return;
-  }
 
   int32_t my_flags = 0;
 
@@ -555,6 +551,13 @@ __global__ void __launch_bounds__(kRowThreads, 2)
     else
       return hsh.find(t);
   };
+
+  // The request map needed only the top-k row: the state's copies had until
+  // now to arrive.
+  if (!block_wait(bar + 1, 0, p.fail_wait == 0 ? 0u : kMaxPolls)) {
+    rows_timeout_exit(q.status, q.miss_count, b, bar, ids_issued);
+    return;
+  }
 
   // ---- P2: walk the LRU order; the lowest position holding a wanted token
   // claims it.  The first walk also checks the LRU row: a slot outside [0, H)
