@@ -914,10 +914,8 @@ def run_transfer(dev, stream, link_peak, hot_rows_target, host=True, hbm_peak=No
     ptrs = (hs.layer_pointer_array(src, dev), hs.layer_pointer_array(dst, dev))
     torch.cuda.synchronize()
     fn = lambda: hs.transfer_kv_layers(src, dst, src_idx, dst_idx, stream=stream, ptrs=ptrs)  # noqa
-    with torch.cuda.stream(stream):
-        fn()
-    torch.cuda.synchronize()
-    t = time_launches(fn, 3, stream, torch.empty(16, device=dev))
+    # one call per graph replay, so the time is the GPU's alone (no host enqueue)
+    t = time_replayed(lambda _: fn(), 1, stream, reps=3)
     link_bytes = n * NL * S
     alg = 2 * n * NL * S + 16 * n
     # sampled check of the property dst_l[dst_idx[i]] == src_l[src_idx[i]]

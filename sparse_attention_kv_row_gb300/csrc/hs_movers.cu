@@ -26,6 +26,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "hs_device.cuh"
 #include "hs_host.h"
@@ -464,11 +465,30 @@ hs_err launch_bulk(void (*kernel)(Params), const Params& p, int64_t units, int64
   const int smem = bulk_slots_offset(threads) + threads * static_cast<int>(bytes);
   hs_err err = ensure_smem(reinterpret_cast<const void*>(kernel), dev.device, smem);
   if (err != HS_OK) return err;
+  // CTAs per SM for this (kernel, row size), queried once per device.
+  static std::mutex mu;
+  static struct { const void* fn; int device, bytes, per_sm; } seen[32];
+  static int n_seen = 0;
   int per_sm = 0;
-  cudaError_t e =
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
-  if (e != cudaSuccess) return fail(HS_ERR_CUDA, "%s: occupancy query: %s", who, cudaGetErrorString(e));
-  int64_t grid = static_cast<int64_t>(dev.sm_count) * (per_sm > 0 ? per_sm : 1);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_seen; ++i)
+      if (seen[i].fn == reinterpret_cast<const void*>(kernel) && seen[i].device == dev.device &&
+          seen[i].bytes == bytes)
+        per_sm = seen[i].per_sm;
+  }
+  cudaError_t e = cudaSuccess;
+  if (per_sm == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+    if (e != cudaSuccess)
+      return fail(HS_ERR_CUDA, "%s: occupancy query: %s", who, cudaGetErrorString(e));
+    if (per_sm < 1) per_sm = 1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (n_seen < 32)
+      seen[n_seen++] = {reinterpret_cast<const void*>(kernel), dev.device,
+                        static_cast<int>(bytes), per_sm};
+  }
+  int64_t grid = static_cast<int64_t>(dev.sm_count) * per_sm;
   const int64_t need = (units + threads - 1) / threads;
   if (grid > need) grid = need;
   kernel<<<static_cast<unsigned>(grid), threads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(p);
