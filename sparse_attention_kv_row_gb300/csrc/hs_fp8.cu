@@ -117,7 +117,7 @@ __device__ __forceinline__ void convert_store(uint4 raw, float sc, bool scaled, 
 // chunks of the [heads x dim] row.  p.chunks = chunks per row, p.units =
 // tokens x (1 + has_v).
 template <int kDtype>
-__global__ void __launch_bounds__(kFp8Threads) fp8_row_kernel(const Fp8Params p) {
+__global__ void __launch_bounds__(kFp8Threads, 6) fp8_row_kernel(const Fp8Params p) {
   constexpr int E = chunk_elems<kDtype>();
   constexpr int U = 4;  // chunks per lane in flight
   const int lane = threadIdx.x & 31;
@@ -130,28 +130,37 @@ __global__ void __launch_bounds__(kFp8Threads) fp8_row_kernel(const Fp8Params p)
     const bool is_v = kvn == 2 && (u & 1u);
     const int64_t t = p.t_begin + (kvn == 2 ? (u >> 1) : u);
     const int64_t L = __ldg(p.loc + t);
+    const unsigned char* src = (is_v ? p.in[1] : p.in[0]) +
+                               t * (is_v ? p.stride_token[1] : p.stride_token[0]);
+    // The row's first round of chunks loads together with its slot index (the
+    // source row of token t is always in range): one round trip, not two.
+    uint4 raw[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t c = lane + j * kWarp;
+      if (c < p.chunks) raw[j] = ld_stream_v4(src + static_cast<int64_t>(c) * 16);
+    }
     if (L < 0 || L >= p.num_slots) {
       if (!is_v && lane == 0 && p.status) atomicOr(p.status, HS_ST_BAD_INDEX);
       continue;
     }
     const int64_t page = div_any(static_cast<uint32_t>(L), p.div_page);
     const int64_t off = L - page * p.page_size;
-    const unsigned char* src = (is_v ? p.in[1] : p.in[0]) +
-                               t * (is_v ? p.stride_token[1] : p.stride_token[0]);
     unsigned char* dst = (is_v ? p.cache[1] : p.cache[0]) + page * p.c_page + off * p.c_off;
     const float sc = is_v ? inv_v : inv_k;
     const bool scaled = (is_v ? p.scale[1] : p.scale[0]) != nullptr;
-    for (uint32_t c0 = lane; c0 < p.chunks; c0 += kWarp * U) {
-      uint4 raw[U];
-#pragma unroll
-      for (int j = 0; j < U; ++j) {
-        const uint32_t c = c0 + j * kWarp;
-        if (c < p.chunks) raw[j] = ld_stream_v4(src + static_cast<int64_t>(c) * 16);
-      }
+    for (uint32_t c0 = lane;;) {
 #pragma unroll
       for (int j = 0; j < U; ++j) {
         const uint32_t c = c0 + j * kWarp;
         if (c < p.chunks) convert_store<kDtype>(raw[j], sc, scaled, dst + static_cast<int64_t>(c) * E);
+      }
+      c0 += kWarp * U;
+      if (c0 >= p.chunks) break;
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const uint32_t c = c0 + j * kWarp;
+        if (c < p.chunks) raw[j] = ld_stream_v4(src + static_cast<int64_t>(c) * 16);
       }
     }
   }

@@ -212,6 +212,41 @@ __global__ void __launch_bounds__(kMoverThreads) store_kv_kernel(const StoreKvPa
   }
 }
 
+// Rows of 16-byte chunks, at most 512 * U bytes, every base and stride a
+// multiple of 16 (the common KV layout).  One warp per unit; a lane's U chunks
+// are loaded together with the unit's destination index -- the source row of
+// token t is always in range, so its loads do not wait for the index check --
+// which makes a unit one memory round trip instead of two.  At 32 registers 64
+// warps fit on an SM, so a decode step's K+V scatter is in flight at once.
+template <int U>
+__global__ void __launch_bounds__(kMoverThreads, 8) store_kv_vec_kernel(const StoreKvParams p) {
+  const int lane = threadIdx.x & 31;
+  const bool has_v = p.v_src != nullptr;
+  // Loop bounds re-read from the parameters and gridDim, not held in registers.
+  for (uint32_t u = blockIdx.x * (kMoverThreads / kWarp) + (threadIdx.x >> 5);
+       u < (static_cast<uint32_t>(p.n_tokens) << (has_v ? 1 : 0));  // < 2^31
+       u += gridDim.x * (kMoverThreads / kWarp)) {
+    const int left = static_cast<int>(p.row_bytes >> 4) - lane;  // lane's chunks: 32 * k < left
+    const uint32_t t = has_v ? (u >> 1) : u;
+    const bool is_v = has_v && (u & 1);
+    const int64_t d = __ldg(p.loc + t);
+    const unsigned char* src =
+        (is_v ? p.v_src + t * p.src_v_stride : p.k_src + t * p.src_k_stride) + (lane << 4);
+    uint4 v[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k)
+      if (32 * k < left) v[k] = ld_stream_v4(src + 512 * k);
+    if (d < 0 || d >= p.dst_rows) {
+      if (lane == 0 && !is_v && p.status) atomicOr(p.status, HS_ST_BAD_INDEX);
+      continue;
+    }
+    unsigned char* dst = (is_v ? p.v_dst : p.k_dst) + d * p.dst_stride + (lane << 4);
+#pragma unroll
+    for (int k = 0; k < U; ++k)
+      if (32 * k < left) st_stream_v4(dst + 512 * k, v[k]);
+  }
+}
+
 struct TransferParams {
   const uint64_t* src_ptrs;
   const uint64_t* dst_ptrs;
@@ -541,8 +576,22 @@ extern "C" hs_err hs_store_kv(const void* k_src, const void* v_src, int64_t src_
                   row_bytes,
                   status};
   const int64_t units = n_tokens * (v_src != nullptr ? 2 : 1);
-  store_kv_kernel<<<mover_grid(dev, units), kMoverThreads, 0,
-                    reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  const uintptr_t al = reinterpret_cast<uintptr_t>(k_src) | reinterpret_cast<uintptr_t>(v_src) |
+                       reinterpret_cast<uintptr_t>(k_dst) | reinterpret_cast<uintptr_t>(v_dst) |
+                       static_cast<uintptr_t>(src_k_stride) |
+                       static_cast<uintptr_t>(v_src != nullptr ? src_v_stride : 0) |
+                       static_cast<uintptr_t>(dst_stride) | static_cast<uintptr_t>(row_bytes);
+  const int grid = mover_grid(dev, units);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool vec = (al & 15) == 0 && units < (int64_t{1} << 31);
+  if (vec && row_bytes <= 512)
+    store_kv_vec_kernel<1><<<grid, kMoverThreads, 0, st>>>(p);
+  else if (vec && row_bytes <= 1024)
+    store_kv_vec_kernel<2><<<grid, kMoverThreads, 0, st>>>(p);
+  else if (vec && row_bytes <= 2048)
+    store_kv_vec_kernel<4><<<grid, kMoverThreads, 0, st>>>(p);
+  else
+    store_kv_kernel<<<grid, kMoverThreads, 0, st>>>(p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(HS_ERR_CUDA, "hs_store_kv launch: %s", cudaGetErrorString(e));
   return HS_OK;
