@@ -325,7 +325,7 @@ struct GatherParams {
 
 constexpr int kGatherUnits = 256;  // (miss, pointer pair) units a block stages per round
 constexpr int kGatherBlocksPerSm = 4;  // resident blocks of the replay (<= 64 registers)
-constexpr int kGatherUnroll = 4;       // 16-byte chunks in flight per thread
+constexpr int kGatherUnroll = 6;       // 16-byte chunks in flight per thread
 
 // Block (row, y) replays misses [y*mb, (y+1)*mb) of its row, mb = ceil(n /
 // gridDim.y): units u = (miss - first miss) * ptr_pairs + pointer pair, in
@@ -386,26 +386,31 @@ __global__ void __launch_bounds__(kMoverThreads, kGatherBlocksPerSm)
     const bool any_misaligned = __syncthreads_or(misaligned) != 0;
     if (p.chunks16 != 0 && !any_misaligned) {
       const uint32_t items = static_cast<uint32_t>(nu) * p.chunks16;
+      // An item in flight holds its data and its unit; the destination is
+      // recomputed for the store, which keeps registers for more items.
       for (uint32_t w0 = tid; w0 < items; w0 += kMoverThreads * kGatherUnroll) {
         uint4 v[kGatherUnroll];
-        unsigned char* to[kGatherUnroll];
+        uint32_t unit[kGatherUnroll];
 #pragma unroll
         for (int j = 0; j < kGatherUnroll; ++j) {
           const uint32_t w = w0 + j * kMoverThreads;
-          to[j] = nullptr;
+          unit[j] = kGatherUnits;  // none
           if (w < items) {
             const uint32_t k = fast_div(w, p.div_chunks16);
-            const uint32_t off = (w - k * p.chunks16) << 4;
             const unsigned char* from = s_src[k];
             if (from != nullptr) {
-              v[j] = ld_stream_v4(from + off);
-              to[j] = s_dst[k] + off;
+              v[j] = ld_stream_v4(from + ((w - k * p.chunks16) << 4));
+              unit[j] = k;
             }
           }
         }
 #pragma unroll
-        for (int j = 0; j < kGatherUnroll; ++j)
-          if (to[j] != nullptr) st_l2_v4(to[j], v[j]);
+        for (int j = 0; j < kGatherUnroll; ++j) {
+          const uint32_t k = unit[j];
+          if (k == kGatherUnits) continue;
+          const uint32_t w = w0 + j * kMoverThreads;
+          st_l2_v4(s_dst[k] + ((w - k * p.chunks16) << 4), v[j]);
+        }
       }
     } else {
       for (int k = tid >> 5; k < nu; k += W)
