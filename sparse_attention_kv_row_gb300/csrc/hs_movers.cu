@@ -256,6 +256,8 @@ struct TransferParams {
   uint32_t units;          // pairs_in_launch * ptr_pairs  (< 2^32)
   uint32_t ptr_pairs;      // num_layers * (1 + has_v)
   FastDiv div_ptr_pairs;
+  uint32_t pairs;          // pairs in this launch (bulk path: units are layer-major)
+  FastDiv div_pairs;
   int64_t src_stride, dst_stride, src_rows, dst_rows, row_bytes;
   int32_t* status;
 };
@@ -282,13 +284,17 @@ __global__ void __launch_bounds__(kMoverThreads) transfer_kernel(const TransferP
   }
 }
 
+// Units of the bulk path are layer-major (u = pointer pair * pairs + pair):
+// the rows in flight at any moment lie in one or two layers' buffers, not in
+// every layer's, which spares the address translation caches.  Rows are
+// independent, so the order is free.
 struct TransferUnit {
   const TransferParams* p;
   __device__ __forceinline__ bool operator()(uint64_t u32, const unsigned char** src,
                                              unsigned char** dst) const {
     const uint32_t u = static_cast<uint32_t>(u32);
-    const uint32_t pair = p->ptr_pairs == 1 ? u : fast_div(u, p->div_ptr_pairs);
-    const uint32_t layer = u - pair * p->ptr_pairs;
+    const uint32_t layer = p->ptr_pairs == 1 ? 0u : div_any(u, p->div_pairs);
+    const uint32_t pair = u - layer * p->pairs;
     const int64_t n = p->pair_begin + pair;
     const int64_t s = __ldg(p->src_idx + n);
     const int64_t d = __ldg(p->dst_idx + n);
@@ -638,6 +644,8 @@ extern "C" hs_err hs_transfer_kv(const uint64_t* src_ptrs, const uint64_t* dst_p
     p.units = static_cast<uint32_t>(pairs * ptr_pairs);
     p.ptr_pairs = ptr_pairs;
     p.div_ptr_pairs = FastDiv{fastdiv_magic(ptr_pairs), ptr_pairs};
+    p.pairs = static_cast<uint32_t>(pairs);
+    p.div_pairs = FastDiv{fastdiv_magic(p.pairs), p.pairs};
     p.src_stride = src_stride;
     p.dst_stride = dst_stride;
     p.src_rows = src_rows;

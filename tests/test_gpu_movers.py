@@ -145,3 +145,30 @@ def test_probe_read(dev):
     torch.cuda.synchronize()
     x = np.bitwise_xor.reduce(np.arange(1 << 20, dtype=np.uint32))
     assert (sink.item() & 0xFFFFFFFF) == int(x)
+
+
+@pytest.mark.parametrize("n", [1, 2, 7])
+def test_transfer_bulk_path_few_pairs_many_layers(dev, n):
+    """The bulk path runs its units layer-major (u = pointer pair * n + pair);
+    with one pair the divisor is 1.  K and V of five layers, device sources."""
+    rng = np.random.default_rng(70 + n)
+    L, S, src_rows, dst_rows = 5, 656, 50, 40
+    P = 2 * L
+    src = [rng.integers(0, 256, (src_rows, S), dtype=np.uint8) for _ in range(P)]
+    dst = [rng.integers(0, 256, (dst_rows, S), dtype=np.uint8) for _ in range(P)]
+    src_idx = rng.integers(0, src_rows, n).astype(np.int64)
+    dst_idx = rng.choice(dst_rows, size=n, replace=False).astype(np.int64)
+    if n > 2:
+        dst_idx[n - 1] = dst_rows  # a bad pair
+    g_src = [torch.from_numpy(x).to(dev) for x in src]
+    g_dst = [torch.from_numpy(x.copy()).to(dev) for x in dst]
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    _hs().transfer_kv_layers(g_src, g_dst, torch.from_numpy(src_idx).to(dev),
+                             torch.from_numpy(dst_idx).to(dev), has_v=True, status=st)
+    r_st = np.zeros(1, np.int32)
+    oracle.transfer_kv(src_layers=src, dst_layers=dst, src_idx=src_idx, dst_idx=dst_idx,
+                       status=r_st)
+    torch.cuda.synchronize()
+    for l in range(P):
+        np.testing.assert_array_equal(g_dst[l].cpu().numpy(), dst[l], err_msg=f"layer {l}")
+    assert st.item() == r_st[0]
