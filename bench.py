@@ -823,6 +823,27 @@ def run_swapin_cfg(cfg, dev, stream, steps, hbm_peak, link_peak, flush=None, sha
     return res
 
 
+def run_shared_index_op(dev, stream, args):
+    """The shared-index leg on its own (for profiling): `--layers` DeepSeek-V3.2
+    layers (default 4: one resolving launch and one replay launch per step)
+    sharing one 2.75 GB HBM pool."""
+    import dataclasses
+
+    NL = args.layers or 4
+    cfg = dataclasses.replace(synth.DSV32, layers=NL,
+                              name=synth.DSV32.name + f" [{NL} layers, one shared pool]")
+    w = SwapInWorkload(cfg, dev, NL, 0, n_pools=1)
+    with torch.cuda.stream(stream):
+        for _ in range(cfg.warm_steps):
+            w.eager_step(w.next_topk(), stream)
+    torch.cuda.synchronize()
+    out = run_shared_index(w, args, stream)
+    out["workload"] = cfg.name
+    w.free()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_layers_op(dev, stream, hbm_peak, layers, steps=20):
     """The layers variant on its own (for profiling): `layers` DeepSeek-V3.2
     layers, each with its own state and hot buffer, sharing one 2.75 GB HBM
@@ -1142,7 +1163,7 @@ def main():
                     help="profiling only: fewer layers than the workload's 61")
     ap.add_argument("--op", choices=["store_kv", "fp8_store_kv", "dsv32_layer_swap_in",
                                      "tables_swap_in", "indexer_swap_in", "stress_swap_in",
-                                     "layers_swap_in", "transfer_hbm"],
+                                     "layers_swap_in", "transfer_hbm", "shared_index"],
                     default=None,
                     help="profiling only: run this one secondary line and print it")
     ap.add_argument("--rows-kernel", action="store_true",
@@ -1197,6 +1218,8 @@ def main():
         flush_ = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         if args.op == "layers_swap_in":
             out_ = run_layers_op(dev, s_, hbm_peak, args.layers or 8)
+        elif args.op == "shared_index":
+            out_ = run_shared_index_op(dev, s_, args)
         elif args.op == "transfer_hbm":
             out_ = run_transfer(dev, s_, None, synth.STRESS.batch * (synth.STRESS.hot_size + 1),
                                 host=False, hbm_peak=hbm_peak, layers=args.layers)
