@@ -844,17 +844,19 @@ def run_shared_index_op(dev, stream, args):
     return out
 
 
-def run_layers_op(dev, stream, hbm_peak, layers, steps=20):
-    """The layers variant on its own (for profiling): `layers` DeepSeek-V3.2
-    layers, each with its own state and hot buffer, sharing one 2.75 GB HBM
-    pool, resolved by one hs_swap_in_layers launch per step (graphs, back to
-    back, after the warm-up to the steady state)."""
+def run_layers_op(dev, stream, hbm_peak, layers, steps=20, base=None, link_peak=None):
+    """The layers variant on its own: `layers` layers of `base` (default the
+    DeepSeek-V3.2 shape), each with its own state and hot buffer, sharing one
+    pool (HBM, or pinned host memory for a host-pool shape), resolved by one
+    hs_swap_in_layers launch per step (graphs, back to back, after the warm-up
+    to the steady state)."""
     import dataclasses
 
-    cfg = dataclasses.replace(synth.DSV32, layers=layers,
-                              name=synth.DSV32.name + f" [{layers} layers, one shared pool]")
+    base = base or synth.DSV32
+    cfg = dataclasses.replace(base, layers=layers,
+                              name=base.name + f" [{layers} layers, one shared pool]")
     B, K, H, S = cfg.batch, cfg.top_k, cfg.hot_size, cfg.row_bytes
-    w = SwapInWorkload(cfg, dev, layers, 0, n_pools=1)
+    w = SwapInWorkload(cfg, dev, layers, 0, n_pools=1, pool_host=cfg.pool_in_host)
     w.overlap = False
     hs = w.hs
 
@@ -880,10 +882,16 @@ def run_layers_op(dev, stream, hbm_peak, layers, steps=20):
     del graphs, caps
     w.free()
     torch.cuda.empty_cache()
-    return dict(workload=cfg.name, us_per_launch=t / steps * 1e6, rows_per_s=misses / t,
-                alg_bytes_per_launch=alg / steps,
-                roofline=dict(bound="hbm", achieved=alg / t / 1e9, peak=hbm_peak,
-                              frac=alg / t / 1e9 / hbm_peak, unit="GB/s"))
+    res = dict(workload=cfg.name, us_per_launch=t / steps * 1e6, rows_per_s=misses / t,
+               alg_bytes_per_launch=alg / steps, miss_rows_per_launch=misses / steps)
+    if cfg.pool_in_host:
+        res["roofline"] = dict(bound="host_link", achieved=misses * S / t / 1e9, peak=link_peak,
+                               frac=misses * S / t / 1e9 / link_peak, unit="GB/s",
+                               note="bytes over the host link = miss rows")
+    else:
+        res["roofline"] = dict(bound="hbm", achieved=alg / t / 1e9, peak=hbm_peak,
+                               frac=alg / t / 1e9 / hbm_peak, unit="GB/s")
+    return res
 
 
 def dsv32_block_tables(w, bs=64, recent=4096):
@@ -1163,7 +1171,8 @@ def main():
                     help="profiling only: fewer layers than the workload's 61")
     ap.add_argument("--op", choices=["store_kv", "fp8_store_kv", "dsv32_layer_swap_in",
                                      "tables_swap_in", "indexer_swap_in", "stress_swap_in",
-                                     "layers_swap_in", "transfer_hbm", "shared_index"],
+                                     "layers_swap_in", "transfer_hbm", "shared_index",
+                                     "indexer_layers"],
                     default=None,
                     help="profiling only: run this one secondary line and print it")
     ap.add_argument("--rows-kernel", action="store_true",
@@ -1226,6 +1235,12 @@ def main():
         elif args.op in ("store_kv", "fp8_store_kv"):
             fn_ = run_store_kv if args.op == "store_kv" else run_fp8_store
             out_ = fn_(dev, hbm_peak, flush_, s_)
+        elif args.op == "indexer_layers":
+            probe_ = torch.empty(2 * GiB, dtype=torch.uint8, pin_memory=True)
+            link_ = run_host_link_peak(dev, s_, probe_)
+            del probe_
+            out_ = run_layers_op(dev, s_, hbm_peak, args.layers or synth.DSV32.layers, steps=10,
+                                 base=synth.INDEXER, link_peak=link_["peak_gbs"])
         elif args.op in ("indexer_swap_in", "stress_swap_in"):
             probe_ = torch.empty(2 * GiB, dtype=torch.uint8, pin_memory=True)
             link_ = run_host_link_peak(dev, s_, probe_)
@@ -1267,6 +1282,12 @@ def main():
                                                 link["peak_gbs"])
         ops["stress_swap_in"] = run_swapin_cfg(synth.STRESS, dev, s, 10, hbm_peak,
                                                link["peak_gbs"])
+        il = run_layers_op(dev, s, hbm_peak, synth.DSV32.layers, steps=10, base=synth.INDEXER,
+                           link_peak=link["peak_gbs"])
+        il["how"] = ("variant: every layer's indexer-row swap-in of a decode step in one "
+                     "hs_swap_in_layers launch (one CTA per row and layer), one pinned pool "
+                     "shared by the layers; one CUDA graph per step")
+        ops["indexer_layers_variant"] = il
         one = run_swapin_cfg(synth.DSV32, dev, s, 30, hbm_peak, None, flush=flush)
         one["workload"] += " [one layer; L2 flushed before each launch]"
         ops["dsv32_layer_swap_in"] = one
