@@ -1079,7 +1079,13 @@ def cpu_oracle_decode_steps(steps: int, warm: int):
     for _ in range(NL):
         tokens, rows, lru = synth.cold_state(B, H)
         states.append((tokens, rows, lru, np.zeros((B * (H + 1), S), np.uint8)))
-    ts = synth.TopkStream(cfg.seed, 0, NL * B, K, L, cfg.reuse)
+    if torch.cuda.is_available():  # the headline's own stream, drawn on the GPU (untimed)
+        tsd = synth.TopkStreamTorch(rank_seed(cfg.seed, 0), NL * B, K, L, cfg.reuse, "cuda")
+
+        def next_ids():
+            return tsd.next().cpu().numpy()
+    else:
+        next_ids = synth.TopkStream(cfg.seed, 0, NL * B, K, L, cfg.reuse).next
 
     def step(ids):
         for l, (tokens, rows, lru, hot) in enumerate(states):
@@ -1088,11 +1094,11 @@ def cpu_oracle_decode_steps(steps: int, warm: int):
                            pool_k=pool, hot_k=hot, out_rows=out, hot_size=H, stats=stats)
 
     for _ in range(cfg.warm_steps + warm):
-        step(ts.next())
+        step(next_ids())
     stats[:] = 0
     spent = 0.0
     for _ in range(steps):
-        ids = ts.next()
+        ids = next_ids()
         t0 = time.perf_counter()
         step(ids)
         spent += time.perf_counter() - t0
@@ -1162,7 +1168,7 @@ def rank_seed(base: int, rank: int) -> int:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--headline-only", action="store_true")
