@@ -176,7 +176,7 @@ __device__ __forceinline__ uint32_t bloom_bit(int32_t key) { return filter_bit(k
 // returns with the copy outstanding; HS_ST_TIMEOUT then says the context is
 // suspect.
 __device__ __noinline__ void timeout_tail(const SwapInParams& p, int b, int j, int C,
-                                          uint64_t* bar, bool ids_issued) {
+                                          uint64_t* bar) {
   cluster_wait();
   if (C > 1) cluster_arrive_relaxed();
   if (threadIdx.x == 0) {
@@ -188,7 +188,7 @@ __device__ __noinline__ void timeout_tail(const SwapInParams& p, int b, int j, i
     }
     if (j == 0 && p.miss_count) p.miss_count[b] = 0;
     mbar_wait(bar + 1, 0, kDrainPolls, kDrainNs);
-    if (ids_issued) mbar_wait(bar, 0, kDrainPolls, kDrainNs);
+    mbar_wait(bar, 0, kDrainPolls, kDrainNs);
   }
   __syncthreads();
   if (C > 1) cluster_wait();
@@ -257,7 +257,6 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   // only on the full path, so the padding and short-sequence exits leave
   // nothing in flight.
   grid_dep_launch_dependents();
-  const bool overlap = (p.flags & HS_OVERLAP_PREV) != 0;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.o_bar);
   if (tid == 0) {
     mbar_init(bar, 1);
@@ -348,10 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     stage_body(tok, tokens_g, sp_tok, bar + 1);
     stage_body(rows, rows_g, sp_rows, bar + 1);
   }
-  // Without early start the top-k row is final already: its copy goes out
-  // with the state's.
-  bool ids_issued = !overlap;
-  if (!overlap) stage_ids();
+  // The grid-dependency wait comes right after the state's copies are
+  // issued, and the top-k row's copy right after it (without early start the
+  // wait returns at once).  The CTAs that set a launch's length are the last
+  // to get an SM, after the preceding kernel has ended: for them the wait is
+  // free, and the row's fetch overlaps the fills and the state half below.
+  // A CTA that started early does those after the wait, with time to spare.
+  grid_dep_wait();
+  stage_ids();
   const StagePending pend_lru = stage_edges(lru_g, 2LL * H, sp_lru, tid);
   const StagePending pend_tok = stage_edges(tokens_g, 4LL * H, sp_tok, tid);
   const StagePending pend_rows = stage_edges(rows_g, 4LL * (H + 1), sp_rows, tid);
@@ -398,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       fence_acq_rel_cluster();
     }
     cluster_arrive_relaxed();
-    timeout_tail(p, b, j, C, bar, ids_issued);
+    timeout_tail(p, b, j, C, bar);
     return;
   }
   // ---- P1 (state half): check the LRU row is a permutation of the slots.
@@ -457,11 +460,6 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   }
 
   // ---- P1 (request half): the top-k row, written by the preceding kernel.
-  grid_dep_wait();
-  if (overlap) {
-    stage_ids();
-    ids_issued = true;
-  }
   stage_finish(ids, pend_ids);
   const uint32_t polls_ids = (p.fail_rank == j && p.fail_wait == 1) ? 0u : kMaxPolls;
   const bool ids_ok = block_wait(bar, 0, polls_ids);
@@ -475,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   }
   cluster_arrive_relaxed();
   if (!ids_ok) {
-    timeout_tail(p, b, j, C, bar, ids_issued);
+    timeout_tail(p, b, j, C, bar);
     return;
   }
   // Block tables: each valid id's entries are loaded with LDGSTS into prs
