@@ -651,7 +651,9 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   }
   cp_async_commit();
 
-  // ---- P3: hit ranks in LRU order; evictables compacted in LRU order.
+  // ---- P3/P4 counts: hits per chunk of LRU positions, then (once this
+  // thread's own pool-row loads have landed) each entry's class and the
+  // misses per chunk of entries.  One barrier, then one warp scans each.
   const int chunks_p = (H + 31) / 32;
   bool hit[IT];
   unsigned hm[IT];
@@ -666,29 +668,9 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
       if (lane == 0 && k * kThreads + warp * 32 < H) cntp[k * 32 + warp] = __popc(hm[k]);
     }
   }
-  __syncthreads();
-  if (warp == 0) {
-    const int nh = warp_scan_array(cntp, chunks_p, lane);
-    if (lane == 0) misc[kMiscHits] = nh;
-  }
-  __syncthreads();
-  int hb[IT];  // hits before each of my positions
-#pragma unroll
-  for (int k = 0; k < IT; ++k) {
-    const int q = k * kThreads + tid;
-    hb[k] = 0;
-    if (q >= H) continue;
-    hb[k] = cntp[k * 32 + warp] + __popc(hm[k] & lanes_before);
-    if (!hit[k]) {
-      const bool corrupt = f[k] == -2;
-      if (corrupt) my_flags |= HS_ST_BAD_LRU_SLOT;
-      evl[q - hb[k]] = (corrupt ? 0x10000 : 0) | (sl[k] & 0xFFFF);
-    }
-  }
-
-  // ---- P4: entries in top-k order.
+  // ---- P4: entries in top-k order (a thread reads back only the pool rows
+  // its own loads fetched).
   cp_async_wait_all();
-  __syncthreads();
   const int chunks_e = (K + 31) / 32;
   for (int base = 0; base < K; base += kThreads) {
     const int i = base + tid;
@@ -727,10 +709,29 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   }
   __syncthreads();
   if (warp == 0) {
+    const int nh = warp_scan_array(cntp, chunks_p, lane);
+    if (lane == 0) misc[kMiscHits] = nh;
+  } else if (warp == 1) {
     const int nm = warp_scan_array(cnte, chunks_e, lane);
     if (lane == 0) misc[kMiscMisses] = nm;
   }
   __syncthreads();
+  // ---- P3: hit ranks in LRU order; evictables compacted in LRU order.
+  int hb[IT];  // hits before each of my positions
+#pragma unroll
+  for (int k = 0; k < IT; ++k) {
+    const int q = k * kThreads + tid;
+    hb[k] = 0;
+    if (q >= H) continue;
+    hb[k] = cntp[k * 32 + warp] + __popc(hm[k] & lanes_before);
+    if (!hit[k]) {
+      const bool corrupt = f[k] == -2;
+      if (corrupt) my_flags |= HS_ST_BAD_LRU_SLOT;
+      evl[q - hb[k]] = (corrupt ? 0x10000 : 0) | (sl[k] & 0xFFFF);
+    }
+  }
+
+  __syncthreads();  // the evictables are listed before the misses take them
   const int NH = misc[kMiscHits];
   const int M = misc[kMiscMisses];
   const int E = H - NH;
