@@ -696,7 +696,6 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
         if (pr >= 0 && pr < p.pool_num_rows) {
           c = kMiss;
           miss = true;
-          if (i >= e0 && i < e1) jsrc[i - e0] = pr;  // compacted below
         } else {
           c = kBadPool;
           my_flags |= HS_ST_BAD_POOL_ROW;
@@ -737,19 +736,15 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
   const int E = H - NH;
   const int my_first_miss = e0 < K ? cnte[e0 >> 5] : M;
   // Only my own entries: their chunks are whole and 32-aligned, so a warp's
-  // ballot covers one chunk.
-  int64_t my_pr = 0;
+  // ballot covers one chunk.  A miss's pool row is still in prs.
   for (int base = e0; base < e1; base += kThreads) {
     const int i = base + tid;
     const bool mine = i < e1;
     const int8_t c = mine ? code[i] : kInvalid;
     const unsigned m = __ballot_sync(kFullMask, c == kMiss);
-    if (mine) {
-      my_pr = c == kMiss ? jsrc[i - e0] : 0;
-      if (p.miss_mask) p.miss_mask[b * p.mask_stride + i] = c == kMiss;
-    }
-    __syncthreads();  // jsrc is rewritten in compacted order below
+    if (mine && p.miss_mask) p.miss_mask[b * p.mask_stride + i] = c == kMiss;
     if (c == kMiss) {
+      const int64_t my_pr = prs[i];
       const int mm = cnte[i >> 5] + __popc(m & lanes_before);  // the row's mm-th miss
       const int32_t e = evl[mm];                               // takes the mm-th evictable
       int32_t d = -1;
