@@ -367,7 +367,6 @@ def run_headline(args, dev, rank, world, dist):
     # e2e leg inputs: continue the stream, pinned host copies (two more steps warm
     # the e2e graphs up before the timed window)
     n_e2e = min(args.steps, 64)
-    e2e_host = [w.next_topk().cpu().pin_memory() for _ in range(n_e2e + 2)]
     # two buffer sets: step k's copies overlap the neighbouring steps' swap-ins
     topk_dev = [torch.empty((NL, B, K), dtype=torch.int32, device=dev) for _ in range(2)]
     out_dev = [torch.empty((NL, B, K), dtype=torch.int32, device=dev) for _ in range(2)]
@@ -392,93 +391,106 @@ def run_headline(args, dev, rank, world, dist):
         torch.distributed.barrier()
     hits, misses = (int(x) for x in w.stats.cpu())
 
-    # e2e: every step uploads its top-k rows from pinned host memory, runs the
-    # step's 61 swap-ins and reads back the outputs and miss counts; uploads and
-    # read-backs run on their own streams, double-buffered, so step k's copies
-    # overlap steps k-1 and k+1 on the GPU (step k's read-back is enqueued after
-    # step k+1's replay).
-    with torch.cuda.stream(s):  # untimed: each e2e graph's first replay
-        for i in range(2):
-            topk_dev[i].copy_(e2e_host[i], non_blocking=True)
-            g_e2e[i].replay()
-            out_host[i].copy_(out_dev[i], non_blocking=True)
-    torch.cuda.synchronize()
-    w.stats.zero_()
-    torch.cuda.synchronize()
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    comp_done = [None, None]  # the step that last used buffer i finished computing
-    out_done = [None, None]   # ... and its outputs reached the host
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    marks = []  # per step: (compute start, compute end, outputs on the host)
-    wall0 = time.perf_counter()
-    e0.record(s)
-    s_in.wait_event(e0)
-    s_out.wait_event(e0)
-    def read_back(i):
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(comp_done[i])
-            out_host[i].copy_(out_dev[i], non_blocking=True)
-            miss_host[i].copy_(miss_dev[i], non_blocking=True)
-            out_done[i] = ev()
-            out_done[i].record(s_out)
+    def e2e_window():
+        """One e2e window of n_e2e steps with fresh inputs (the stream goes on)."""
+        e2e_host = [w.next_topk().cpu().pin_memory() for _ in range(n_e2e + 2)]
+        # e2e: every step uploads its top-k rows from pinned host memory, runs the
+        # step's 61 swap-ins and reads back the outputs and miss counts; uploads and
+        # read-backs run on their own streams, double-buffered, so step k's copies
+        # overlap steps k-1 and k+1 on the GPU (step k's read-back is enqueued after
+        # step k+1's replay).
+        with torch.cuda.stream(s):  # untimed: each e2e graph's first replay
+            for i in range(2):
+                topk_dev[i].copy_(e2e_host[i], non_blocking=True)
+                g_e2e[i].replay()
+                out_host[i].copy_(out_dev[i], non_blocking=True)
+        torch.cuda.synchronize()
+        w.stats.zero_()
+        torch.cuda.synchronize()
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        comp_done = [None, None]  # the step that last used buffer i finished computing
+        out_done = [None, None]   # ... and its outputs reached the host
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        marks = []  # per step: (compute start, compute end, outputs on the host)
+        wall0 = time.perf_counter()
+        e0.record(s)
+        s_in.wait_event(e0)
+        s_out.wait_event(e0)
+        def read_back(i):
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[i])
+                out_host[i].copy_(out_dev[i], non_blocking=True)
+                miss_host[i].copy_(miss_dev[i], non_blocking=True)
+                out_done[i] = ev()
+                out_done[i].record(s_out)
 
-    c0s, ups = [], []
-    for k_, hb in enumerate(e2e_host[2:]):
-        i = k_ % 2
-        with torch.cuda.stream(s_in):
-            if comp_done[i] is not None:
-                s_in.wait_event(comp_done[i])  # the buffer's previous step has read it
-            u0 = ev()
-            u0.record(s_in)
-            topk_dev[i].copy_(hb, non_blocking=True)
-            up = ev()
-            up.record(s_in)
-            ups.append((u0, up))
-        with torch.cuda.stream(s):  # a graph replays on the current stream
-            s.wait_event(up)
-            if out_done[i] is not None:
-                s.wait_event(out_done[i])  # the buffer's previous outputs have left
-            c0 = ev()
-            c0.record(s)
-            g_e2e[i].replay()
-            comp_done[i] = ev()
-            comp_done[i].record(s)
-        c0s.append(c0)
-        # The previous step's read-back is enqueued after this step's replay: a
-        # copy waiting on a step must not sit ahead of the next step's kernels
-        # where the streams share a hardware queue.
-        if k_ > 0:
-            read_back(1 - i)
-            marks.append((c0s[k_ - 1], comp_done[1 - i], out_done[1 - i]))
-    last = (len(e2e_host) - 3) % 2
-    read_back(last)
-    marks.append((c0s[-1], comp_done[last], out_done[last]))
-    enqueue_ms = (time.perf_counter() - wall0) * 1e3
-    for d in out_done:
-        if d is not None:
-            s.wait_event(d)
-    e1.record(s)
-    torch.cuda.synchronize()
-    t_e2e = e0.elapsed_time(e1) / 1e3
-    wall_e2e = time.perf_counter() - wall0
-    # where the window went: the steps' compute, the GPU idle between steps, read-backs
-    comp_us = [a.elapsed_time(b) * 1e3 for a, b, _ in marks]
-    idle_us = e0.elapsed_time(marks[0][0]) * 1e3 + sum(
-        marks[k - 1][1].elapsed_time(marks[k][0]) * 1e3 for k in range(1, len(marks)))
-    d2h_us = [b.elapsed_time(c) * 1e3 for _, b, c in marks]
-    h2d_us = [a.elapsed_time(b) * 1e3 for a, b in ups]
-    # GPU idle before a step's compute while its upload was still running
-    wait_up_us = sum(max(0.0, marks[k - 1][1].elapsed_time(ups[k][1]) * 1e3)
-                     for k in range(1, len(marks)))
-    e2e_detail = dict(compute_us_per_step_median=statistics.median(comp_us),
-                      compute_us_per_step_max=max(comp_us),
-                      idle_us_between_steps_total=idle_us,
-                      readback_us_median=statistics.median(d2h_us), readback_us_max=max(d2h_us),
-                      upload_us_median=statistics.median(h2d_us), upload_us_max=max(h2d_us),
-                      idle_waiting_for_upload_us_total=wait_up_us,
-                      host_enqueue_ms=enqueue_ms)
-    e2e_misses = int(w.stats[1].item())
+        c0s, ups = [], []
+        for k_, hb in enumerate(e2e_host[2:]):
+            i = k_ % 2
+            with torch.cuda.stream(s_in):
+                if comp_done[i] is not None:
+                    s_in.wait_event(comp_done[i])  # the buffer's previous step has read it
+                u0 = ev()
+                u0.record(s_in)
+                topk_dev[i].copy_(hb, non_blocking=True)
+                up = ev()
+                up.record(s_in)
+                ups.append((u0, up))
+            with torch.cuda.stream(s):  # a graph replays on the current stream
+                s.wait_event(up)
+                if out_done[i] is not None:
+                    s.wait_event(out_done[i])  # the buffer's previous outputs have left
+                c0 = ev()
+                c0.record(s)
+                g_e2e[i].replay()
+                comp_done[i] = ev()
+                comp_done[i].record(s)
+            c0s.append(c0)
+            # The previous step's read-back is enqueued after this step's replay: a
+            # copy waiting on a step must not sit ahead of the next step's kernels
+            # where the streams share a hardware queue.
+            if k_ > 0:
+                read_back(1 - i)
+                marks.append((c0s[k_ - 1], comp_done[1 - i], out_done[1 - i]))
+        last = (len(e2e_host) - 3) % 2
+        read_back(last)
+        marks.append((c0s[-1], comp_done[last], out_done[last]))
+        enqueue_ms = (time.perf_counter() - wall0) * 1e3
+        for d in out_done:
+            if d is not None:
+                s.wait_event(d)
+        e1.record(s)
+        torch.cuda.synchronize()
+        t_e2e = e0.elapsed_time(e1) / 1e3
+        wall_e2e = time.perf_counter() - wall0
+        # where the window went: the steps' compute, the GPU idle between steps, read-backs
+        comp_us = [a.elapsed_time(b) * 1e3 for a, b, _ in marks]
+        idle_us = e0.elapsed_time(marks[0][0]) * 1e3 + sum(
+            marks[k - 1][1].elapsed_time(marks[k][0]) * 1e3 for k in range(1, len(marks)))
+        d2h_us = [b.elapsed_time(c) * 1e3 for _, b, c in marks]
+        h2d_us = [a.elapsed_time(b) * 1e3 for a, b in ups]
+        # GPU idle before a step's compute while its upload was still running
+        wait_up_us = sum(max(0.0, marks[k - 1][1].elapsed_time(ups[k][1]) * 1e3)
+                         for k in range(1, len(marks)))
+        e2e_detail = dict(compute_us_per_step_median=statistics.median(comp_us),
+                          compute_us_per_step_max=max(comp_us),
+                          idle_us_between_steps_total=idle_us,
+                          readback_us_median=statistics.median(d2h_us), readback_us_max=max(d2h_us),
+                          upload_us_median=statistics.median(h2d_us), upload_us_max=max(h2d_us),
+                          idle_waiting_for_upload_us_total=wait_up_us,
+                          host_enqueue_ms=enqueue_ms)
+        e2e_misses = int(w.stats[1].item())
+        return t_e2e, wall_e2e, e2e_misses, e2e_detail
+
+    # Three windows; the one with the median time is reported, all three are
+    # listed: on this machine another tenant's host traffic can slow a whole
+    # window's uploads several-fold without changing the compute.
+    wins = [e2e_window() for _ in range(3)]
+    mid = sorted(range(len(wins)), key=lambda k_: wins[k_][0])[len(wins) // 2]
+    t_e2e, wall_e2e, e2e_misses, e2e_detail = wins[mid]
+    e2e_detail = dict(e2e_detail, windows_us_per_step=[x[0] / n_e2e * 1e6 for x in wins],
+                      window="median of 3 windows by time, each with its own inputs")
     smi_summary = stop_smi(smi, smi_f, smi_path)
 
     # the same decode step with every launch waiting for the one before it
@@ -1354,7 +1366,8 @@ def main():
                  how="every step: pinned-host top-k -> device, the step's 61 swap-ins "
                      "(CUDA graph through the C ABI), out rows and miss counts -> pinned host; "
                      "uploads and read-backs on their own streams, double-buffered, so they "
-                     "overlap the neighbouring steps' swap-ins"),
+                     "overlap the neighbouring steps' swap-ins; three windows of `steps` steps "
+                     "with their own inputs, the median one reported (all three in detail)"),
         sequential=dict(us_per_decode_step=h["t_seq"] / h["seq_steps"] * 1e6,
                         value=h["seq_misses"] / h["t_seq"], unit="rows/s",
                         steps=h["seq_steps"],
