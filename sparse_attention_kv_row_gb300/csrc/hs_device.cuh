@@ -155,6 +155,12 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint3
       : "memory");
 }
 
+// A hint to bring [src, src + bytes) of global memory into L2 (no data
+// returned, nothing to wait for).  src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // A bulk copy shared -> global, in this thread's current bulk group.
 // dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint32_t bytes) {

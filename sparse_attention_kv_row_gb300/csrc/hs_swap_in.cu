@@ -155,6 +155,7 @@ struct SwapInParams {
   int32_t entry_bits;       // bits of a top-k entry index in the packed hash
   int64_t max_seq_len;      // 0, or a bound on every row's sequence length
   int32_t copy_width;       // 16, 4 or 1 bytes per copy chunk
+  int32_t prefetch_rows;    // device pools, 16-byte rows: a miss's row is prefetched into L2
   int32_t fail_rank;        // self-test: this cluster rank's wait gives up at once (-1: none)
   int32_t fail_wait;        // self-test: 0 = the state-row wait, 1 = the top-k-row wait
 };
@@ -696,6 +697,11 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
         if (pr >= 0 && pr < p.pool_num_rows) {
           c = kMiss;
           miss = true;
+          if (p.prefetch_rows && i >= e0 && i < e1) {  // in L2 by the time P6 copies it
+            bulk_prefetch_l2(p.pool_k + pr * p.row_bytes, static_cast<uint32_t>(p.row_bytes));
+            if (p.pool_v != nullptr)
+              bulk_prefetch_l2(p.pool_v + pr * p.row_bytes, static_cast<uint32_t>(p.row_bytes));
+          }
         } else {
           c = kBadPool;
           my_flags |= HS_ST_BAD_POOL_ROW;
@@ -944,6 +950,7 @@ hs_err swap_in_launch(const hs_swap_in_args* a, hs_stream_t stream, int fail_ran
   p.entry_bits = dv.entry_bits;
   p.max_seq_len = a->max_seq_len;
   p.copy_width = dv.copy_width;
+  p.prefetch_rows = dv.copy_width == 16 && dv.pools_device;
   p.fail_rank = fail_rank == -1 ? -1 : (fail_rank < 0 ? C - 1 : fail_rank % C);
   p.fail_wait = fail_wait;
 
@@ -1058,6 +1065,8 @@ hs_err derive_swap_in(const hs_swap_in_args* a, const char* who, SwapInDerived* 
                           reinterpret_cast<uintptr_t>(a->hot_v) |
                           static_cast<uintptr_t>(a->row_bytes);
   d->copy_width = (align & 15) == 0 ? 16 : ((align & 3) == 0 ? 4 : 1);
+  d->pools_device = (pk == MemKind::kDevice || pk == MemKind::kManaged) &&
+                    (pv == MemKind::kDevice || pv == MemKind::kManaged);
   const uint64_t cpr = static_cast<uint64_t>(a->row_bytes) / d->copy_width;
   if (cpr * static_cast<uint64_t>(a->top_k) >= (1ull << 32))
     return fail(HS_ERR_UNSUPPORTED, "%s: top_k * row chunks must be < 2^32", who);

@@ -191,6 +191,7 @@ struct SwapInDerived {
   int entry_bits;          // bits of a top-k entry index
   bool packed;             // the packed request hash is usable
   bool tables;             // block tables given
+  bool pools_device;       // both pools in device (or managed) memory
   FastDiv div_src_bs, div_res_bs;
 };
 
