@@ -157,6 +157,7 @@ struct RowCommon {
   int64_t src_bt_stride, res_bt_stride;
   int32_t src_bt_blocks, src_bs, res_bt_blocks, res_bs, res_null;
   int32_t entry_bits, copy_width, fail_wait;
+  int32_t prefetch_rows;  // device pools, 16-byte rows: a miss's row is prefetched into L2
   uint32_t chunks_per_row;
   FastDiv div_src_bs, div_res_bs, div_chunks, div_batch;
   RowLayout lay;
@@ -729,6 +730,11 @@ __global__ void __launch_bounds__(kRowThreads, 2)
         if (pr >= 0 && pr < p.pool_num_rows) {
           c = kMiss;
           miss = true;
+          if (p.prefetch_rows) {  // in L2 by the time P6 copies it
+            bulk_prefetch_l2(q.pool_k + pr * p.row_bytes, static_cast<uint32_t>(p.row_bytes));
+            if (q.pool_v != nullptr)
+              bulk_prefetch_l2(q.pool_v + pr * p.row_bytes, static_cast<uint32_t>(p.row_bytes));
+          }
         } else {
           c = kBadPool;
           my_flags |= HS_ST_BAD_POOL_ROW;
@@ -982,10 +988,12 @@ hs_err swap_in_rows_launch(const hs_swap_in_args* layers, int num_layers, hs_str
   // The copy width is the narrowest any layer's buffers allow.
   SwapInDerived dv{};
   int width = 16;
+  bool pools_device = true;
   for (int l = 0; l < num_layers; ++l) {
     hs_err err = derive_swap_in(&layers[l], who, &dv);
     if (err != HS_OK) return err;
     width = dv.copy_width < width ? dv.copy_width : width;
+    pools_device = pools_device && dv.pools_device;
   }
   DeviceInfo dev;
   hs_err err = current_device(&dev);
@@ -1025,6 +1033,7 @@ hs_err swap_in_rows_launch(const hs_swap_in_args* layers, int num_layers, hs_str
   c.res_null = a.res_null_block;
   c.entry_bits = dv.entry_bits;
   c.copy_width = width;
+  c.prefetch_rows = width == 16 && pools_device;
   c.fail_wait = fail_wait;
   c.chunks_per_row = static_cast<uint32_t>(a.row_bytes / width);
   c.div_src_bs = dv.div_src_bs;
