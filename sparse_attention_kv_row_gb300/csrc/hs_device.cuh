@@ -155,11 +155,6 @@ __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint3
       : "memory");
 }
 
-// A hint to bring the cache line holding *p (global memory) into L2.
-__device__ __forceinline__ void prefetch_line_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // A hint to bring [src, src + bytes) of global memory into L2 (no data
 // returned, nothing to wait for).  src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {

@@ -477,16 +477,6 @@ __global__ void __launch_bounds__(kThreads, 1) swap_in_kernel(const SwapInParams
     timeout_tail(p, b, j, C, bar);
     return;
   }
-  // My own ids' pool-row entries go into L2 now, so the candidates' lookups
-  // after the walk hit L2 (the hits' entries come along needlessly: a few KB
-  // against a memory round trip on the launch's chain).
-  if (p.prefetch_rows && p.src_bt == nullptr && p.pool_rows != nullptr) {
-    const int64_t* prow = p.pool_rows + r * p.pool_rows_stride;
-    for (int i = e0 + tid; i < e1; i += kThreads) {
-      const int32_t t = ids[i];
-      if (static_cast<uint32_t>(t) < lim && t < p.pool_rows_cols) prefetch_line_l2(prow + t);
-    }
-  }
   // Block tables: each valid id's entries are loaded with LDGSTS into prs
   // (free until P2's candidate prefetch), read back after the hash insert by
   // the thread that loaded them.
