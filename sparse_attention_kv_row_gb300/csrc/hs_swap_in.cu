@@ -28,13 +28,16 @@
 //               when an id repeats does a second pass make its smallest entry
 //               index canonical;
 //   P2 walk     every position probes its slot's token; the lowest position
-//               holding a wanted token claims the entry (atomicMin);
-//   P3 hits     position-ordered ballot/popc + one warp scan of chunk counts:
-//               hit ranks, and the evictables in LRU order;
-//   P4 misses   entries in top-k order: candidates look up their pool row; the
-//               same scan gives each miss its rank m, and the m-th miss takes
-//               the m-th evictable; the CTA owning the entry emits its output,
-//               records the slot's new token and queues the row copy;
+//               holding a wanted token claims the entry (atomicMin); the
+//               candidates then look up their pool rows (LDGSTS);
+//   P3/P4 count position-ordered ballot/popc gives hits per chunk; entries
+//               in top-k order are classified (a miss's pool row is then
+//               prefetched into L2 by the CTA owning it) and ballot/popc gives
+//               misses per chunk; two warps scan both at once: hit ranks, the
+//               evictables in LRU order, and each miss's rank m;
+//   P4 assign   the m-th miss takes the m-th evictable; the CTA owning the
+//               entry emits its output, records the slot's new token and
+//               queues the row copy;
 //   P5 LRU      each CTA writes its positions' places in the new order
 //               [stale evictables][misses][hits];
 //   P6 copy     (miss, 16-byte chunk) work items over all threads: read-only
@@ -42,9 +45,10 @@
 //               stores into the hot buffer.
 //
 // With HS_OVERLAP_PREV the launch may begin while the preceding kernel in the
-// stream is still running: P0 and the state half of P1 read only request
-// metadata and state rows, and the grid-dependency wait sits right before the
-// top-k row is read; nothing is written to global memory before it.
+// stream is still running: before the grid-dependency wait (right after the
+// state's copies are issued) it reads only request metadata and state rows;
+// the top-k row is read after the wait, and nothing is written to global
+// memory before it.
 #include <cuda_runtime.h>
 
 #include <climits>
