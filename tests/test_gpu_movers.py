@@ -27,7 +27,12 @@ def _hs():
     return hs
 
 
+# 16-byte rows up to 2048 B take the form that loads a row with its slot
+# index (U = 1, 2 or 4 chunks per lane; 400 and 656 B leave some lanes a
+# chunk short), longer or unaligned rows the general one.
 @pytest.mark.parametrize("S,n,rows,with_v", [(2048, 4096, 9000, True), (656, 333, 1000, False),
+                                              (400, 900, 2000, True), (512, 700, 1600, False),
+                                              (4096, 300, 1000, True),
                                               (132, 1000, 5000, True), (17, 77, 300, True),
                                               (4, 3000, 3001, False)])
 def test_store_kv_parity(dev, S, n, rows, with_v):
